@@ -1,0 +1,445 @@
+"""Benchmark of the Fibonacci-offset sparse attention hot path on B300.
+
+One step = one pass of the whole path over one batch: the offset tables, the forward
+(window band + offsets, online softmax) and, for the training-step workload, the
+backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
+(B=8, H=8, T=1024, d=64), W=64, coprime reassignment (l -> 5l mod 16) of the linear
+stagger alpha 0.5 -> 2.0, bf16, forward + backward.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
+(weak scaling: the (layer, batch, head) slices are independent, no collective on the
+data path); value = all ranks' query tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import fibattn_inputs as fi  # noqa: E402
+
+METRIC = "Fib-sparse attn fwd/bwd query-tokens/s (B·H·T) and % HBM roofline, 1×B300"
+UNIT = "query-tokens/s"
+
+# Algorithmic HBM bytes per query token (per (layer, b, h, t)) of each kernel: every
+# input row read once, every output row written once; the offset and band re-reads
+# are on-chip reuse, not compulsory traffic.
+ALGO_BYTES = {
+    "fwd_tc_bf16": 3 * 128 + 128 + 4,          # q, k, v in; o, lse out
+    "fwd_simt_bf16": 3 * 128 + 128 + 4,
+    "fwd_simt_f32": 3 * 256 + 256 + 4,
+    "bwd_delta_simt": 2 * 128 + 4,              # o, dO in; D out
+    "bwd_delta": 2 * 128 + 4,
+    "bwd_dq_simt": 4 * 128 + 8 + 128,           # q, k, v, dO, lse, D in; dq out
+    "bwd_dkdv_simt": 4 * 128 + 8 + 2 * 128,     # q, k, v, dO, lse, D in; dk, dv out
+    "bwd_fused_tc": 5 * 128 + 8 + 3 * 128,      # q, k, v, o, dO, lse, D in; dq, dk, dv out
+}
+# Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
+KERNEL_SRC = {
+    "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
+    "bwd_delta_simt": "simt.cu", "bwd_dq_simt": "simt.cu", "bwd_dkdv_simt": "simt.cu",
+    "bwd_delta": "bwd_tc.cu", "bwd_fused_tc": "bwd_tc.cu",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="c5", choices=["c5", "c4", "c2", "c3", "c3p"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def tokens(spec):
+    return spec["Lc"] * spec["B"] * spec["H"] * spec["T"]
+
+
+def src_hash(fn):
+    path = os.path.join(ROOT, "static_fibonacci_offset_fibattn_b300", "csrc", fn)
+    try:
+        with open(path, "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+def committed_traffic(kernel):
+    """Bytes per query token from the committed ncu summary, or None when absent or when
+    the kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = src_hash(KERNEL_SRC.get(kernel, ""))
+    for line in open(path):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("src") == want:
+            return float(f["bytes_per_token"])
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(a, spec, world, rank, local):
+    import static_fibonacci_offset_fibattn_b300 as fa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L = fa.lib()
+    sched = fa.Schedule(**spec["sched"])
+    inp = fi.workload_inputs(a.workload)
+    d_in = {n: t.to(dev) for n, t in inp.items()}
+    W = spec["W"]
+    train = "bwd" in spec["passes"]
+    o = torch.empty_like(d_in["q"])
+    lse = torch.empty(d_in["q"].shape[:-1], dtype=torch.float32, device=dev)
+    if train:
+        dq, dk, dv = (torch.empty_like(d_in["q"]) for _ in range(3))
+        delta = torch.empty_like(lse)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x):
+        fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
+        if train:
+            fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched, dq=dq, dk=dk, dv=dv,
+                   delta=delta)
+
+    for _ in range(a.warmup):
+        step(d_in)
+        flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+    fa.poll_device_error(dev)
+
+    # ---- timed region (device time, CUDA events on the launch stream; L2 flushed between
+    # steps outside the event pairs)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    L.fibattn_profile_read(None, 0, None, None, 0)
+    L.fibattn_profile_enable(1)
+    n0 = L.fibattn_launch_count()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(a.steps)]
+    with Clocks(clock_index(local)) as clk:
+        for s, e in evs:
+            s.record(stream)
+            step(d_in)
+            e.record(stream)
+            flush.fill_(1.0)
+        torch.cuda.synchronize(dev)
+    launches = L.fibattn_launch_count() - n0
+    L.fibattn_profile_enable(0)
+    names = ctypes.create_string_buffer(64 * 32)
+    tot = (ctypes.c_double * 32)()
+    cnt = (ctypes.c_int64 * 32)()
+    nk = L.fibattn_profile_read(names, 64, tot, cnt, 32)
+    per_kernel = {}
+    for i in range(min(nk, 32)):
+        nm = names.raw[i * 64:(i + 1) * 64].split(b"\0")[0].decode()
+        if cnt[i]:
+            per_kernel[nm] = (tot[i], int(cnt[i]))
+    if world > 1:
+        torch.distributed.barrier()
+    fa.poll_device_error(dev)
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / a.steps
+    value = world * tokens(spec) / (ms_per_step / 1e3)
+
+    # ---- roofline of the dominant kernel
+    hbm, peak_kind = peaks()
+    dom = max(per_kernel, key=lambda k: per_kernel[k][0]) if per_kernel else None
+    roof = None
+    if dom:
+        ms, n = per_kernel[dom]
+        per_launch_tokens = tokens(spec) / max(1, math.ceil(spec["Lc"] / 16))
+        algo = ALGO_BYTES.get(dom, 0) * per_launch_tokens
+        avg_s = ms / n / 1e3
+        achieved = algo / avg_s / 1e9
+        traffic_pt = committed_traffic(dom)
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+                "frac": round(achieved / hbm, 4),
+                "traffic": None if traffic_pt is None else round(traffic_pt * per_launch_tokens),
+                "algorithmic_bytes_per_launch": int(algo),
+                "avg_launch_us": round(avg_s * 1e6, 2),
+                "share_of_step": round(ms / total_ms if world == 1 else ms / sum(step_ms), 4)}
+    kernels = {k: {"avg_us": round(v[0] / v[1] * 1e3, 2), "launches_per_step": v[1] / a.steps,
+                   "share": round(v[0] / sum(step_ms), 4)} for k, v in per_kernel.items()}
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region
+    e2e = None
+    if not a.no_e2e:
+        e2e = run_e2e(fa, a, spec, inp, sched, dev, stream, world)
+
+    out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec["dtype"],
+           "data": "synthetic (seeded N(0,1)*scale inputs shaped like the pages' model; no dataset)",
+           "config": {"workload": f"{a.workload}: {spec['desc']}", "layers": spec["Lc"],
+                      "B": spec["B"], "H": spec["H"], "T": spec["T"], "d_head": spec["d"],
+                      "W": spec["W"], "schedule": spec["sched"], "passes": list(spec["passes"]),
+                      "parallelism": f"replicas x{world} (independent batches, no collective)",
+                      "l2": "inputs larger than L2 and L2 flushed between steps (outside the "
+                            "timed event pairs)"},
+           "roofline": roof, "kernels": kernels, "gpu_launches": int(launches),
+           "clocks": clk.summary(), "e2e": e2e}
+    return out
+
+
+def clock_index(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [p for p in vis.split(",") if p.strip()]
+        if local < len(parts) and parts[local].strip().isdigit():
+            return int(parts[local])
+    return local
+
+
+def run_e2e(fa, a, spec, inp, sched, dev, stream, world):
+    pinned = {n: t.pin_memory() for n, t in inp.items()}
+    W = spec["W"]
+    train = "bwd" in spec["passes"]
+    outs_host = {}
+    shapes = {"o": inp["q"].shape, "lse": inp["q"].shape[:-1]}
+    if train:
+        shapes.update(dq=inp["q"].shape, dk=inp["q"].shape, dv=inp["q"].shape)
+    for n, shp in shapes.items():
+        dt = torch.float32 if n == "lse" else inp["q"].dtype
+        outs_host[n] = torch.empty(shp, dtype=dt).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+
+    def step():
+        x = {n: t.to(dev, non_blocking=True) for n, t in pinned.items()}
+        o, lse = fa.fwd(x["q"], x["k"], x["v"], W, sched)
+        res = {"o": o, "lse": lse}
+        if train:
+            dq, dk, dv = fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched)
+            res.update(dq=dq, dk=dk, dv=dv)
+        for n, t in res.items():
+            outs_host[n].copy_(t, non_blocking=True)
+
+    steps = max(3, min(a.steps, 10))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(world * tokens(spec) / (ms / steps / 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(ms / steps, 3)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_sample(spec, n_slices, n_threads=0):
+    """Run the oracle (as it stands) on n_slices (layer, b, h) slices of the workload.
+    Returns (seconds, query tokens processed, threads used)."""
+    import numpy as np
+    from fractions import Fraction
+
+    import oracle
+
+    sc = spec["sched"]
+    T, W = spec["T"], spec["W"]
+    layers = sorted({(i * 7) % spec["Lc"] for i in range(n_slices)})
+    name = [k for k, v in fi.WORKLOADS.items() if v is spec][0]
+    inp = fi.workload_inputs(name, layers=layers)
+    per_layer = {l: [] for l in layers}
+    for i in range(n_slices):
+        l = layers[i % len(layers)]
+        per_layer[l].append(((i // len(layers)) % spec["B"], (i * 3) % spec["H"]))
+    kw_of = lambda: ({"alpha": Fraction(*sc["alpha"])} if sc["kind"] == "fixed" else
+                     {"alpha_min": Fraction(*sc["alpha_min"]), "alpha_max": Fraction(*sc["alpha_max"]),
+                      "coprime_c": sc.get("coprime_c", 7)})
+    f64 = lambda t: t.to(torch.float64).numpy()
+    threads = oracle.threads(n_threads)
+    t0 = time.perf_counter()
+    done = 0
+    for li, l in enumerate(layers):
+        tab = oracle.layer_table(sc["base"], sc["kind"], l, sc["n_layers"], W, T,
+                                 sc.get("base_max", 0), **kw_of())
+        picks = per_layer[l]
+        if not picks:
+            continue
+        g = lambda n: np.stack([f64(inp[n][li, b, h]) for b, h in picks])
+        if "bwd" in spec["passes"]:
+            oracle.bwd(g("q"), g("k"), g("v"), g("dO"), W, tab, None, n_threads)
+        else:
+            oracle.fwd(g("q"), g("k"), g("v"), W, tab, None, n_threads)
+        done += len(picks) * T
+    return time.perf_counter() - t0, done, threads
+
+
+def calibrate_slices(spec, target_s):
+    """Slices of oracle work that take about target_s seconds on this host."""
+    sec, toks, _ = oracle_sample(spec, 4)
+    per_slice = sec / 4
+    return max(1, int(target_s / max(per_slice, 1e-6)))
+
+
+def run_reference(a, spec, world, rank):
+    if rank != 0:
+        return None
+    n = calibrate_slices(spec, 6.0)
+    for _ in range(a.warmup):
+        oracle_sample(spec, max(1, n // 8))
+    secs, toks = 0.0, 0
+    for _ in range(a.steps):
+        s, t, threads = oracle_sample(spec, n)
+        secs += s
+        toks += t
+    value = toks / secs
+    sample = (f"{n} (layer,b,h) slices of T={spec['T']} per step "
+              f"({'fwd+bwd' if 'bwd' in spec['passes'] else 'fwd'}, fp64, OpenMP over slices)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+            "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": round(secs / a.steps * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same seeded inputs as the GPU arm)",
+            "config": {"workload": f"{a.workload}: {spec['desc']}", "layers": spec["Lc"],
+                       "B": spec["B"], "H": spec["H"], "T": spec["T"], "d_head": spec["d"],
+                       "W": spec["W"], "schedule": spec["sched"]},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    a = parse()
+    world, rank, local = dist_env()
+    spec = fi.WORKLOADS[a.workload]
+    if a.impl == "reference":
+        out = run_reference(a, spec, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out = run_ours(a, spec, world, rank, local)
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        n = calibrate_slices(spec, 15.0)
+        secs, toks, threads = oracle_sample(spec, n)
+        out["cpu_baseline"] = {
+            "value": round(toks / secs, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} (layer,b,h) slices of T={spec['T']} "
+                      f"({'fwd+bwd' if 'bwd' in spec['passes'] else 'fwd'}, fp64, OpenMP), "
+                      f"{secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

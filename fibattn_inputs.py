@@ -47,3 +47,60 @@ def draw_layers(n_layers: int, slice_shape, seed, scale: float, dtype: str = "bf
 def to_f64(t: torch.Tensor):
     """Exact upcast of a (possibly bf16) CPU tensor to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+# Workloads shaped like the pages' model (hidden 512 = 8 heads x 64, 16 layers,
+# trained length 1024 and 4x = 4096). Plain data: shapes, seeds, scales, schedules.
+# 'sched' keys follow the library's Schedule fields; 'seed' is an int (one draw shared
+# by every layer, stored in distinct per-layer buffers) or 'per_layer:<s0>' (seed s0 + l).
+WORKLOADS = {
+    "c1": dict(desc="single sparse-attention layer, fp32", dtype="f32", Lc=1, B=1, H=2, T=256,
+               d=64, W=16, seed=0, scale=1.0, names=("q", "k", "v"), passes=("fwd",),
+               sched=dict(kind="fixed", base="fib", alpha=(1, 1), n_layers=1)),
+    "c2": dict(desc="one layer of the 60M model, bf16", dtype="bf16", Lc=1, B=8, H=8, T=1024,
+               d=64, W=64, seed=1, scale=0.125, names=("q", "k", "v"), passes=("fwd",),
+               sched=dict(kind="fixed", base="fib", alpha=(1, 1), n_layers=1)),
+    "c3": dict(desc="16-layer stack, linear stagger 0.5->2.0, bf16", dtype="bf16", Lc=16, B=8,
+               H=8, T=1024, d=64, W=64, seed="per_layer:2", scale=0.125, names=("q", "k", "v"),
+               passes=("fwd",),
+               sched=dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
+                          n_layers=16)),
+    "c3p": dict(desc="16-layer stack, power-of-two control (alpha = 1), bf16", dtype="bf16",
+                Lc=16, B=8, H=8, T=1024, d=64, W=64, seed="per_layer:2", scale=0.125,
+                names=("q", "k", "v"), passes=("fwd",),
+                sched=dict(kind="fixed", base="pow2", alpha=(1, 1), n_layers=16)),
+    "c4": dict(desc="4x length extrapolation, 16 layers, linear stagger 0.5->2.0, bf16",
+               dtype="bf16", Lc=16, B=2, H=8, T=4096, d=64, W=64, seed=3, scale=0.125,
+               names=("q", "k", "v"), passes=("fwd",),
+               sched=dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
+                          n_layers=16)),
+    "c5": dict(desc="training step fwd+bwd, 16 layers, coprime (5l mod 16) of the linear "
+                    "stagger 0.5->2.0, bf16", dtype="bf16", Lc=16, B=8, H=8, T=1024, d=64,
+               W=64, seed=4, scale=0.125, names=("q", "k", "v", "dO"), passes=("fwd", "bwd"),
+               sched=dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
+                          n_layers=16, coprime_c=5)),
+}
+
+
+def seed_of(spec):
+    s = spec["seed"]
+    if isinstance(s, str) and s.startswith("per_layer:"):
+        s0 = int(s.split(":")[1])
+        return lambda l: s0 + l
+    return int(s)
+
+
+def workload_inputs(name: str, layers=None, **override):
+    """CPU tensors [Lc, B, H, T, d] of a named workload (optionally only `layers`)."""
+    spec = dict(WORKLOADS[name], **override)
+    shape = (spec["B"], spec["H"], spec["T"], spec["d"])
+    seed = seed_of(spec)
+    Lc = spec["Lc"]
+    if layers is None:
+        layers = list(range(Lc))
+    if callable(seed):
+        per = [draw(shape, seed(l), spec["scale"], spec["dtype"], spec["names"]) for l in layers]
+    else:
+        one = draw(shape, seed, spec["scale"], spec["dtype"], spec["names"])
+        per = [{n: t.clone() for n, t in one.items()} for _ in layers]
+    return {n: torch.stack([p[n] for p in per]).contiguous() for n in spec["names"]}

@@ -1,0 +1,187 @@
+/*
+ * fibattn.h -- C ABI of the B300 (sm_103a) Fibonacci-offset sparse attention library.
+ *
+ * The operation ("Depth-Staggered Fibonacci Spacing for Sparse Attention: Static
+ * Schedules Beat Learned Dilation and Extrapolate Where Dense Attention Fails",
+ * gist.science explainer, Metodologia / Arquitetura e Mecanismo de Atencao):
+ * causal softmax attention in which query i of layer l attends
+ *     S_i = { j : 0 <= i - j < W }  U  { i - o : o in O_l, i - o >= 0 }
+ * where O_l is the layer's offset table: the base offsets F (Fibonacci
+ * 1, 2, 3, 5, ..., 987, or the power-of-two control 2^k) scaled by the layer's
+ * alpha_l and rounded, alpha_l coming from a static per-layer schedule
+ * (Metodologia / Variaveis Experimentais and Controles).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense, contiguous, row-major [Lc][B][H][T][d] (Lc = layers in
+ *     the call); lse and delta are [Lc][B][H][T] float32, natural log. Call-layer c
+ *     uses schedule layer (layer0 + c).
+ *   - The caller owns every buffer; the library allocates no device memory apart
+ *     from a 4-byte device error word. Device pointers must be 16-byte aligned.
+ *   - Work is enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns once launched; results are ready when the stream is.
+ *   - Nothing is printed. Errors are returned as fibattn_status; kernel-side
+ *     failures (a bounded wait that ran out) are latched in the device error word
+ *     and reported by fibattn_poll_device_error().
+ *   - d (head size) must be 64; dtype FIBATTN_F32 or FIBATTN_BF16, the same for
+ *     every q/k/v/o/dO/dq/dk/dv tensor of a call.
+ */
+#ifndef FIBATTN_H
+#define FIBATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols (the library is built with hidden visibility by default). */
+#if defined(FIBATTN_BUILD) && defined(__GNUC__)
+#define FIBATTN_API __attribute__((visibility("default")))
+#else
+#define FIBATTN_API
+#endif
+
+typedef enum {
+    FIBATTN_OK = 0,
+    FIBATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad schedule */
+    FIBATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (d != 64, unknown dtype) */
+    FIBATTN_ERR_CAPACITY = 3,    /* an offset table does not fit the given capacity */
+    FIBATTN_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
+    FIBATTN_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (device error word) */
+} fibattn_status;
+
+typedef enum { FIBATTN_BASE_FIB = 0, FIBATTN_BASE_POW2 = 1 } fibattn_base;
+typedef enum { FIBATTN_SCHED_FIXED = 0, FIBATTN_SCHED_LINEAR = 1, FIBATTN_SCHED_COPRIME = 2 } fibattn_sched;
+typedef enum { FIBATTN_F32 = 0, FIBATTN_BF16 = 1 } fibattn_dtype;
+
+/* An exact rational alpha = num / den; 1 <= num, den <= FIBATTN_RATIO_MAX. */
+typedef struct { int32_t num, den; } fibattn_ratio;
+#define FIBATTN_RATIO_MAX (1 << 20)
+#define FIBATTN_LAYERS_MAX (1 << 20)
+
+/*
+ * A per-layer alpha schedule (Metodologia / Variaveis Experimentais):
+ *   FIXED   : alpha_l = alpha for every layer.
+ *   LINEAR  : alpha_l = alpha_min + (alpha_max - alpha_min) * l / (n_layers - 1)
+ *             (n_layers = 1 gives alpha_min), the static linear stagger.
+ *   COPRIME : alpha_l = LINEAR alpha of layer (coprime_c * l mod n_layers); requires
+ *             gcd(coprime_c, n_layers) = 1, coprime_c >= 1 (the coprime reassignment).
+ * base      : FIBATTN_BASE_FIB (1, 2, 3, 5, ..., 987) or FIBATTN_BASE_POW2 (1, 2, 4, ...:
+ *             the power-of-two control of Metodologia / Controles).
+ * base_max  : 0 = default (Fibonacci stops at 987; powers of two run while the scaled
+ *             offset is <= T - 1); > 0 = largest base value used, for either base.
+ * n_layers  : L >= 1; every layer index passed to the library must be in [0, L).
+ * Offsets of layer l: o = floor(alpha_l * F + 1/2) (exact, round half up) for each base
+ * value F, kept when W <= o <= T - 1, ascending and without duplicates.
+ */
+typedef struct {
+    int32_t base;                  /* fibattn_base */
+    int32_t kind;                  /* fibattn_sched */
+    fibattn_ratio alpha;           /* FIXED */
+    fibattn_ratio alpha_min;       /* LINEAR, COPRIME */
+    fibattn_ratio alpha_max;       /* LINEAR, COPRIME */
+    int32_t n_layers;              /* L */
+    int32_t coprime_c;             /* COPRIME */
+    int64_t base_max;              /* 0 = default */
+} fibattn_schedule;
+
+/* Most offsets one layer's table may hold inside the kernels. */
+#define FIBATTN_MAX_OFFSETS 64
+
+/*
+ * Offset table of one layer, on the host (Metodologia / Arquitetura, "Escalonamento":
+ * target distance d_k = alpha * f_k). Writes *n_out entries to out[0..cap).
+ * Errors: INVALID_ARG (null, W < 1, T < 1, bad schedule or layer), CAPACITY (more than
+ * `cap` entries; *n_out then holds the needed count).
+ */
+FIBATTN_API fibattn_status fibattn_offsets(const fibattn_schedule* sched, int32_t layer, int32_t W, int32_t T,
+                               int32_t* out, int32_t cap, int32_t* n_out);
+
+/*
+ * The same tables built by a device kernel, for n_layers_call layers starting at layer0:
+ * d_tables is a device int32 [n_layers_call][FIBATTN_MAX_OFFSETS] (unused entries -1),
+ * d_counts a device int32 [n_layers_call]. Used to cross-check the device integer
+ * arithmetic bit-exactly against the host. Errors as fibattn_offsets (checked on the
+ * host first), plus CUDA.
+ */
+FIBATTN_API fibattn_status fibattn_offsets_device(const fibattn_schedule* sched, int32_t layer0,
+                                      int32_t n_layers_call, int32_t W, int32_t T,
+                                      int32_t* d_tables, int32_t* d_counts, void* cuda_stream);
+
+/*
+ * Forward (the attended set of Metodologia / Arquitetura; scores scale * q.k, softmax
+ * over S_i, output sum_j p_ij v_j):
+ *   q, k, v : [Lc][B][H][T][d] device, dtype `dtype` (RoPE, if any, already applied:
+ *             the pages apply it before the gather).
+ *   o       : [Lc][B][H][T][d] device, written, same dtype.
+ *   lse     : [Lc][B][H][T] float32 device, written: log sum_j exp(scale * q_i.k_j).
+ *   scale   : <= 0 selects 1/sqrt(d).
+ *   W >= 1 (W >= T gives dense causal attention). bf16 runs on the tcgen05 tensor-core
+ *   kernel; f32 on the SIMT fp32 kernel.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (a layer table above FIBATTN_MAX_OFFSETS),
+ * CUDA (launch failure).
+ */
+FIBATTN_API fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                           float scale, const fibattn_schedule* sched, int32_t layer0,
+                           int32_t n_layers_call, void* cuda_stream);
+
+/*
+ * Backward from the saved forward (the analytic gradient of softmax attention over S_i):
+ *   D_i = dO_i . o_i,  P_ij = exp(scale q_i.k_j - lse_i),  dS_ij = P_ij (dO_i . v_j - D_i),
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dO_i.
+ *   q, k, v, o, dO : inputs as in fibattn_fwd; lse : the forward's lse.
+ *   dq, dk, dv     : written (every element; no accumulation into old contents).
+ *   delta_ws       : float32 [Lc][B][H][T] device scratch owned by the caller (holds D).
+ * No atomics: each dk/dv row is summed by the one thread block that owns it.
+ * Errors as fibattn_fwd.
+ */
+FIBATTN_API fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           float* delta_ws, int32_t B, int32_t H, int32_t T, int32_t d,
+                           int32_t dtype, int32_t W, float scale, const fibattn_schedule* sched,
+                           int32_t layer0, int32_t n_layers_call, void* cuda_stream);
+
+/*
+ * The attended key sets of one layer, materialised by a device kernel from the same
+ * table and predicate the attention kernels use: d_mask is a device uint32
+ * [T][ceil(T/32)] bitmask, bit (j % 32) of word [i][j / 32] set iff j is in S_i.
+ * For testing only (O(T^2) memory). Errors as fibattn_offsets, plus CUDA.
+ */
+FIBATTN_API fibattn_status fibattn_keyset_debug(const fibattn_schedule* sched, int32_t layer, int32_t W,
+                                    int32_t T, uint32_t* d_mask, void* cuda_stream);
+
+/*
+ * Synchronises `cuda_stream`, then reads and clears the device error word.
+ * Returns OK, TIMEOUT (a kernel gave up a bounded wait and returned early; its
+ * outputs are undefined) or CUDA (a CUDA error is pending on the context).
+ */
+FIBATTN_API fibattn_status fibattn_poll_device_error(void* cuda_stream);
+
+/* Static English text for a status value (never NULL). */
+FIBATTN_API const char* fibattn_status_string(fibattn_status status);
+
+/*
+ * Kernel timing without a profiler. While enabled (on != 0), every kernel the library
+ * launches is bracketed by a pair of CUDA events recorded on the launch stream (the
+ * events are created and pooled by the library; no device memory is allocated).
+ * fibattn_profile_read synchronises the recorded events and, per kernel name, writes
+ * the summed device milliseconds and the number of launches since the previous read,
+ * then resets them. names is a char [cap][name_len] buffer (NUL-terminated names).
+ * Returns the number of kernel names known (may exceed cap).
+ */
+FIBATTN_API fibattn_status fibattn_profile_enable(int32_t on);
+FIBATTN_API int32_t fibattn_profile_read(char* names, int32_t name_len, double* total_ms,
+                                         int64_t* launches, int32_t cap);
+
+/* Kernels launched by the library since it was loaded (always counted). */
+FIBATTN_API int64_t fibattn_launch_count(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+FIBATTN_API int32_t fibattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FIBATTN_H */

@@ -1,0 +1,247 @@
+"""Python binding of libfibattn (B300 / sm_103a Fibonacci-offset sparse attention).
+
+Argument marshalling only: every step of the computation runs in the CUDA kernels
+behind the C ABI declared in include/fibattn.h. PyTorch provides device memory and
+the current stream. There is no CPU fallback: if the library is missing or the
+tensors are not on a CUDA device, these functions raise.
+
+Attention computed ("Depth-Staggered Fibonacci Spacing for Sparse Attention",
+gist.science explainer, Metodologia / Arquitetura e Mecanismo de Atencao): query i
+of layer l attends the window i-W+1..i plus i - o for every o in the layer's
+offset table, o = round(alpha_l * F) over the Fibonacci (or power-of-two) base.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass, field
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+__all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd",
+           "keyset_debug", "poll_device_error", "status_string", "lib", "library_path",
+           "FibSparseAttention", "MAX_OFFSETS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libfibattn.so")
+MAX_OFFSETS = 64
+
+OK, INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA_ERR, TIMEOUT = range(6)
+_BASES = {"fib": 0, "pow2": 1}
+_KINDS = {"fixed": 0, "linear": 1, "coprime": 2}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+class FibAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class _Ratio(ctypes.Structure):
+    _fields_ = [("num", ctypes.c_int32), ("den", ctypes.c_int32)]
+
+
+class _Sched(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_int32), ("kind", ctypes.c_int32), ("alpha", _Ratio),
+                ("alpha_min", _Ratio), ("alpha_max", _Ratio), ("n_layers", ctypes.c_int32),
+                ("coprime_c", ctypes.c_int32), ("base_max", ctypes.c_int64)]
+
+
+@dataclass(frozen=True)
+class Schedule:
+    """A per-layer alpha schedule; ratios are (numerator, denominator) pairs.
+
+    kind: 'fixed' (alpha everywhere), 'linear' (alpha_min -> alpha_max across
+    n_layers), 'coprime' (the linear alphas reassigned l -> coprime_c*l mod n_layers).
+    base: 'fib' (1, 2, 3, ..., 987) or 'pow2' (powers of two)."""
+    kind: str = "fixed"
+    base: str = "fib"
+    alpha: Tuple[int, int] = (1, 1)
+    alpha_min: Tuple[int, int] = (1, 2)
+    alpha_max: Tuple[int, int] = (3, 2)
+    n_layers: int = 1
+    coprime_c: int = 7
+    base_max: int = 0
+
+    def to_c(self) -> _Sched:
+        return _Sched(_BASES[self.base], _KINDS[self.kind], _Ratio(*self.alpha),
+                      _Ratio(*self.alpha_min), _Ratio(*self.alpha_max), int(self.n_layers),
+                      int(self.coprime_c), int(self.base_max))
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded C library (built in-tree; raises if it cannot be loaded or built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            from ._build import build
+            build()
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        sp = ctypes.POINTER(_Sched)
+        L.fibattn_offsets.argtypes = [sp, i32, i32, i32, ctypes.POINTER(i32), i32, ctypes.POINTER(i32)]
+        L.fibattn_offsets_device.argtypes = [sp, i32, i32, i32, i32, vp, vp, vp]
+        L.fibattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, sp, i32,
+                                  i32, vp]
+        L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                  i32, f32, sp, i32, i32, vp]
+        L.fibattn_keyset_debug.argtypes = [sp, i32, i32, i32, vp, vp]
+        L.fibattn_poll_device_error.argtypes = [vp]
+        L.fibattn_status_string.argtypes = [i32]
+        L.fibattn_status_string.restype = ctypes.c_char_p
+        L.fibattn_version.restype = i32
+        L.fibattn_profile_enable.argtypes = [i32]
+        L.fibattn_profile_enable.restype = i32
+        L.fibattn_profile_read.argtypes = [ctypes.c_char_p, i32, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_int64), i32]
+        L.fibattn_profile_read.restype = i32
+        L.fibattn_launch_count.argtypes = []
+        L.fibattn_launch_count.restype = ctypes.c_int64
+        for name in ("fibattn_offsets", "fibattn_offsets_device", "fibattn_fwd", "fibattn_bwd",
+                     "fibattn_keyset_debug", "fibattn_poll_device_error"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fibattn_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise FibAttnError(status, where)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def offsets(sched: Schedule, layer: int, W: int, T: int) -> list:
+    """Host-built offset table of one layer (fibattn_offsets)."""
+    cap = MAX_OFFSETS
+    buf = (ctypes.c_int32 * cap)()
+    n = ctypes.c_int32(0)
+    s = sched.to_c()
+    _check(lib().fibattn_offsets(ctypes.byref(s), layer, W, T, buf, cap, ctypes.byref(n)),
+           "fibattn_offsets")
+    return list(buf[: n.value])
+
+
+def offsets_device(sched: Schedule, layer0: int, n_layers: int, W: int, T: int,
+                   device="cuda") -> Tuple[torch.Tensor, torch.Tensor]:
+    """Device-built tables [n_layers, MAX_OFFSETS] (-1 padded) and counts [n_layers]."""
+    tab = torch.empty((n_layers, MAX_OFFSETS), dtype=torch.int32, device=device)
+    cnt = torch.empty((n_layers,), dtype=torch.int32, device=device)
+    s = sched.to_c()
+    _check(lib().fibattn_offsets_device(ctypes.byref(s), layer0, n_layers, W, T, _ptr(tab),
+                                        _ptr(cnt), _stream(tab)), "fibattn_offsets_device")
+    return tab, cnt
+
+
+def _shape(q: torch.Tensor):
+    if q.dim() == 5:
+        Lc, B, H, T, d = q.shape
+    elif q.dim() == 4:
+        Lc, (B, H, T, d) = 1, q.shape
+    else:
+        raise ValueError("q must be [B, H, T, d] or [Lc, B, H, T, d]")
+    return Lc, B, H, T, d
+
+
+def _check_tensors(ref: torch.Tensor, *ts):
+    if not ref.is_cuda:
+        raise ValueError("tensors must be on a CUDA device (there is no CPU path)")
+    if ref.dtype not in _DTYPES:
+        raise ValueError("dtype must be float32 or bfloat16")
+    for t in ts:
+        if t.device != ref.device or t.dtype != ref.dtype or t.shape != ref.shape:
+            raise ValueError("q/k/v/o/dO/dq/dk/dv must share device, dtype and shape")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, sched: Schedule,
+        layer0: int = 0, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+        lse: Optional[torch.Tensor] = None):
+    """Sparse attention forward; returns (o, lse). q/k/v: [Lc,B,H,T,64] or [B,H,T,64]."""
+    Lc, B, H, T, d = _shape(q)
+    o = torch.empty_like(q) if out is None else out
+    _check_tensors(q, k, v, o)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    s = sched.to_c()
+    st = lib().fibattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, d,
+                           _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0, Lc,
+                           _stream(q))
+    _check(st, "fibattn_fwd")
+    return o, lse
+
+
+def bwd(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
+        scale: Optional[float] = None, dq=None, dk=None, dv=None, delta=None):
+    """Sparse attention backward from the saved forward; returns (dq, dk, dv)."""
+    Lc, B, H, T, d = _shape(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _check_tensors(q, k, v, o, dO, dq, dk, dv)
+    if delta is None:
+        delta = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    s = sched.to_c()
+    st = lib().fibattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(delta), B, H, T, d, _DTYPES[q.dtype], W,
+                           float(scale or 0.0), ctypes.byref(s), layer0, Lc, _stream(q))
+    _check(st, "fibattn_bwd")
+    return dq, dk, dv
+
+
+def keyset_debug(sched: Schedule, layer: int, W: int, T: int, device="cuda") -> torch.Tensor:
+    """Device-materialised key sets of one layer as a bool [T, T] tensor (on `device`)."""
+    words = (T + 31) // 32
+    m = torch.zeros((T, words), dtype=torch.int32, device=device)
+    s = sched.to_c()
+    _check(lib().fibattn_keyset_debug(ctypes.byref(s), layer, W, T, _ptr(m), _stream(m)),
+           "fibattn_keyset_debug")
+    bits = (m.unsqueeze(-1) >> torch.arange(32, device=device, dtype=torch.int32)) & 1
+    return bits.reshape(T, words * 32)[:, :T].bool()
+
+
+def poll_device_error(device="cuda"):
+    """Synchronise the current stream and raise if a kernel latched an error."""
+    st = lib().fibattn_poll_device_error(
+        ctypes.c_void_p(torch.cuda.current_stream(torch.device(device)).cuda_stream))
+    _check(st, "fibattn_poll_device_error")
+
+
+class FibSparseAttention(torch.autograd.Function):
+    """autograd wrapper: forward and backward both run the library's kernels."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, W: int, sched: Schedule, layer0: int = 0, scale=None):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        o, lse = fwd(q, k, v, W, sched, layer0, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.cfg = (W, sched, layer0, scale)
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, o, lse = ctx.saved_tensors
+        W, sched, layer0, scale = ctx.cfg
+        dq, dk, dv = bwd(q, k, v, o, lse, dO.contiguous(), W, sched, layer0, scale)
+        return dq, dk, dv, None, None, None, None

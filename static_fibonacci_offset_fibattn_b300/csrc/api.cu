@@ -1,0 +1,178 @@
+// api.cu -- the extern "C" entry points declared in include/fibattn.h: argument
+// validation, offset-table construction, and dispatch to the kernels.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+using namespace fibattn;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Shared checks of fibattn_fwd / fibattn_bwd.
+fibattn_status check_common(int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                            const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
+    if (!sched) return FIBATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 1 || W < 1 || n_layers_call < 1 || layer0 < 0)
+        return FIBATTN_ERR_INVALID_ARG;
+    if (sched->n_layers < 1 || (int64_t)layer0 + n_layers_call > sched->n_layers)
+        return FIBATTN_ERR_INVALID_ARG;
+    if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
+    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    // rows of one launch layer must index within int32 grids and int64 offsets
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows > ((int64_t)1 << 34)) return FIBATTN_ERR_INVALID_ARG;
+    if (rows * (int64_t)n_layers_call > ((int64_t)1 << 40)) return FIBATTN_ERR_INVALID_ARG;
+    // validate every layer's schedule and table size before launching anything
+    for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
+        int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
+        OffsetTables t;
+        fibattn_status st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
+        if (st != FIBATTN_OK) return st;
+    }
+    return FIBATTN_OK;
+}
+
+size_t elt_size(int32_t dtype) { return dtype == FIBATTN_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t fibattn_version(void) { return 100; }
+
+const char* fibattn_status_string(fibattn_status s) {
+    switch (s) {
+        case FIBATTN_OK: return "ok";
+        case FIBATTN_ERR_INVALID_ARG: return "invalid argument";
+        case FIBATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case FIBATTN_ERR_CAPACITY: return "offset table exceeds capacity";
+        case FIBATTN_ERR_CUDA: return "CUDA error";
+        case FIBATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+fibattn_status fibattn_offsets(const fibattn_schedule* sched, int32_t layer, int32_t W, int32_t T,
+                               int32_t* out, int32_t cap, int32_t* n_out) {
+    if (!sched || !n_out || (cap > 0 && !out) || cap < 0) return FIBATTN_ERR_INVALID_ARG;
+    if (W < 1 || T < 1) return FIBATTN_ERR_INVALID_ARG;
+    Alpha a;
+    fibattn_status st = layer_alpha(sched, layer, &a);
+    if (st != FIBATTN_OK) return st;
+    return build_table(sched, a, W, T, out, cap, n_out);
+}
+
+fibattn_status fibattn_offsets_device(const fibattn_schedule* sched, int32_t layer0,
+                                      int32_t n_layers_call, int32_t W, int32_t T,
+                                      int32_t* d_tables, int32_t* d_counts, void* cuda_stream) {
+    if (!sched || !d_tables || !d_counts || n_layers_call < 1 || layer0 < 0)
+        return FIBATTN_ERR_INVALID_ARG;
+    if (W < 1 || T < 1) return FIBATTN_ERR_INVALID_ARG;
+    if ((int64_t)layer0 + n_layers_call > sched->n_layers) return FIBATTN_ERR_INVALID_ARG;
+    for (int32_t c = 0; c < n_layers_call; ++c) {  // same validation and capacity as the host
+        Alpha a;
+        fibattn_status st = layer_alpha(sched, layer0 + c, &a);
+        if (st != FIBATTN_OK) return st;
+        int32_t tmp[kMaxOffsets], n = 0;
+        st = build_table(sched, a, W, T, tmp, kMaxOffsets, &n);
+        if (st != FIBATTN_OK) return st;
+    }
+    return launch_offsets_device(sched, layer0, n_layers_call, W, T, d_tables, d_counts,
+                                 as_stream(cuda_stream));
+}
+
+fibattn_status fibattn_keyset_debug(const fibattn_schedule* sched, int32_t layer, int32_t W,
+                                    int32_t T, uint32_t* d_mask, void* cuda_stream) {
+    if (!sched || !d_mask) return FIBATTN_ERR_INVALID_ARG;
+    if (W < 1 || T < 1) return FIBATTN_ERR_INVALID_ARG;
+    OffsetTables t;
+    fibattn_status st = build_launch_tables(sched, layer, 1, W, T, &t);
+    if (st != FIBATTN_OK) return st;
+    return launch_keyset(t, W, T, d_mask, as_stream(cuda_stream));
+}
+
+fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                           float scale, const fibattn_schedule* sched, int32_t layer0,
+                           int32_t n_layers_call, void* cuda_stream) {
+    if (!q || !k || !v || !o || !lse) return FIBATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FIBATTN_ERR_INVALID_ARG;
+    fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
+    if (st != FIBATTN_OK) return st;
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    const int64_t per_layer = (int64_t)B * H * T;
+    const size_t es = elt_size(dtype);
+    for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
+        const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
+        OffsetTables t;
+        st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
+        if (st != FIBATTN_OK) return st;
+        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        const size_t off = (size_t)c * per_layer * d * es;
+        const char* qc = (const char*)q + off;
+        const char* kc = (const char*)k + off;
+        const char* vc = (const char*)v + off;
+        char* oc = (char*)o + off;
+        float* lc = lse + (size_t)c * per_layer;
+        if (dtype == FIBATTN_F32)
+            st = launch_fwd_simt_f32((const float*)qc, (const float*)kc, (const float*)vc,
+                                     (float*)oc, lc, sh, t, as_stream(cuda_stream));
+        else
+            st = launch_fwd_simt_bf16(qc, kc, vc, oc, lc, sh, t, as_stream(cuda_stream));
+        if (st != FIBATTN_OK) return st;
+    }
+    return FIBATTN_OK;
+}
+
+fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           float* delta_ws, int32_t B, int32_t H, int32_t T, int32_t d,
+                           int32_t dtype, int32_t W, float scale, const fibattn_schedule* sched,
+                           int32_t layer0, int32_t n_layers_call, void* cuda_stream) {
+    const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta_ws};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return FIBATTN_ERR_INVALID_ARG;
+    fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
+    if (st != FIBATTN_OK) return st;
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    const int64_t per_layer = (int64_t)B * H * T;
+    const size_t es = elt_size(dtype);
+    for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
+        const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
+        OffsetTables t;
+        st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
+        if (st != FIBATTN_OK) return st;
+        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        const size_t off = (size_t)c * per_layer * d * es;
+        const size_t loff = (size_t)c * per_layer;
+        st = launch_bwd((const char*)q + off, (const char*)k + off, (const char*)v + off,
+                        (const char*)o + off, lse + loff, (const char*)dO + off, (char*)dq + off,
+                        (char*)dk + off, (char*)dv + off, delta_ws + loff, sh, t, dtype,
+                        as_stream(cuda_stream));
+        if (st != FIBATTN_OK) return st;
+    }
+    return FIBATTN_OK;
+}
+
+fibattn_status fibattn_poll_device_error(void* cuda_stream) {
+    if (cudaStreamSynchronize(as_stream(cuda_stream)) != cudaSuccess) return FIBATTN_ERR_CUDA;
+    if (cudaPeekAtLastError() != cudaSuccess) return FIBATTN_ERR_CUDA;
+    int32_t* w = device_error_word();
+    if (!w) return FIBATTN_ERR_CUDA;
+    int32_t h = 0;
+    if (cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FIBATTN_ERR_CUDA;
+    if (h != kDevErrNone) {
+        if (cudaMemset(w, 0, sizeof(int32_t)) != cudaSuccess) return FIBATTN_ERR_CUDA;
+        return FIBATTN_ERR_TIMEOUT;
+    }
+    return FIBATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// internal.h -- types shared by the library's host code and its kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fibattn.h"
+
+namespace fibattn {
+
+// Layers handled by one kernel launch; longer calls are split into several launches.
+constexpr int kMaxLayersPerLaunch = 16;
+constexpr int kMaxOffsets = FIBATTN_MAX_OFFSETS;
+
+// Per-launch offset tables, passed by value (__grid_constant__) so that they live in
+// the kernel's constant bank: every launch carries its own copy, so concurrent calls
+// on different streams cannot see each other's tables.
+struct OffsetTables {
+    int32_t count[kMaxLayersPerLaunch];
+    int32_t off[kMaxLayersPerLaunch][kMaxOffsets];  // ascending, each in [W, T-1]
+};
+
+// An exact alpha = num / den of one layer (num, den > 0, already reduced).
+struct Alpha {
+    int64_t num, den;
+};
+
+// Validates a schedule and a layer index; writes the layer's exact alpha.
+fibattn_status layer_alpha(const fibattn_schedule* s, int32_t layer, Alpha* out);
+
+// Host offset table of one layer under an exact alpha (see fibattn_offsets).
+fibattn_status build_table(const fibattn_schedule* s, Alpha a, int32_t W, int32_t T, int32_t* out,
+                           int32_t cap, int32_t* n_out);
+
+// Builds OffsetTables for launch layers [layer0, layer0 + n).
+fibattn_status build_launch_tables(const fibattn_schedule* s, int32_t layer0, int32_t n, int32_t W,
+                                   int32_t T, OffsetTables* t);
+
+// Brackets one kernel launch: counts it and, while profiling is enabled
+// (fibattn_profile_enable), records a start/stop event pair on its stream.
+class KernelScope {
+  public:
+    KernelScope(const char* name, cudaStream_t st);
+    ~KernelScope();
+    KernelScope(const KernelScope&) = delete;
+    KernelScope& operator=(const KernelScope&) = delete;
+
+  private:
+    cudaStream_t st_;
+    int rec_;
+};
+
+// Device error word protocol (see fibattn_poll_device_error).
+enum DeviceError : int32_t { kDevErrNone = 0, kDevErrTimeout = 1 };
+int32_t* device_error_word();  // device address of the error word (current device)
+
+// Launchers (defined in the .cu files).
+fibattn_status launch_offsets_device(const fibattn_schedule* s, int32_t layer0, int32_t n,
+                                     int32_t W, int32_t T, int32_t* d_tables, int32_t* d_counts,
+                                     cudaStream_t st);
+fibattn_status launch_keyset(const OffsetTables& t, int32_t W, int32_t T, uint32_t* d_mask,
+                             cudaStream_t st);
+
+struct AttnShape {
+    int64_t slices_per_layer;  // B * H
+    int32_t T;
+    int32_t W;
+    float scale;
+    int32_t n_layers;          // layers in this launch
+};
+
+fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o,
+                                   float* lse, const AttnShape& sh, const OffsetTables& t,
+                                   cudaStream_t st);
+fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, const AttnShape& sh, const OffsetTables& t,
+                                    cudaStream_t st);
+fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
+fibattn_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          float* delta, const AttnShape& sh, const OffsetTables& t, int32_t dtype,
+                          cudaStream_t st);
+
+}  // namespace fibattn

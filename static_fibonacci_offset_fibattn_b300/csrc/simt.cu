@@ -1,0 +1,263 @@
+// simt.cu -- SIMT (CUDA-core) kernels: the fp32 forward and the backward.
+//
+// One warp owns one row; lane l holds head dims 2l and 2l+1 (d = 64), so every K/V/Q
+// row is read by one coalesced warp access and dot products finish with an xor
+// shuffle reduction (every lane receives the sum, bit-identically).
+//
+// Attended set ("Depth-Staggered Fibonacci Spacing for Sparse Attention", gist.science
+// explainer, Metodologia / Arquitetura, "Conjunto Atendido"): query i sees keys
+// i - W + 1 .. i (clipped at 0) and i - o for each table offset o <= i. Table offsets
+// are >= W, so the two parts never overlap.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace fibattn {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kWarpsPerBlock = 8;
+
+template <typename E>
+struct Io;
+
+template <>
+struct Io<float> {
+    static __device__ __forceinline__ float2 ld(const float* p) {
+        return __ldg(reinterpret_cast<const float2*>(p));
+    }
+    static __device__ __forceinline__ void st(float* p, float2 x) {
+        *reinterpret_cast<float2*>(p) = x;
+    }
+};
+
+template <>
+struct Io<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 ld(const __nv_bfloat16* p) {
+        __nv_bfloat162 h = __ldg(reinterpret_cast<const __nv_bfloat162*>(p));
+        return __bfloat1622float2(h);
+    }
+    static __device__ __forceinline__ void st(__nv_bfloat16* p, float2 x) {
+        *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(x);
+    }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+// ---------------------------------------------------------------- forward (fp32 path)
+// Online softmax over S_i in fp32: running max m, running sum l, accumulator acc.
+template <typename E>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+fwd_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
+                E* __restrict__ o, float* __restrict__ lse, AttnShape sh,
+                const __grid_constant__ OffsetTables tab) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int layer = blockIdx.y;
+    if (row >= rows) return;
+    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int32_t i = (int32_t)(row % sh.T);
+    const int64_t base = slice * sh.T * kD;
+    const float2 qv = Io<E>::ld(q + base + (int64_t)i * kD + 2 * lane);
+
+    float m = -INFINITY, l = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
+    auto visit = [&](int32_t j) {
+        const float2 kv = Io<E>::ld(k + base + (int64_t)j * kD + 2 * lane);
+        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y) * sh.scale;
+        const float2 vv = Io<E>::ld(v + base + (int64_t)j * kD + 2 * lane);
+        const float mn = fmaxf(m, s);
+        const float corr = expf(m - mn);  // m = -inf on the first key: corr = 0
+        const float p = expf(s - mn);
+        l = l * corr + p;
+        acc.x = acc.x * corr + p * vv.x;
+        acc.y = acc.y * corr + p * vv.y;
+        m = mn;
+    };
+    const int n_off = tab.count[layer];
+    for (int e = n_off - 1; e >= 0; --e) {
+        const int32_t j = i - tab.off[layer][e];
+        if (j >= 0) visit(j);
+    }
+    const int32_t j0 = i - sh.W + 1 > 0 ? i - sh.W + 1 : 0;
+    for (int32_t j = j0; j <= i; ++j) visit(j);
+
+    const float inv = 1.f / l;
+    Io<E>::st(o + base + (int64_t)i * kD + 2 * lane, make_float2(acc.x * inv, acc.y * inv));
+    if (lane == 0) lse[slice * sh.T + i] = m + logf(l);
+}
+
+// ---------------------------------------------------------------- backward
+// D_i = dO_i . O_i
+template <typename E>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __restrict__ delta,
+                 int64_t total_rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (row >= total_rows) return;
+    const float2 a = Io<E>::ld(o + row * kD + 2 * lane);
+    const float2 b = Io<E>::ld(dO + row * kD + 2 * lane);
+    const float s = warp_sum(a.x * b.x + a.y * b.y);
+    if (lane == 0) delta[row] = s;
+}
+
+// dQ_i = scale * sum_{j in S_i} P_ij (dO_i . v_j - D_i) k_j   (query owner)
+template <typename E>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+bwd_dq_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
+              const float* __restrict__ lse, const E* __restrict__ dO,
+              const float* __restrict__ delta, E* __restrict__ dq, AttnShape sh,
+              const __grid_constant__ OffsetTables tab) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int layer = blockIdx.y;
+    if (row >= rows) return;
+    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int32_t i = (int32_t)(row % sh.T);
+    const int64_t base = slice * sh.T * kD;
+    const int64_t ri = base + (int64_t)i * kD + 2 * lane;
+    const float2 qv = Io<E>::ld(q + ri);
+    const float2 gv = Io<E>::ld(dO + ri);
+    const float Li = lse[slice * sh.T + i];
+    const float Di = delta[slice * sh.T + i];
+    float2 acc = make_float2(0.f, 0.f);
+    auto visit = [&](int32_t j) {
+        const int64_t rj = base + (int64_t)j * kD + 2 * lane;
+        const float2 kv = Io<E>::ld(k + rj);
+        const float2 vv = Io<E>::ld(v + rj);
+        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
+        const float dp = warp_sum(gv.x * vv.x + gv.y * vv.y);
+        const float p = expf(s * sh.scale - Li);
+        const float ds = p * (dp - Di);
+        acc.x += ds * kv.x;
+        acc.y += ds * kv.y;
+    };
+    for (int e = tab.count[layer] - 1; e >= 0; --e) {
+        const int32_t j = i - tab.off[layer][e];
+        if (j >= 0) visit(j);
+    }
+    const int32_t j0 = i - sh.W + 1 > 0 ? i - sh.W + 1 : 0;
+    for (int32_t j = j0; j <= i; ++j) visit(j);
+    Io<E>::st(dq + ri, make_float2(acc.x * sh.scale, acc.y * sh.scale));
+}
+
+// dK_j = scale * sum_{i : j in S_i} dS_ij q_i,  dV_j = sum_{i : j in S_i} P_ij dO_i  (key owner)
+// The queries that see key j: i = j + t for 0 <= t < W, and i = j + o for table offsets o,
+// each only while i < T. No atomics: this warp is the only writer of row j.
+template <typename E>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+bwd_dkdv_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
+                const float* __restrict__ lse, const E* __restrict__ dO,
+                const float* __restrict__ delta, E* __restrict__ dk, E* __restrict__ dv,
+                AttnShape sh, const __grid_constant__ OffsetTables tab) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int layer = blockIdx.y;
+    if (row >= rows) return;
+    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int32_t j = (int32_t)(row % sh.T);
+    const int64_t base = slice * sh.T * kD;
+    const int64_t rj = base + (int64_t)j * kD + 2 * lane;
+    const float2 kv = Io<E>::ld(k + rj);
+    const float2 vv = Io<E>::ld(v + rj);
+    float2 ak = make_float2(0.f, 0.f), av = make_float2(0.f, 0.f);
+    auto visit = [&](int32_t i) {
+        const int64_t ri = base + (int64_t)i * kD + 2 * lane;
+        const float2 qv = Io<E>::ld(q + ri);
+        const float2 gv = Io<E>::ld(dO + ri);
+        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
+        const float dp = warp_sum(gv.x * vv.x + gv.y * vv.y);
+        const float p = expf(s * sh.scale - lse[slice * sh.T + i]);
+        const float ds = p * (dp - delta[slice * sh.T + i]);
+        av.x += p * gv.x;
+        av.y += p * gv.y;
+        ak.x += ds * qv.x;
+        ak.y += ds * qv.y;
+    };
+    const int32_t i1 = j + sh.W - 1 < sh.T - 1 ? j + sh.W - 1 : sh.T - 1;
+    for (int32_t i = j; i <= i1; ++i) visit(i);
+    for (int e = 0; e < tab.count[layer]; ++e) {
+        const int64_t i = (int64_t)j + tab.off[layer][e];
+        if (i < sh.T) visit((int32_t)i);
+    }
+    Io<E>::st(dk + rj, make_float2(ak.x * sh.scale, ak.y * sh.scale));
+    Io<E>::st(dv + rj, av);
+}
+
+}  // namespace
+
+fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o,
+                                   float* lse, const AttnShape& sh, const OffsetTables& t,
+                                   cudaStream_t st) {
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    dim3 grid((unsigned)blocks, sh.n_layers);
+    KernelScope ks("fwd_simt_f32", st);
+    fwd_simt_kernel<float><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, o, lse, sh, t);
+    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+}
+
+fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, const AttnShape& sh, const OffsetTables& t,
+                                    cudaStream_t st) {
+    typedef __nv_bfloat16 E;
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    dim3 grid((unsigned)blocks, sh.n_layers);
+    KernelScope ks("fwd_simt_bf16", st);
+    fwd_simt_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(
+        (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
+    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+}
+
+template <typename E>
+static fibattn_status bwd_typed(const E* q, const E* k, const E* v, const E* o, const float* lse,
+                                const E* dO, E* dq, E* dk, E* dv, float* delta,
+                                const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t all_rows = rows * sh.n_layers;
+    const int64_t dblocks = (all_rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffff || dblocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    {
+        KernelScope ks("bwd_delta_simt", st);
+        bwd_delta_kernel<E><<<(unsigned)dblocks, kWarpsPerBlock * 32, 0, st>>>(o, dO, delta, all_rows);
+    }
+    dim3 grid((unsigned)blocks, sh.n_layers);
+    {
+        KernelScope ks("bwd_dq_simt", st);
+        bwd_dq_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dq, sh, t);
+    }
+    {
+        KernelScope ks("bwd_dkdv_simt", st);
+        bwd_dkdv_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dk, dv, sh, t);
+    }
+    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+}
+
+fibattn_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          float* delta, const AttnShape& sh, const OffsetTables& t, int32_t dtype,
+                          cudaStream_t st) {
+    if (dtype == FIBATTN_F32)
+        return bwd_typed<float>((const float*)q, (const float*)k, (const float*)v, (const float*)o,
+                                lse, (const float*)dO, (float*)dq, (float*)dk, (float*)dv, delta,
+                                sh, t, st);
+    typedef __nv_bfloat16 E;
+    return bwd_typed<E>((const E*)q, (const E*)k, (const E*)v, (const E*)o, lse, (const E*)dO,
+                        (E*)dq, (E*)dk, (E*)dv, delta, sh, t, st);
+}
+
+}  // namespace fibattn

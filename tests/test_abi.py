@@ -1,0 +1,162 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, builds host offset tables identical to the oracle's, and rejects bad
+arguments with the documented status before touching the device."""
+import ctypes
+import os
+import re
+from fractions import Fraction
+
+import pytest
+import torch
+
+import static_fibonacci_offset_fibattn_b300 as fa
+from oracle import schedule as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"FIBATTN_API\s+[\w\s\*]+?\b(fibattn_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 8
+    L = fa.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.fibattn_version() >= 100
+
+
+def test_status_strings():
+    for s in range(6):
+        assert fa.status_string(s)
+    assert fa.status_string(99) == "unknown status"
+
+
+def _sched_to_oracle(sc: fa.Schedule, layer, W, T):
+    kw = {}
+    if sc.kind == "fixed":
+        kw["alpha"] = Fraction(*sc.alpha)
+    else:
+        kw["alpha_min"] = Fraction(*sc.alpha_min)
+        kw["alpha_max"] = Fraction(*sc.alpha_max)
+        kw["coprime_c"] = sc.coprime_c
+    return S.layer_table(sc.base, sc.kind, layer, sc.n_layers, W, T, sc.base_max, **kw)
+
+
+SCHEDS = [
+    fa.Schedule("fixed", "fib", alpha=(1, 1)),
+    fa.Schedule("fixed", "pow2", alpha=(1, 1)),
+    fa.Schedule("linear", "fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16),
+    fa.Schedule("linear", "fib", alpha_min=(1, 2), alpha_max=(3, 2), n_layers=16),
+    fa.Schedule("coprime", "fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16, coprime_c=5),
+    fa.Schedule("coprime", "fib", alpha_min=(1, 2), alpha_max=(3, 2), n_layers=16, coprime_c=7),
+    fa.Schedule("linear", "pow2", alpha_min=(1, 2), alpha_max=(3, 2), n_layers=16),
+    fa.Schedule("linear", "fib", alpha_min=(3, 2), alpha_max=(1, 3), n_layers=5),
+    fa.Schedule("fixed", "fib", alpha=(7, 3), base_max=100000),
+    fa.Schedule("fixed", "pow2", alpha=(1, 1000), base_max=0),
+    fa.Schedule("coprime", "pow2", alpha_min=(1, 7), alpha_max=(9, 4), n_layers=9, coprime_c=4),
+    fa.Schedule("linear", "fib", alpha_min=(5, 4), alpha_max=(5, 4), n_layers=1),
+]
+
+
+@pytest.mark.parametrize("sc", SCHEDS)
+@pytest.mark.parametrize("WT", [(16, 256), (64, 1024), (64, 4096), (6, 1024), (12, 100000), (1, 3)])
+def test_host_tables_match_oracle(sc, WT):
+    W, T = WT
+    for layer in range(sc.n_layers):
+        want = _sched_to_oracle(sc, layer, W, T)
+        if len(want) > fa.MAX_OFFSETS:
+            with pytest.raises(fa.FibAttnError) as e:
+                fa.offsets(sc, layer, W, T)
+            assert e.value.status == fa.CAPACITY
+        else:
+            assert fa.offsets(sc, layer, W, T) == want, (layer, want)
+
+
+def test_offsets_rejects_bad_schedules():
+    bad = [
+        fa.Schedule("coprime", "fib", n_layers=16, coprime_c=4),
+        fa.Schedule("coprime", "fib", n_layers=16, coprime_c=0),
+        fa.Schedule("fixed", "fib", alpha=(0, 1)),
+        fa.Schedule("fixed", "fib", alpha=(1, 0)),
+        fa.Schedule("fixed", "fib", alpha=(-1, 2)),
+        fa.Schedule("linear", "fib", alpha_min=(1, 2), alpha_max=(1, 0), n_layers=4),
+        fa.Schedule("fixed", "fib", alpha=(1 << 21, 1)),
+        fa.Schedule("fixed", "fib", n_layers=0),
+        fa.Schedule("fixed", "fib", base_max=-1),
+    ]
+    for sc in bad:
+        with pytest.raises(fa.FibAttnError) as e:
+            fa.offsets(sc, 0, 16, 256)
+        assert e.value.status == fa.INVALID_ARG, sc
+    sc = fa.Schedule("fixed", "fib", n_layers=2)
+    for (layer, W, T) in [(2, 16, 256), (-1, 16, 256), (0, 0, 256), (0, 16, 0)]:
+        with pytest.raises(fa.FibAttnError) as e:
+            fa.offsets(sc, layer, W, T)
+        assert e.value.status == fa.INVALID_ARG
+
+
+def test_capacity_status_reports_needed_count():
+    L = fa.lib()
+    sc = fa.Schedule("fixed", "fib").to_c()
+    buf = (ctypes.c_int32 * 2)()
+    n = ctypes.c_int32(0)
+    st = L.fibattn_offsets(ctypes.byref(sc), 0, 16, 256, buf, 2, ctypes.byref(n))
+    assert st == fa.CAPACITY and n.value == 6 and list(buf) == [21, 34]
+
+
+def _fwd_raw(q=1, k=1, v=1, o=1, lse=1, B=1, H=1, T=8, d=64, dtype=1, W=4, sched=None,
+             layer0=0, n=1):
+    L = fa.lib()
+    sc = (sched or fa.Schedule()).to_c()
+    P = lambda x: ctypes.c_void_p(x * 256)  # non-null, 16-byte aligned, never dereferenced
+    return L.fibattn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, T, d, dtype, W, 0.0,
+                         ctypes.byref(sc), layer0, n, None)
+
+
+def test_fwd_validates_before_launch():
+    # every one of these is rejected on the host, so no kernel runs (no GPU needed)
+    assert _fwd_raw(q=0) == fa.INVALID_ARG
+    assert _fwd_raw(B=0) == fa.INVALID_ARG
+    assert _fwd_raw(T=0) == fa.INVALID_ARG
+    assert _fwd_raw(W=0) == fa.INVALID_ARG
+    assert _fwd_raw(d=128) == fa.UNSUPPORTED
+    assert _fwd_raw(dtype=7) == fa.UNSUPPORTED
+    assert _fwd_raw(n=2) == fa.INVALID_ARG  # schedule has one layer
+    assert _fwd_raw(layer0=-1) == fa.INVALID_ARG
+    assert _fwd_raw(sched=fa.Schedule("coprime", n_layers=4, coprime_c=2)) == fa.INVALID_ARG
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    mis = ctypes.c_void_p(256 + 8)
+    ok = ctypes.c_void_p(256)
+    assert L.fibattn_fwd(mis, ok, ok, ok, ok, 1, 1, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
+                         None) == fa.INVALID_ARG
+    assert L.fibattn_fwd(ok, ok, ok, ok, ok, 1, 1, 8, 64, 1, 4, 0.0, None, 0, 1,
+                         None) == fa.INVALID_ARG
+
+
+def test_bwd_validates_before_launch():
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    ok = ctypes.c_void_p(256)
+    args = [ok] * 10
+    for bad in range(10):
+        a = list(args)
+        a[bad] = ctypes.c_void_p(0)
+        assert L.fibattn_bwd(*a, 1, 1, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
+                             None) == fa.INVALID_ARG
+    assert L.fibattn_bwd(*args, 1, 1, 8, 32, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
+                         None) == fa.UNSUPPORTED
+
+
+def test_binding_refuses_cpu_tensors():
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd(q, q, q, 4, fa.Schedule())

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle (needs a B300).
+
+Index work is compared bit-exactly (offset tables, key sets); values within the
+stated max-abs tolerances (1e-5 fp32 path, 2e-2 bf16 path). Full-size workloads run
+in the same launch configuration the benchmark times, and sampled slices are
+recomputed by the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fibattn_inputs as fi
+import oracle
+import static_fibonacci_offset_fibattn_b300 as fa
+from gpu_common import (LSE_TOL, TOL, f64, lib_schedule, max_abs, oracle_bwd_slices,
+                        oracle_fwd_slices, oracle_table, sample_slices, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+SCHEDS = [
+    dict(kind="fixed", base="fib", alpha=(1, 1), n_layers=1),
+    dict(kind="fixed", base="pow2", alpha=(1, 1), n_layers=16),
+    dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16),
+    dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(3, 2), n_layers=16),
+    dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16, coprime_c=5),
+    dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(3, 2), n_layers=16, coprime_c=7),
+    dict(kind="linear", base="pow2", alpha_min=(1, 2), alpha_max=(3, 2), n_layers=16),
+    dict(kind="fixed", base="fib", alpha=(7, 3), n_layers=1, base_max=100000),
+    dict(kind="coprime", base="pow2", alpha_min=(1, 7), alpha_max=(9, 4), n_layers=9, coprime_c=4),
+]
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("WT", [(16, 256), (64, 1024), (64, 4096), (6, 1024), (12, 100000)])
+def test_device_tables_bit_exact(sched, WT):
+    W, T = WT
+    L = sched["n_layers"]
+    tab, cnt = fa.offsets_device(lib_schedule(sched), 0, L, W, T)
+    tab, cnt = tab.cpu().tolist(), cnt.cpu().tolist()
+    for l in range(L):
+        want = oracle_table(sched, l, W, T)
+        assert cnt[l] == len(want)
+        assert tab[l][: cnt[l]] == want
+        assert all(x == -1 for x in tab[l][cnt[l]:])
+        assert fa.offsets(lib_schedule(sched), l, W, T) == want
+
+
+@pytest.mark.parametrize("WT", [(16, 256), (6, 300), (64, 1024), (1, 100), (300, 257)])
+@pytest.mark.parametrize("sched", SCHEDS[:5])
+def test_keyset_debug_matches_oracle(sched, WT):
+    W, T = WT
+    for l in sorted({0, sched["n_layers"] - 1}):
+        m = fa.keyset_debug(lib_schedule(sched), l, W, T).cpu().numpy()
+        tab = oracle_table(sched, l, W, T)
+        for i in range(T):
+            assert np.flatnonzero(m[i]).tolist() == oracle.key_set(i, W, tab), (l, i)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("WT", [(16, 256), (64, 640), (6, 300)])
+def test_keyset_probe_through_forward(dtype, WT):
+    # Black box: Q = 0 makes every attended key weigh 1/|S_i|; V = one-hot over a block of
+    # 64 keys makes |S_i| * O_i[c] = [key 64*blk + c in S_i]. LSE_i = ln |S_i|.
+    W, T = WT
+    sched = dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    layer = 9
+    tab = oracle_table(sched, layer, W, T)
+    want = np.zeros((T, T), dtype=bool)
+    for i in range(T):
+        want[i, oracle.key_set(i, W, tab)] = True
+    got = np.zeros((T, T), dtype=bool)
+    q = torch.zeros(1, 1, T, 64, dtype=dt, device="cuda")
+    k = torch.randn(1, 1, T, 64, device="cuda").to(dt)
+    for blk in range((T + 63) // 64):
+        v = torch.zeros(1, 1, T, 64, dtype=dt, device="cuda")
+        for c in range(64):
+            j = 64 * blk + c
+            if j < T:
+                v[0, 0, j, c] = 1
+        o, lse = fa.fwd(q, k, v, W, lib_schedule(sched), layer0=layer)
+        n = torch.exp(lse[0, 0].double())
+        cnt = want.sum(1)
+        assert np.max(np.abs(n.cpu().numpy() - cnt)) < 1e-3 * cnt.max()
+        frac = (o[0, 0].double() * torch.from_numpy(cnt).cuda()[:, None]).cpu().numpy()
+        hi = min(T, 64 * blk + 64)
+        got[:, 64 * blk: hi] = frac[:, : hi - 64 * blk] > 0.5
+    assert (got == want).all()
+
+
+def _run_fwd(name, picks_per_layer, **override):
+    spec = dict(fi.WORKLOADS[name], **override)
+    inp = fi.workload_inputs(name, **override)
+    dev = to_dev(inp)
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], spec["W"], lib_schedule(spec["sched"]))
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    picks = [(l, b, h) for l in range(spec["Lc"])
+             for (b, h) in sample_slices(spec["B"], spec["H"], picks_per_layer)]
+    ref = oracle_fwd_slices(inp, spec["sched"], spec["W"], 0, picks)
+    worst_o = worst_l = 0.0
+    for (l, b, h), (ro, rl) in ref.items():
+        worst_o = max(worst_o, max_abs(f64(o[l, b, h]), ro))
+        worst_l = max(worst_l, max_abs(f64(lse[l, b, h]), rl))
+    return spec, worst_o, worst_l
+
+
+def test_fwd_c1_fp32_all_slices():
+    spec, eo, el = _run_fwd("c1", 64)
+    assert eo <= TOL["f32"], eo
+    assert el <= LSE_TOL["f32"], el
+
+
+def test_fwd_c2_bf16_all_slices():
+    spec, eo, el = _run_fwd("c2", 64)
+    assert eo <= TOL["bf16"], eo
+    assert el <= LSE_TOL["bf16"], el
+
+
+@pytest.mark.parametrize("name", ["c3", "c3p"])
+def test_fwd_c3_sixteen_layers_sampled(name):
+    spec, eo, el = _run_fwd(name, 3)
+    assert eo <= TOL["bf16"], eo
+    assert el <= LSE_TOL["bf16"], el
+
+
+def test_fwd_c4_extrapolation_sampled():
+    spec, eo, el = _run_fwd("c4", 2)
+    assert eo <= TOL["bf16"], eo
+    assert el <= LSE_TOL["bf16"], el
+
+
+EDGE = [
+    # (B, H, T, W, sched)
+    (1, 1, 1, 4, SCHEDS[0]),
+    (1, 2, 2, 1, SCHEDS[0]),
+    (2, 1, 63, 6, SCHEDS[2]),
+    (1, 3, 127, 8, SCHEDS[3]),
+    (1, 1, 129, 12, SCHEDS[4]),
+    (2, 2, 1000, 10, SCHEDS[5]),
+    (1, 2, 300, 64, SCHEDS[1]),
+    (1, 1, 700, 700, SCHEDS[0]),       # W >= T: dense causal
+    (1, 1, 333, 5000, SCHEDS[2]),      # W > T
+    (2, 1, 515, 100, SCHEDS[2]),       # W > 64
+    (1, 1, 1024, 1, SCHEDS[0]),        # window = the query itself
+    (1, 2, 2049, 64, SCHEDS[6]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", EDGE)
+def test_fwd_edge_cases(dtype, case):
+    B, H, T, W, sched = case
+    layer = sched["n_layers"] - 1
+    sched_one = dict(sched)
+    inp = fi.draw((1, B, H, T, 64), seed=11 + T, scale=0.5, dtype=dtype)
+    dev = to_dev(inp)
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], W, lib_schedule(sched_one), layer0=layer)
+    torch.cuda.synchronize()
+    picks = [(0, b, h) for b in range(B) for h in range(H)]
+    ref = oracle_fwd_slices(inp, sched_one, W, layer, picks)
+    for (l, b, h), (ro, rl) in ref.items():
+        assert max_abs(f64(o[l, b, h]), ro) <= TOL[dtype]
+        assert max_abs(f64(lse[l, b, h]), rl) <= LSE_TOL[dtype]
+
+
+def test_fwd_empty_table_is_sliding_window():
+    sched = dict(kind="fixed", base="fib", alpha=(1, 1), n_layers=1, base_max=10)
+    inp = fi.draw((1, 2, 2, 500, 64), seed=5, scale=0.5, dtype="bf16")
+    assert oracle_table(sched, 0, 16, 500) == []
+    dev = to_dev(inp)
+    o, _ = fa.fwd(dev["q"], dev["k"], dev["v"], 16, lib_schedule(sched))
+    T = 500
+    band = torch.ones(T, T, dtype=torch.bool).tril() & ~torch.ones(T, T, dtype=torch.bool).tril(-16)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        inp["q"].double(), inp["k"].double(), inp["v"].double(), attn_mask=band)
+    assert max_abs(f64(o), ref.numpy()) <= TOL["bf16"]
+
+
+def test_fwd_dense_causal_matches_sdpa():
+    inp = fi.draw((1, 2, 4, 1024, 64), seed=6, scale=0.125, dtype="bf16")
+    dev = to_dev(inp)
+    o, _ = fa.fwd(dev["q"], dev["k"], dev["v"], 1024, lib_schedule(SCHEDS[0]))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        dev["q"][0], dev["k"][0], dev["v"][0], is_causal=True)
+    assert max_abs(f64(o[0]), f64(ref)) <= TOL["bf16"]
+
+
+def test_fwd_layer_batched_equals_per_layer_calls():
+    spec = fi.WORKLOADS["c3"]
+    inp = to_dev(fi.workload_inputs("c3", layers=range(4), B=2, H=2))
+    sc = lib_schedule(spec["sched"])
+    o_all, l_all = fa.fwd(inp["q"], inp["k"], inp["v"], 64, sc, layer0=3)
+    for c in range(4):
+        o1, l1 = fa.fwd(inp["q"][c], inp["k"][c], inp["v"][c], 64, sc, layer0=3 + c)
+        assert torch.equal(o1, o_all[c]) and torch.equal(l1, l_all[c])
+
+
+def test_fwd_on_side_stream():
+    inp = to_dev(fi.draw((1, 1, 2, 777, 64), seed=9, scale=0.125, dtype="bf16"))
+    o0, _ = fa.fwd(inp["q"], inp["k"], inp["v"], 64, lib_schedule(SCHEDS[0]))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, _ = fa.fwd(inp["q"], inp["k"], inp["v"], 64, lib_schedule(SCHEDS[0]))
+    s.synchronize()
+    assert torch.equal(o0, o1)
+
+
+def test_fwd_deterministic():
+    inp = to_dev(fi.workload_inputs("c2", B=2))
+    sc = lib_schedule(fi.WORKLOADS["c2"]["sched"])
+    a = fa.fwd(inp["q"], inp["k"], inp["v"], 64, sc)
+    b = fa.fwd(inp["q"], inp["k"], inp["v"], 64, sc)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------ backward
+
+def _run_bwd(name, picks_per_layer, **override):
+    spec = dict(fi.WORKLOADS[name], **override)
+    inp = fi.workload_inputs(name, **override)
+    dev = to_dev(inp)
+    sc = lib_schedule(spec["sched"])
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], spec["W"], sc)
+    dq, dk, dv = fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], spec["W"], sc)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    picks = [(l, b, h) for l in range(spec["Lc"])
+             for (b, h) in sample_slices(spec["B"], spec["H"], picks_per_layer)]
+    ref = oracle_bwd_slices(inp, spec["sched"], spec["W"], 0, picks)
+    worst = dict(dq=0.0, dk=0.0, dv=0.0, o=0.0)
+    for (l, b, h), (rq, rk, rv, ro, rl) in ref.items():
+        worst["dq"] = max(worst["dq"], max_abs(f64(dq[l, b, h]), rq))
+        worst["dk"] = max(worst["dk"], max_abs(f64(dk[l, b, h]), rk))
+        worst["dv"] = max(worst["dv"], max_abs(f64(dv[l, b, h]), rv))
+        worst["o"] = max(worst["o"], max_abs(f64(o[l, b, h]), ro))
+    return worst
+
+
+def test_bwd_c5_training_step_sampled():
+    worst = _run_bwd("c5", 2)
+    for name, e in worst.items():
+        assert e <= TOL["bf16"], (name, e)
+
+
+BWD_EDGE = [
+    (1, 1, 1, 4, SCHEDS[0]),
+    (1, 2, 63, 6, SCHEDS[2]),
+    (2, 1, 129, 12, SCHEDS[4]),
+    (1, 1, 1000, 64, SCHEDS[5]),
+    (1, 1, 300, 300, SCHEDS[0]),
+    (1, 2, 517, 100, SCHEDS[1]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", BWD_EDGE)
+def test_bwd_edge_cases(dtype, case):
+    B, H, T, W, sched = case
+    layer = sched["n_layers"] - 1
+    inp = fi.draw((1, B, H, T, 64), seed=21 + T, scale=0.25, dtype=dtype,
+                  names=("q", "k", "v", "dO"))
+    dev = to_dev(inp)
+    sc = lib_schedule(sched)
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], W, sc, layer0=layer)
+    dq, dk, dv = fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], W, sc, layer0=layer)
+    torch.cuda.synchronize()
+    picks = [(0, b, h) for b in range(B) for h in range(H)]
+    ref = oracle_bwd_slices(inp, sched, W, layer, picks)
+    tol = TOL[dtype] if dtype == "bf16" else 1e-4
+    for (l, b, h), (rq, rk, rv, ro, rl) in ref.items():
+        assert max_abs(f64(dq[l, b, h]), rq) <= tol
+        assert max_abs(f64(dk[l, b, h]), rk) <= tol
+        assert max_abs(f64(dv[l, b, h]), rv) <= tol
+
+
+def test_autograd_wrapper_matches_bwd():
+    inp = to_dev(fi.draw((1, 2, 1, 300, 64), seed=31, scale=0.25, dtype="bf16",
+                         names=("q", "k", "v", "dO")))
+    sc = lib_schedule(SCHEDS[2])
+    q, k, v = (inp[n][0].clone().requires_grad_() for n in "qkv")
+    o = fa.FibSparseAttention.apply(q, k, v, 64, sc, 4)
+    o.backward(inp["dO"][0])
+    o2, lse = fa.fwd(inp["q"][0], inp["k"][0], inp["v"][0], 64, sc, layer0=4)
+    dq, dk, dv = fa.bwd(inp["q"][0], inp["k"][0], inp["v"][0], o2, lse, inp["dO"][0], 64, sc, 4)
+    assert torch.equal(o, o2) and torch.equal(q.grad, dq) and torch.equal(k.grad, dk)
+    assert torch.equal(v.grad, dv)
