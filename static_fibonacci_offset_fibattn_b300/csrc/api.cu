@@ -125,7 +125,7 @@ fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o,
             st = launch_fwd_simt_f32((const float*)qc, (const float*)kc, (const float*)vc,
                                      (float*)oc, lc, sh, t, as_stream(cuda_stream));
         else
-            st = launch_fwd_simt_bf16(qc, kc, vc, oc, lc, sh, t, as_stream(cuda_stream));
+            st = launch_fwd_tc_bf16(qc, kc, vc, oc, lc, sh, t, as_stream(cuda_stream));
         if (st != FIBATTN_OK) return st;
     }
     return FIBATTN_OK;

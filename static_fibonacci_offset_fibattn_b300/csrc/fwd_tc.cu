@@ -1,0 +1,470 @@
+// fwd_tc.cu -- bf16 forward of Fibonacci-offset sparse attention on sm_103a tensor cores.
+//
+// What is computed ("Depth-Staggered Fibonacci Spacing for Sparse Attention", gist.science
+// explainer, Metodologia / Arquitetura e Mecanismo de Atencao, "Conjunto Atendido"):
+// query i attends the dense window i-W+1..i and the keys i-o for the layer's offsets o;
+// o_i = softmax(scale * q_i . k_j over those keys) . v_j, lse_i = log sum_j exp(...).
+// The pages' static variants use fused boolean masking instead of a gather (same page,
+// Principais Contribuicoes 2, "Eficiencia"); here the window is a masked dense band on
+// the tensor cores and each offset is a diagonal handled by CUDA-core row dot products.
+//
+// One CTA = one tile of 128 queries [i0, i0+128) of one (layer, batch, head) slice.
+//   warps 0-3 : one thread per query row (TMEM lane = row); softmax, offsets, epilogue.
+//   warp 4    : TMEM allocation, band TMA loads, tcgen05.mma issue (lane 0).
+//   warp 5    : TMA loads of the shifted offset tiles into a 2-stage ring (lane 0).
+// Band: keys [max(0, i0-W+1), i0+127] in 64-key chunks, up to 3 chunks per group:
+//   S = Q K^T (tcgen05, M=128, N=64*chunks, K=64) -> TMEM columns [0, 192)
+//   masked online softmax per row (fp32, log2 domain), P (bf16) written back over S
+//   O_band += P V (tcgen05, A = P from TMEM, B = V MN-major in smem) -> TMEM [192, 256)
+// Offsets: for table entry o the shifted tiles K[i0-o .. i0-o+127], V[same] arrive by TMA
+//   (negative rows zero-filled); thread r takes row r of each: s = q_r . k_{i-o}, then a
+//   second pass accumulates exp(s - m) v_{i-o} in registers. The band and offset parts
+//   keep separate running maxima and are merged once in the epilogue.
+// Epilogue: O = (O_band 2^(m_b-m) + O_off 2^(m_o-m)) / l, staged to smem, TMA-stored;
+//   lse = (m + log2 l) ln 2.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "tc_prims.cuh"
+
+namespace fibattn {
+namespace {
+
+using namespace tc;
+
+constexpr int kRows = 128;          // queries per tile
+constexpr int kChunk = 64;          // keys per band chunk (one TMA box)
+constexpr int kMaxGroupChunks = 3;  // band chunks per S group (N <= 192)
+constexpr int kRing = 2;            // offset-tile ring stages
+constexpr int kBatch = 16;          // offsets scored per pass (register array)
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemO = 192;    // O accumulator columns [192, 256)
+
+constexpr uint32_t kTileBytes = kRows * 128;    // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kChunkBytes = kChunk * 128;  // 8 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffV = kOffK + kMaxGroupChunks * kChunkBytes;
+constexpr uint32_t kOffRing = kOffV + kMaxGroupChunks * kChunkBytes;
+constexpr uint32_t kOffBar = kOffRing + kRing * kTileBytes;
+// barriers: q, k, v, s, p, o, full[kRing], empty[kRing]; then the TMEM address word
+constexpr uint32_t kNumBars = 6 + 2 * kRing;
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffTmemSlot + 16;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+
+struct FwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3D {64, T, slices}, box {64, 64, 1}, 128B swizzle
+    float* lse;
+    int32_t* err;
+    int64_t slices_per_layer;
+    int32_t T, W;
+    int32_t tiles_per_slice;
+    float scale_log2;  // scale * log2(e)
+    OffsetTables tabs;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int idx) { return base + kOffBar + 8u * idx; }
+
+__global__ void __launch_bounds__(kThreads, 2)
+fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int layer = blockIdx.y;
+    const int tile = blockIdx.x % p.tiles_per_slice;
+    const int64_t slice = (int64_t)layer * p.slices_per_layer + blockIdx.x / p.tiles_per_slice;
+    const int32_t z = (int32_t)slice;
+    const int32_t T = p.T, W = p.W;
+    const int32_t i0 = tile * kRows;
+
+    const uint32_t B_Q = bar_addr(sbase, 0), B_K = bar_addr(sbase, 1), B_V = bar_addr(sbase, 2);
+    const uint32_t B_S = bar_addr(sbase, 3), B_P = bar_addr(sbase, 4), B_O = bar_addr(sbase, 5);
+    auto B_FULL = [&](int s) { return bar_addr(sbase, 6 + s); };
+    auto B_EMPTY = [&](int s) { return bar_addr(sbase, 6 + kRing + s); };
+
+    // band extent (64-key chunks) and active offsets (the table is ascending)
+    const int32_t kstart = i0 - W + 1 > 0 ? i0 - W + 1 : 0;
+    const int32_t klast = (i0 + kRows - 1 < T - 1) ? i0 + kRows - 1 : T - 1;
+    const int32_t c_lo = kstart / kChunk;
+    const int32_t n_chunks = klast / kChunk - c_lo + 1;
+    const int32_t n_groups = (n_chunks + kMaxGroupChunks - 1) / kMaxGroupChunks;
+    const int32_t* offs = p.tabs.off[layer];
+    int32_t n_act = 0;
+    for (int e = 0; e < p.tabs.count[layer]; ++e)
+        if (offs[e] <= klast) n_act = e + 1;
+
+    if (tid == 0) {
+        for (int b = 0; b < (int)kNumBars; ++b) {
+            uint32_t cnt = 1;
+            if (b == 4) cnt = kRows;                       // P written by every row thread
+            if (b >= 6 + kRing) cnt = kRows;               // ring slot released by every row
+            mbar_init(bar_addr(sbase, b), cnt);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+    bool aborted = false;
+
+    if (warp == 4) {
+        // ------------------------------------------------ band loads + MMA issue
+        if (lane == 0) {
+            prefetch_tmap(&p.tm_q);
+            prefetch_tmap(&p.tm_k);
+            prefetch_tmap(&p.tm_v);
+            mbar_arrive_expect_tx(B_Q, kTileBytes);
+            tma_load_3d(sbase + kOffQ, &p.tm_q, B_Q, 0, i0, z);
+            tma_load_3d(sbase + kOffQ + kChunkBytes, &p.tm_q, B_Q, 0, i0 + kChunk, z);
+            for (int g = 0; g < n_groups; ++g) {
+                const int nch = min(kMaxGroupChunks, n_chunks - g * kMaxGroupChunks);
+                const int32_t ybase = (c_lo + g * kMaxGroupChunks) * kChunk;
+                if (g > 0) {  // K and V buffers (and the P columns) free again
+                    mbar_wait(B_S, (g - 1) & 1, aborted, p.err);
+                    mbar_wait(B_O, (g - 1) & 1, aborted, p.err);
+                }
+                mbar_arrive_expect_tx(B_K, nch * kChunkBytes);
+                for (int c = 0; c < nch; ++c)
+                    tma_load_3d(sbase + kOffK + c * kChunkBytes, &p.tm_k, B_K, 0, ybase + c * kChunk, z);
+                mbar_arrive_expect_tx(B_V, nch * kChunkBytes);
+                for (int c = 0; c < nch; ++c)
+                    tma_load_3d(sbase + kOffV + c * kChunkBytes, &p.tm_v, B_V, 0, ybase + c * kChunk, z);
+                if (g == 0) mbar_wait(B_Q, 0, aborted, p.err);
+                mbar_wait(B_K, g & 1, aborted, p.err);
+                tc_fence_after();
+                const uint32_t idesc_s = idesc_bf16(128, 64 * nch, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem, sdesc_sw128(sbase + kOffQ + 32 * kk, 16, 1024),
+                           sdesc_sw128(sbase + kOffK + 32 * kk, 16, 1024), idesc_s, kk > 0);
+                mma_commit(B_S);
+                mbar_wait(B_P, g & 1, aborted, p.err);
+                tc_fence_after();
+                mbar_wait(B_V, g & 1, aborted, p.err);
+                const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);
+                for (int kk = 0; kk < nch * (kChunk / 16); ++kk)
+                    mma_ts(tmem + kTmemO, tmem + 8 * kk, sdesc_sw128(sbase + kOffV + 2048 * kk, 0, 1024),
+                           idesc_o, (g > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(B_O);
+            }
+            // teardown: the last commit must have landed before TMEM is released
+            mbar_wait(B_O, (n_groups - 1) & 1, aborted, p.err);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ offset tiles (K pass, then V pass)
+        if (lane == 0 && n_act > 0) {
+            uint32_t seq = 0;
+            for (int b0 = 0; b0 < n_act; b0 += kBatch) {
+                const int nb = min(kBatch, n_act - b0);
+                for (int pass = 0; pass < 2; ++pass) {
+                    const CUtensorMap* map = pass == 0 ? &p.tm_k : &p.tm_v;
+                    for (int k = 0; k < nb; ++k, ++seq) {
+                        const int s = seq % kRing;
+                        mbar_wait(B_EMPTY(s), ((seq / kRing) & 1) ^ 1, aborted, p.err);
+                        const int32_t y = i0 - offs[b0 + k];
+                        mbar_arrive_expect_tx(B_FULL(s), kTileBytes);
+                        tma_load_3d(sbase + kOffRing + s * kTileBytes, map, B_FULL(s), 0, y, z);
+                        tma_load_3d(sbase + kOffRing + s * kTileBytes + kChunkBytes, map, B_FULL(s), 0,
+                                    y + kChunk, z);
+                    }
+                }
+            }
+            // teardown: wait for the copies still in flight (already-completed phases pass)
+            for (uint32_t q = seq > kRing ? seq - kRing : 0; q < seq; ++q)
+                mbar_wait(B_FULL(q % kRing), (q / kRing) & 1, aborted, p.err);
+        }
+    } else {
+        // ------------------------------------------------ row threads
+        const int r = tid;
+        const int32_t i = i0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const float sl2 = p.scale_log2;
+
+        mbar_wait(B_Q, 0, aborted, p.err);
+
+        float m_o = -INFINITY, l_o = 0.f;
+        float oacc[64];
+        uint32_t seq = 0;
+        float sc[kBatch];
+
+        // pass 1 of an offset batch: scores of this row against K[i - o]
+        auto score_pass = [&](int b0, int nb) {
+            float q[64];  // this row of Q, reloaded per batch to keep it out of the band's registers
+            {
+                const uint8_t* qrow = smem + kOffQ;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
+                    q[8 * c + 0] = bf16lo(w.x); q[8 * c + 1] = bf16hi(w.x);
+                    q[8 * c + 2] = bf16lo(w.y); q[8 * c + 3] = bf16hi(w.y);
+                    q[8 * c + 4] = bf16lo(w.z); q[8 * c + 5] = bf16hi(w.z);
+                    q[8 * c + 6] = bf16lo(w.w); q[8 * c + 7] = bf16hi(w.w);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (k < nb) {
+                    const int s = seq % kRing;
+                    mbar_wait(B_FULL(s), (seq / kRing) & 1, aborted, p.err);
+                    const uint8_t* krow = smem + kOffRing + s * kTileBytes;
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
+                        a0 = fmaf(q[8 * c + 0], bf16lo(w.x), a0); a1 = fmaf(q[8 * c + 1], bf16hi(w.x), a1);
+                        a2 = fmaf(q[8 * c + 2], bf16lo(w.y), a2); a3 = fmaf(q[8 * c + 3], bf16hi(w.y), a3);
+                        a0 = fmaf(q[8 * c + 4], bf16lo(w.z), a0); a1 = fmaf(q[8 * c + 5], bf16hi(w.z), a1);
+                        a2 = fmaf(q[8 * c + 6], bf16lo(w.w), a2); a3 = fmaf(q[8 * c + 7], bf16hi(w.w), a3);
+                    }
+                    mbar_arrive(B_EMPTY(s));
+                    ++seq;
+                    const bool valid = i - offs[b0 + k] >= 0;
+                    sc[k] = valid ? ((a0 + a1) + (a2 + a3)) * sl2 : -INFINITY;
+                }
+            }
+            float mb = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+                if (k < nb) mb = fmaxf(mb, sc[k]);
+            const float mn = fmaxf(m_o, mb);
+            if (mn > m_o && m_o != -INFINITY) {  // later batch raised the max: rescale
+                const float corr = ex2(m_o - mn);
+                l_o *= corr;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) oacc[c] *= corr;
+            }
+            m_o = mn;
+        };
+        // pass 2 of an offset batch: accumulate exp2(s - m_o) * V[i - o]
+        auto value_pass = [&](int nb) {
+            const float mu = m_o == -INFINITY ? 0.f : m_o;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (k < nb) {
+                    const int s = seq % kRing;
+                    mbar_wait(B_FULL(s), (seq / kRing) & 1, aborted, p.err);
+                    const float pk = ex2(sc[k] - mu);  // sc = -inf -> 0
+                    l_o += pk;
+                    const uint8_t* vrow = smem + kOffRing + s * kTileBytes;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(vrow + sw128_off(r, c));
+                        oacc[8 * c + 0] = fmaf(pk, bf16lo(w.x), oacc[8 * c + 0]);
+                        oacc[8 * c + 1] = fmaf(pk, bf16hi(w.x), oacc[8 * c + 1]);
+                        oacc[8 * c + 2] = fmaf(pk, bf16lo(w.y), oacc[8 * c + 2]);
+                        oacc[8 * c + 3] = fmaf(pk, bf16hi(w.y), oacc[8 * c + 3]);
+                        oacc[8 * c + 4] = fmaf(pk, bf16lo(w.z), oacc[8 * c + 4]);
+                        oacc[8 * c + 5] = fmaf(pk, bf16hi(w.z), oacc[8 * c + 5]);
+                        oacc[8 * c + 6] = fmaf(pk, bf16lo(w.w), oacc[8 * c + 6]);
+                        oacc[8 * c + 7] = fmaf(pk, bf16hi(w.w), oacc[8 * c + 7]);
+                    }
+                    mbar_arrive(B_EMPTY(s));
+                    ++seq;
+                }
+            }
+        };
+
+        const int nb0 = min(kBatch, n_act);
+        if (nb0 > 0) score_pass(0, nb0);
+
+        // ---- band: masked online softmax over the S groups
+        float m_b = -INFINITY, l_b = 0.f;
+        for (int g = 0; g < n_groups; ++g) {
+            const int nch = min(kMaxGroupChunks, n_chunks - g * kMaxGroupChunks);
+            const int32_t kbase = (c_lo + g * kMaxGroupChunks) * kChunk;
+            mbar_wait(B_S, g & 1, aborted, p.err);
+            tc_fence_after();
+            uint32_t v[32];
+            float mx = -INFINITY;
+            for (int cc = 0; cc < nch * 2; ++cc) {
+                tmem_ld32(tmem + lane_base + 32 * cc, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const uint32_t dist = (uint32_t)(i - (kbase + 32 * cc + e));
+                    if (dist < (uint32_t)W) mx = fmaxf(mx, __uint_as_float(v[e]));
+                }
+            }
+            const float mn = fmaxf(m_b, mx == -INFINITY ? -INFINITY : mx * sl2);
+            if (g > 0) {
+                mbar_wait(B_O, (g - 1) & 1, aborted, p.err);
+                tc_fence_after();
+                const float corr = (m_b == -INFINITY) ? 0.f : ex2(m_b - mn);
+                if (__any_sync(0xffffffffu, mn != m_b)) {
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
+                        tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
+                    }
+                    tmem_st_wait();
+                }
+                l_b *= corr;
+            }
+            m_b = mn;
+            const float mu = m_b == -INFINITY ? 0.f : m_b;
+            for (int cc = 0; cc < nch * 2; ++cc) {
+                tmem_ld32(tmem + lane_base + 32 * cc, v);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const uint32_t d0 = (uint32_t)(i - (kbase + 32 * cc + e));
+                    const uint32_t d1 = d0 - 1u;
+                    const float p0 = d0 < (uint32_t)W ? ex2(__uint_as_float(v[e]) * sl2 - mu) : 0.f;
+                    const float p1 = d1 < (uint32_t)W ? ex2(__uint_as_float(v[e + 1]) * sl2 - mu) : 0.f;
+                    l_b += p0 + p1;
+                    pk[e >> 1] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tmem + lane_base + 16 * cc, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(B_P);
+        }
+
+#pragma unroll
+        for (int c = 0; c < 64; ++c) oacc[c] = 0.f;
+        if (nb0 > 0) value_pass(nb0);
+        for (int b0 = kBatch; b0 < n_act; b0 += kBatch) {
+            const int nb = min(kBatch, n_act - b0);
+            score_pass(b0, nb);
+            value_pass(nb);
+        }
+
+        // ---- epilogue: merge the band and offset softmax parts
+        mbar_wait(B_O, (n_groups - 1) & 1, aborted, p.err);
+        tc_fence_after();
+        const float m = fmaxf(m_b, m_o);
+        const float mu = m == -INFINITY ? 0.f : m;
+        const float fb = m_b == -INFINITY ? 0.f : ex2(m_b - mu);
+        const float fo = m_o == -INFINITY ? 0.f : ex2(m_o - mu);
+        const float l = l_b * fb + l_o * fo;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint8_t* orow = smem + kOffQ;  // Q tile is free: stage O there for the TMA store
+        for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint4 w;
+                const int e = 8 * c;
+                const int d = 32 * h + e;
+                w.x = pack_bf16x2((__uint_as_float(v[e + 0]) * fb + oacc[d + 0] * fo) * inv,
+                                  (__uint_as_float(v[e + 1]) * fb + oacc[d + 1] * fo) * inv);
+                w.y = pack_bf16x2((__uint_as_float(v[e + 2]) * fb + oacc[d + 2] * fo) * inv,
+                                  (__uint_as_float(v[e + 3]) * fb + oacc[d + 3] * fo) * inv);
+                w.z = pack_bf16x2((__uint_as_float(v[e + 4]) * fb + oacc[d + 4] * fo) * inv,
+                                  (__uint_as_float(v[e + 5]) * fb + oacc[d + 5] * fo) * inv);
+                w.w = pack_bf16x2((__uint_as_float(v[e + 6]) * fb + oacc[d + 6] * fo) * inv,
+                                  (__uint_as_float(v[e + 7]) * fb + oacc[d + 7] * fo) * inv);
+                *reinterpret_cast<uint4*>(orow + sw128_off(r, 4 * h + c)) = w;
+            }
+        }
+        if (i < T) p.lse[slice * T + i] = (m + lg2(l)) * 0.69314718055994531f;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (tid == 0 && !aborted) {
+            tma_store_3d(&p.tm_o, sbase + kOffQ, 0, i0, z);
+            if (i0 + kChunk < T) tma_store_3d(&p.tm_o, sbase + kOffQ + kChunkBytes, 0, i0 + kChunk, z);
+            tma_store_commit();
+            tma_store_wait_read0();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// [slices][T][64] bf16, box 64 x 64 rows, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)slices};
+    cuuint64_t strides[2] = {128, (cuuint64_t)T * 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kChunk, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
+    const int64_t slices = sh.slices_per_layer * sh.n_layers;
+    if (slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    const int32_t tiles = (sh.T + kRows - 1) / kRows;
+    const int64_t gx = (int64_t)tiles * sh.slices_per_layer;
+    if (gx > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    FwdParams P;
+    if (!make_map(&P.tm_q, q, slices, sh.T) || !make_map(&P.tm_k, k, slices, sh.T) ||
+        !make_map(&P.tm_v, v, slices, sh.T) || !make_map(&P.tm_o, o, slices, sh.T))
+        return FIBATTN_ERR_CUDA;
+    P.lse = lse;
+    P.err = device_error_word();
+    if (!P.err) return FIBATTN_ERR_CUDA;
+    P.slices_per_layer = sh.slices_per_layer;
+    P.T = sh.T;
+    P.W = sh.W;
+    P.tiles_per_slice = tiles;
+    P.scale_log2 = sh.scale * 1.4426950408889634f;
+    P.tabs = t;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FIBATTN_ERR_CUDA;
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64) return FIBATTN_ERR_UNSUPPORTED;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemAlloc) != cudaSuccess)
+            return FIBATTN_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    dim3 grid((unsigned)gx, sh.n_layers);
+    {
+        KernelScope ks("fwd_tc_bf16", st);
+        fwd_tc_kernel<<<grid, kThreads, kSmemAlloc, st>>>(P);
+    }
+    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+}
+
+}  // namespace fibattn
