@@ -40,7 +40,6 @@ constexpr int kRows = 128;          // queries per tile
 constexpr int kChunk = 64;          // keys per band chunk (one TMA box)
 constexpr int kMaxGroupChunks = 3;  // band chunks per S group (N <= 192)
 constexpr int kRing = 2;            // offset-tile ring stages
-constexpr int kBatch = 16;          // offsets scored per pass (register array)
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemO = 192;    // O accumulator columns [192, 256)
@@ -166,22 +165,19 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
             mbar_wait(B_O, (n_groups - 1) & 1, aborted, p.err);
         }
     } else if (warp == 5) {
-        // ------------------------------------------------ offset tiles (K pass, then V pass)
+        // ------------------------------------------------ offset tiles: K_o then V_o, per offset
         if (lane == 0 && n_act > 0) {
             uint32_t seq = 0;
-            for (int b0 = 0; b0 < n_act; b0 += kBatch) {
-                const int nb = min(kBatch, n_act - b0);
-                for (int pass = 0; pass < 2; ++pass) {
-                    const CUtensorMap* map = pass == 0 ? &p.tm_k : &p.tm_v;
-                    for (int k = 0; k < nb; ++k, ++seq) {
-                        const int s = seq % kRing;
-                        mbar_wait(B_EMPTY(s), ((seq / kRing) & 1) ^ 1, aborted, p.err);
-                        const int32_t y = i0 - offs[b0 + k];
-                        mbar_arrive_expect_tx(B_FULL(s), kTileBytes);
-                        tma_load_3d(sbase + kOffRing + s * kTileBytes, map, B_FULL(s), 0, y, z);
-                        tma_load_3d(sbase + kOffRing + s * kTileBytes + kChunkBytes, map, B_FULL(s), 0,
-                                    y + kChunk, z);
-                    }
+            for (int k = 0; k < n_act; ++k) {
+                const int32_t y = i0 - offs[k];
+                for (int h = 0; h < 2; ++h, ++seq) {
+                    const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
+                    const int s = seq % kRing;
+                    mbar_wait(B_EMPTY(s), ((seq / kRing) & 1) ^ 1, aborted, p.err);
+                    mbar_arrive_expect_tx(B_FULL(s), kTileBytes);
+                    tma_load_3d(sbase + kOffRing + s * kTileBytes, map, B_FULL(s), 0, y, z);
+                    tma_load_3d(sbase + kOffRing + s * kTileBytes + kChunkBytes, map, B_FULL(s), 0,
+                                y + kChunk, z);
                 }
             }
             // teardown: wait for the copies still in flight (already-completed phases pass)
@@ -195,157 +191,195 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const float sl2 = p.scale_log2;
 
-        mbar_wait(B_Q, 0, aborted, p.err);
-
-        float m_o = -INFINITY, l_o = 0.f;
-        float oacc[64];
-        uint32_t seq = 0;
-        float sc[kBatch];
-
-        // pass 1 of an offset batch: scores of this row against K[i - o]
-        auto score_pass = [&](int b0, int nb) {
-            float q[64];  // this row of Q, reloaded per batch to keep it out of the band's registers
-            {
-                const uint8_t* qrow = smem + kOffQ;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
-                    q[8 * c + 0] = bf16lo(w.x); q[8 * c + 1] = bf16hi(w.x);
-                    q[8 * c + 2] = bf16lo(w.y); q[8 * c + 3] = bf16hi(w.y);
-                    q[8 * c + 4] = bf16lo(w.z); q[8 * c + 5] = bf16hi(w.z);
-                    q[8 * c + 6] = bf16lo(w.w); q[8 * c + 7] = bf16hi(w.w);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                if (k < nb) {
-                    const int s = seq % kRing;
-                    mbar_wait(B_FULL(s), (seq / kRing) & 1, aborted, p.err);
-                    const uint8_t* krow = smem + kOffRing + s * kTileBytes;
-                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
-                        a0 = fmaf(q[8 * c + 0], bf16lo(w.x), a0); a1 = fmaf(q[8 * c + 1], bf16hi(w.x), a1);
-                        a2 = fmaf(q[8 * c + 2], bf16lo(w.y), a2); a3 = fmaf(q[8 * c + 3], bf16hi(w.y), a3);
-                        a0 = fmaf(q[8 * c + 4], bf16lo(w.z), a0); a1 = fmaf(q[8 * c + 5], bf16hi(w.z), a1);
-                        a2 = fmaf(q[8 * c + 6], bf16lo(w.w), a2); a3 = fmaf(q[8 * c + 7], bf16hi(w.w), a3);
-                    }
-                    mbar_arrive(B_EMPTY(s));
-                    ++seq;
-                    const bool valid = i - offs[b0 + k] >= 0;
-                    sc[k] = valid ? ((a0 + a1) + (a2 + a3)) * sl2 : -INFINITY;
-                }
-            }
-            float mb = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k)
-                if (k < nb) mb = fmaxf(mb, sc[k]);
-            const float mn = fmaxf(m_o, mb);
-            if (mn > m_o && m_o != -INFINITY) {  // later batch raised the max: rescale
-                const float corr = ex2(m_o - mn);
-                l_o *= corr;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) oacc[c] *= corr;
-            }
-            m_o = mn;
-        };
-        // pass 2 of an offset batch: accumulate exp2(s - m_o) * V[i - o]
-        auto value_pass = [&](int nb) {
-            const float mu = m_o == -INFINITY ? 0.f : m_o;
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                if (k < nb) {
-                    const int s = seq % kRing;
-                    mbar_wait(B_FULL(s), (seq / kRing) & 1, aborted, p.err);
-                    const float pk = ex2(sc[k] - mu);  // sc = -inf -> 0
-                    l_o += pk;
-                    const uint8_t* vrow = smem + kOffRing + s * kTileBytes;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(vrow + sw128_off(r, c));
-                        oacc[8 * c + 0] = fmaf(pk, bf16lo(w.x), oacc[8 * c + 0]);
-                        oacc[8 * c + 1] = fmaf(pk, bf16hi(w.x), oacc[8 * c + 1]);
-                        oacc[8 * c + 2] = fmaf(pk, bf16lo(w.y), oacc[8 * c + 2]);
-                        oacc[8 * c + 3] = fmaf(pk, bf16hi(w.y), oacc[8 * c + 3]);
-                        oacc[8 * c + 4] = fmaf(pk, bf16lo(w.z), oacc[8 * c + 4]);
-                        oacc[8 * c + 5] = fmaf(pk, bf16hi(w.z), oacc[8 * c + 5]);
-                        oacc[8 * c + 6] = fmaf(pk, bf16lo(w.w), oacc[8 * c + 6]);
-                        oacc[8 * c + 7] = fmaf(pk, bf16hi(w.w), oacc[8 * c + 7]);
-                    }
-                    mbar_arrive(B_EMPTY(s));
-                    ++seq;
-                }
-            }
-        };
-
-        const int nb0 = min(kBatch, n_act);
-        if (nb0 > 0) score_pass(0, nb0);
-
-        // ---- band: masked online softmax over the S groups
+        // ---- band: masked online softmax over the S groups. Only the 32-column chunks that
+        // some row of this warp can reach are read (3 of 6 at W = 64); the rest of P is zero.
         float m_b = -INFINITY, l_b = 0.f;
         for (int g = 0; g < n_groups; ++g) {
             const int nch = min(kMaxGroupChunks, n_chunks - g * kMaxGroupChunks);
             const int32_t kbase = (c_lo + g * kMaxGroupChunks) * kChunk;
+            const int32_t d0 = i - kbase;  // dist(i, key kbase + c) = d0 - c
+            const int32_t wrow = i0 + warp * 32 - kbase;
+            const int32_t colA = max(0, wrow - W + 1);
+            const int32_t colB = min(nch * kChunk - 1, wrow + 31);
+            const int ccA = colA / 32;
+            const int n_need = colA <= colB ? colB / 32 - ccA + 1 : 0;
             mbar_wait(B_S, g & 1, aborted, p.err);
             tc_fence_after();
-            uint32_t v[32];
-            float mx = -INFINITY;
-            for (int cc = 0; cc < nch * 2; ++cc) {
-                tmem_ld32(tmem + lane_base + 32 * cc, v);
+            float mn = m_b;
+            if (n_need <= 3) {
+                uint32_t v[3][32];
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    if (j < n_need) tmem_ld32(tmem + lane_base + 32 * (ccA + j), v[j]);
                 tmem_ld_wait();
+                float mx = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const uint32_t dist = (uint32_t)(i - (kbase + 32 * cc + e));
-                    if (dist < (uint32_t)W) mx = fmaxf(mx, __uint_as_float(v[e]));
-                }
-            }
-            const float mn = fmaxf(m_b, mx == -INFINITY ? -INFINITY : mx * sl2);
-            if (g > 0) {
-                mbar_wait(B_O, (g - 1) & 1, aborted, p.err);
-                tc_fence_after();
-                const float corr = (m_b == -INFINITY) ? 0.f : ex2(m_b - mn);
-                if (__any_sync(0xffffffffu, mn != m_b)) {
-                    for (int h = 0; h < 2; ++h) {
-                        tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
-                        tmem_ld_wait();
+                for (int j = 0; j < 3; ++j) {
+                    if (j < n_need) {
+                        const int32_t dj = d0 - 32 * (ccA + j);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
-                        tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
+                        for (int e = 0; e < 32; ++e) {
+                            const bool ok = (uint32_t)(dj - e) < (uint32_t)W;
+                            const float x = ok ? __uint_as_float(v[j][e]) * sl2 : -INFINITY;
+                            v[j][e] = __float_as_uint(x);
+                            mx = fmaxf(mx, x);
+                        }
                     }
-                    tmem_st_wait();
                 }
-                l_b *= corr;
+                mn = fmaxf(m_b, mx);
+                if (g > 0) {
+                    mbar_wait(B_O, (g - 1) & 1, aborted, p.err);
+                    tc_fence_after();
+                    const float corr = (m_b == -INFINITY) ? 0.f : ex2(m_b - mn);
+                    if (__any_sync(0xffffffffu, mn != m_b)) {
+                        uint32_t o[32];
+                        for (int h = 0; h < 2; ++h) {
+                            tmem_ld32(tmem + lane_base + kTmemO + 32 * h, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+                            tmem_st32(tmem + lane_base + kTmemO + 32 * h, o);
+                        }
+                        tmem_st_wait();
+                    }
+                    l_b *= corr;
+                }
+                const float mu = mn == -INFINITY ? 0.f : mn;
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    if (j < n_need) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = ex2(__uint_as_float(v[j][e]) - mu);
+                            const float p1 = ex2(__uint_as_float(v[j][e + 1]) - mu);
+                            l_b += p0 + p1;
+                            pk[e >> 1] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tmem + lane_base + 16 * (ccA + j), pk);
+                    }
+                }
+                uint32_t zero[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) zero[e] = 0u;
+                for (int cc = 0; cc < nch * 2; ++cc)
+                    if (cc < ccA || cc >= ccA + n_need) tmem_st16(tmem + lane_base + 16 * cc, zero);
+            } else {
+                // general window (more than 96 reachable columns): two passes over TMEM
+                uint32_t v[32];
+                float mx = -INFINITY;
+                for (int j = 0; j < n_need; ++j) {
+                    tmem_ld32(tmem + lane_base + 32 * (ccA + j), v);
+                    tmem_ld_wait();
+                    const int32_t dj = d0 - 32 * (ccA + j);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if ((uint32_t)(dj - e) < (uint32_t)W) mx = fmaxf(mx, __uint_as_float(v[e]) * sl2);
+                }
+                mn = fmaxf(m_b, mx);
+                if (g > 0) {
+                    mbar_wait(B_O, (g - 1) & 1, aborted, p.err);
+                    tc_fence_after();
+                    const float corr = (m_b == -INFINITY) ? 0.f : ex2(m_b - mn);
+                    if (__any_sync(0xffffffffu, mn != m_b)) {
+                        for (int h = 0; h < 2; ++h) {
+                            tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
+                            tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
+                        }
+                        tmem_st_wait();
+                    }
+                    l_b *= corr;
+                }
+                const float mu = mn == -INFINITY ? 0.f : mn;
+                for (int cc = 0; cc < nch * 2; ++cc) {
+                    const int j = cc - ccA;
+                    uint32_t pk[16];
+                    if (j >= 0 && j < n_need) {
+                        tmem_ld32(tmem + lane_base + 32 * cc, v);
+                        tmem_ld_wait();
+                        const int32_t dj = d0 - 32 * cc;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = (uint32_t)(dj - e) < (uint32_t)W
+                                                 ? ex2(__uint_as_float(v[e]) * sl2 - mu) : 0.f;
+                            const float p1 = (uint32_t)(dj - e - 1) < (uint32_t)W
+                                                 ? ex2(__uint_as_float(v[e + 1]) * sl2 - mu) : 0.f;
+                            l_b += p0 + p1;
+                            pk[e >> 1] = pack_bf16x2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                    }
+                    tmem_st16(tmem + lane_base + 16 * cc, pk);
+                }
             }
             m_b = mn;
-            const float mu = m_b == -INFINITY ? 0.f : m_b;
-            for (int cc = 0; cc < nch * 2; ++cc) {
-                tmem_ld32(tmem + lane_base + 32 * cc, v);
-                tmem_ld_wait();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const uint32_t d0 = (uint32_t)(i - (kbase + 32 * cc + e));
-                    const uint32_t d1 = d0 - 1u;
-                    const float p0 = d0 < (uint32_t)W ? ex2(__uint_as_float(v[e]) * sl2 - mu) : 0.f;
-                    const float p1 = d1 < (uint32_t)W ? ex2(__uint_as_float(v[e + 1]) * sl2 - mu) : 0.f;
-                    l_b += p0 + p1;
-                    pk[e >> 1] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tmem + lane_base + 16 * cc, pk);
-            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(B_P);
         }
 
+        // ---- offsets: one pass per offset; the running max starts at the band's max and is
+        // only raised when a score exceeds it by more than 2^8 (bounded growth, rare rescale)
+        uint32_t qw[32];
+        {
+            const uint8_t* qrow = smem + kOffQ;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 w = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
+                qw[4 * c + 0] = w.x; qw[4 * c + 1] = w.y; qw[4 * c + 2] = w.z; qw[4 * c + 3] = w.w;
+            }
+        }
+        float m_o = m_b, l_o = 0.f;
+        float oacc[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) oacc[c] = 0.f;
-        if (nb0 > 0) value_pass(nb0);
-        for (int b0 = kBatch; b0 < n_act; b0 += kBatch) {
-            const int nb = min(kBatch, n_act - b0);
-            score_pass(b0, nb);
-            value_pass(nb);
+        uint32_t seq = 0;
+#pragma unroll 1
+        for (int k = 0; k < n_act; ++k) {
+            const bool valid = i - offs[k] >= 0;
+            int s = seq % kRing;
+            mbar_wait(B_FULL(s), (seq / kRing) & 1, aborted, p.err);
+            const uint8_t* krow = smem + kOffRing + s * kTileBytes;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
+                fma2_bf16(qw[4 * c + 0], w.x, a0, a1);
+                fma2_bf16(qw[4 * c + 1], w.y, a2, a3);
+                fma2_bf16(qw[4 * c + 2], w.z, a0, a1);
+                fma2_bf16(qw[4 * c + 3], w.w, a2, a3);
+            }
+            mbar_arrive(B_EMPTY(s));
+            ++seq;
+            const float sc = valid ? ((a0 + a1) + (a2 + a3)) * sl2 : -INFINITY;
+            if (sc > m_o + 8.f) {
+                const float corr = m_o == -INFINITY ? 0.f : ex2(m_o - sc);
+                l_o *= corr;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) oacc[c] *= corr;
+                m_o = sc;
+            }
+            const float pk = valid ? ex2(sc - m_o) : 0.f;
+            l_o += pk;
+            const uint32_t pb = pack_bf16x2(pk, 0.f);
+            s = seq % kRing;
+            mbar_wait(B_FULL(s), (seq / kRing) & 1, aborted, p.err);
+            const uint8_t* vrow = smem + kOffRing + s * kTileBytes;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 w = *reinterpret_cast<const uint4*>(vrow + sw128_off(r, c));
+                axpy2_bf16(pb, w.x, oacc[8 * c + 0], oacc[8 * c + 1]);
+                axpy2_bf16(pb, w.y, oacc[8 * c + 2], oacc[8 * c + 3]);
+                axpy2_bf16(pb, w.z, oacc[8 * c + 4], oacc[8 * c + 5]);
+                axpy2_bf16(pb, w.w, oacc[8 * c + 6], oacc[8 * c + 7]);
+            }
+            mbar_arrive(B_EMPTY(s));
+            ++seq;
         }
 
         // ---- epilogue: merge the band and offset softmax parts

@@ -250,6 +250,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// c0 += lo(a) * lo(b), c1 += hi(a) * hi(b): bf16 operands, fp32 accumulation (the product
+// of two bf16 values is exact in fp32, so this equals an fp32 FMA of the widened inputs).
+__device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t b, float& c0, float& c1) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "r"(a), "r"(b));
+}
+
+// c0 += p * lo(v), c1 += p * hi(v) with p a bf16 scalar (low half of `p`).
+__device__ __forceinline__ void axpy2_bf16(uint32_t p, uint32_t v, float& c0, float& c1) {
+    asm("{\n\t.reg .b16 pl, ph, vl, vh;\n\tmov.b32 {pl, ph}, %2;\n\tmov.b32 {vl, vh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, pl, vl, %0;\n\tfma.rn.f32.bf16 %1, pl, vh, %1;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "r"(p), "r"(v));
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
