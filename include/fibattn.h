@@ -47,7 +47,8 @@ typedef enum {
     FIBATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (d != 64, unknown dtype) */
     FIBATTN_ERR_CAPACITY = 3,    /* an offset table does not fit the given capacity */
     FIBATTN_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
-    FIBATTN_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (device error word) */
+    FIBATTN_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (device error word) */
+    FIBATTN_ERR_SCRATCH_LIMIT = 6 /* fibattn_bwd_noalloc: call larger than its fixed scratch */
 } fibattn_status;
 
 typedef enum { FIBATTN_BASE_FIB = 0, FIBATTN_BASE_POW2 = 1 } fibattn_base;
@@ -141,6 +142,33 @@ FIBATTN_API fibattn_status fibattn_bwd(const void* q, const void* k, const void*
                            float* delta_ws, int32_t B, int32_t H, int32_t T, int32_t d,
                            int32_t dtype, int32_t W, float scale, const fibattn_schedule* sched,
                            int32_t layer0, int32_t n_layers_call, void* cuda_stream);
+
+/*
+ * fibattn_bwd for callers that cannot allocate device memory. The paper has no
+ * counterpart: this is a deployment variant of the backward above, identical in
+ * arguments, results and errors except that delta_ws is not passed.
+ * Some callers cannot call cudaMalloc: an operator hosted by a framework that owns the
+ * device allocator and hands it no workspace, or a latency-critical loop where
+ * cudaMalloc/cudaFree would synchronise the device. This entry point takes D's scratch
+ * from a fixed file-scope __device__ array of FIBATTN_NOALLOC_MAX_ROWS floats (4 MiB,
+ * held on every GPU that loads the library until the process exits) and allocates
+ * nothing.
+ *   - Calls with n_layers_call * B * H * T > FIBATTN_NOALLOC_MAX_ROWS return
+ *     FIBATTN_ERR_SCRATCH_LIMIT without launching anything.
+ *   - The first call on a device (that device current) looks up the array's device
+ *     address with cudaGetSymbolAddress; make that first call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's contents (every
+ *     entry is rewritten before it is read, so nothing needs clearing). Calls whose
+ *     kernels can overlap on the GPU (unordered streams) race on it.
+ */
+#define FIBATTN_NOALLOC_MAX_ROWS (1 << 20)
+FIBATTN_API fibattn_status fibattn_bwd_noalloc(const void* q, const void* k, const void* v,
+                                               const void* o, const float* lse, const void* dO,
+                                               void* dq, void* dk, void* dv, int32_t B, int32_t H,
+                                               int32_t T, int32_t d, int32_t dtype, int32_t W,
+                                               float scale, const fibattn_schedule* sched,
+                                               int32_t layer0, int32_t n_layers_call,
+                                               void* cuda_stream);
 
 /*
  * The attended key sets of one layer, materialised by a device kernel from the same

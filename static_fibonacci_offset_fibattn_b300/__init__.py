@@ -22,13 +22,14 @@ import torch
 
 __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd",
            "keyset_debug", "poll_device_error", "status_string", "lib", "library_path",
-           "FibSparseAttention", "MAX_OFFSETS"]
+           "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_MAX_ROWS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
 MAX_OFFSETS = 64
 
-OK, INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA_ERR, TIMEOUT = range(6)
+OK, INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA_ERR, TIMEOUT, SCRATCH_LIMIT = range(7)
+NOALLOC_MAX_ROWS = 1 << 20
 _BASES = {"fib": 0, "pow2": 1}
 _KINDS = {"fixed": 0, "linear": 1, "coprime": 2}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
@@ -95,6 +96,8 @@ def lib():
                                   i32, vp]
         L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                   i32, f32, sp, i32, i32, vp]
+        L.fibattn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                          i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_keyset_debug.argtypes = [sp, i32, i32, i32, vp, vp]
         L.fibattn_poll_device_error.argtypes = [vp]
         L.fibattn_status_string.argtypes = [i32]
@@ -108,7 +111,7 @@ def lib():
         L.fibattn_launch_count.argtypes = []
         L.fibattn_launch_count.restype = ctypes.c_int64
         for name in ("fibattn_offsets", "fibattn_offsets_device", "fibattn_fwd", "fibattn_bwd",
-                     "fibattn_keyset_debug", "fibattn_poll_device_error"):
+                     "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -207,6 +210,26 @@ def bwd(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
                            _ptr(dk), _ptr(dv), _ptr(delta), B, H, T, d, _DTYPES[q.dtype], W,
                            float(scale or 0.0), ctypes.byref(s), layer0, Lc, _stream(q))
     _check(st, "fibattn_bwd")
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
+                scale: Optional[float] = None, dq=None, dk=None, dv=None):
+    """Backward for callers that cannot allocate device memory: like bwd(), but the D
+    scratch is the library's fixed per-device array (fibattn_bwd_noalloc), so no delta
+    buffer is needed. Rejects Lc*B*H*T > NOALLOC_MAX_ROWS (FibAttnError SCRATCH_LIMIT).
+    The first call on a device should come before any stream capture; calls whose
+    kernels overlap on the GPU share the one scratch array and race."""
+    Lc, B, H, T, d = _shape(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _check_tensors(q, k, v, o, dO, dq, dk, dv)
+    s = sched.to_c()
+    st = lib().fibattn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H, T, d, _DTYPES[q.dtype], W,
+                                   float(scale or 0.0), ctypes.byref(s), layer0, Lc, _stream(q))
+    _check(st, "fibattn_bwd_noalloc")
     return dq, dk, dv
 
 

@@ -54,6 +54,7 @@ const char* fibattn_status_string(fibattn_status s) {
         case FIBATTN_ERR_CAPACITY: return "offset table exceeds capacity";
         case FIBATTN_ERR_CUDA: return "CUDA error";
         case FIBATTN_ERR_TIMEOUT: return "kernel wait timed out";
+        case FIBATTN_ERR_SCRATCH_LIMIT: return "call exceeds the fixed no-allocation scratch size";
     }
     return "unknown status";
 }

@@ -160,3 +160,14 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fwd(q, q, q, 4, fa.Schedule())
+
+
+def test_bwd_noalloc_rejects_oversize_on_the_host():
+    # rows = Lc*B*H*T above the fixed scratch: SCRATCH_LIMIT, decided before any CUDA call
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    ok = ctypes.c_void_p(256)
+    st = L.fibattn_bwd_noalloc(*([ok] * 9), 1, 1, fa.NOALLOC_MAX_ROWS + 1, 64, 1, 4, 0.0,
+                               ctypes.byref(sc), 0, 1, None)
+    assert st == fa.SCRATCH_LIMIT
+    assert "scratch" in fa.status_string(fa.SCRATCH_LIMIT)
