@@ -43,17 +43,17 @@ ALGO_BYTES = {
     "fwd_tc_bf16": 3 * 128 + 128 + 4,          # q, k, v in; o, lse out
     "fwd_simt_bf16": 3 * 128 + 128 + 4,
     "fwd_simt_f32": 3 * 256 + 256 + 4,
-    "bwd_delta_simt": 2 * 128 + 4,              # o, dO in; D out
-    "bwd_delta": 2 * 128 + 4,
-    "bwd_dq_simt": 4 * 128 + 8 + 128,           # q, k, v, dO, lse, D in; dq out
-    "bwd_dkdv_simt": 4 * 128 + 8 + 2 * 128,     # q, k, v, dO, lse, D in; dk, dv out
-    "bwd_fused_tc": 5 * 128 + 8 + 3 * 128,      # q, k, v, o, dO, lse, D in; dq, dk, dv out
+    "bwd_delta_simt": 2 * 256 + 4,              # fp32: o, dO in; D out
+    "bwd_dq_simt": 4 * 256 + 8 + 256,           # fp32: q, k, v, dO, lse, D in; dq out
+    "bwd_dkdv_simt": 4 * 256 + 8 + 2 * 256,     # fp32: q, k, v, dO, lse, D in; dk, dv out
+    "bwd_dq_tc": 5 * 128 + 4 + 128,             # q, k, v, o, dO, lse in; dq out
+    "bwd_dkdv_tc": 4 * 128 + 4 + 2 * 128,       # q, k, v, dO, lse in; dk, dv out
 }
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
     "bwd_delta_simt": "simt.cu", "bwd_dq_simt": "simt.cu", "bwd_dkdv_simt": "simt.cu",
-    "bwd_delta": "bwd_tc.cu", "bwd_fused_tc": "bwd_tc.cu",
+    "bwd_dq_tc": "bwd_tc.cu", "bwd_dkdv_tc": "bwd_tc.cu",
 }
 
 
@@ -116,29 +116,41 @@ def committed_traffic(kernel):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling (every 50 ms, host-timestamped) around the timed region.
+
+    The sampler starts before the warm-up so that it is running when the timed region
+    begins; summary() keeps the samples whose timestamps fall inside the marked window,
+    or, when the window is shorter than the sampling period, the nearest sample on each
+    side of it (reported as samples_in_window = 0)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.window = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
 
-    def __enter__(self):
+    def start(self):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                          f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
 
-    def __exit__(self, *a):
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
         if self.proc is not None:
+            time.sleep(0.12)  # one more sample after the window
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -147,26 +159,34 @@ class Clocks:
             self.fh.close()
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
+        import datetime
+        if self.proc is None or not os.path.exists(self.path) or self.window is None:
             return None
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                sm.append(float(p[1]))
-                smax = float(p[2])
+                t = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((t, float(p[2]), float(p[3]),
+                             {n for n, v in zip(names, p[6:10]) if v.lower().startswith("active")}))
             except ValueError:
                 continue
-            for n, v in zip(names, p[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        t0, t1 = self.window
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        picked = inside
+        if not picked:
+            before = [r for r in rows if r[0] < t0]
+            after = [r for r in rows if r[0] > t1]
+            picked = ([before[-1]] if before else []) + ([after[0]] if after else [])
+        reasons = set().union(*(r[3] for r in picked)) if picked else set()
+        return {"sm_mhz": statistics.median(r[1] for r in picked), "sm_max_mhz": picked[-1][2],
+                "reasons": sorted(reasons), "samples_in_window": len(inside),
+                "samples_used": len(picked), "window_ms": round((t1 - t0) * 1e3, 2)}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -186,7 +206,8 @@ def run_ours(a, spec, world, rank, local):
     lse = torch.empty(d_in["q"].shape[:-1], dtype=torch.float32, device=dev)
     if train:
         dq, dk, dv = (torch.empty_like(d_in["q"]) for _ in range(3))
-        delta = torch.empty_like(lse)
+        ws = torch.empty(max(1, fa.bwd_workspace_size(d_in["q"], W, sched)), dtype=torch.uint8,
+                         device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -195,8 +216,9 @@ def run_ours(a, spec, world, rank, local):
         fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
         if train:
             fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched, dq=dq, dk=dk, dv=dv,
-                   delta=delta)
+                   workspace=ws)
 
+    clk = Clocks(clock_index(local)).start()
     for _ in range(a.warmup):
         step(d_in)
         flush.fill_(1.0)
@@ -213,13 +235,15 @@ def run_ours(a, spec, world, rank, local):
     n0 = L.fibattn_launch_count()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(a.steps)]
-    with Clocks(clock_index(local)) as clk:
-        for s, e in evs:
-            s.record(stream)
-            step(d_in)
-            e.record(stream)
-            flush.fill_(1.0)
-        torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    for s, e in evs:
+        s.record(stream)
+        step(d_in)
+        e.record(stream)
+        flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+    clk.mark(t_host0, time.time())
+    clk.stop()
     launches = L.fibattn_launch_count() - n0
     L.fibattn_profile_enable(0)
     names = ctypes.create_string_buffer(64 * 32)

@@ -13,10 +13,11 @@
  *
  * Conventions shared by every entry point:
  *   - All tensors are dense, contiguous, row-major [Lc][B][H][T][d] (Lc = layers in
- *     the call); lse and delta are [Lc][B][H][T] float32, natural log. Call-layer c
+ *     the call); lse is [Lc][B][H][T] float32, natural log. Call-layer c
  *     uses schedule layer (layer0 + c).
  *   - The caller owns every buffer; the library allocates no device memory apart
- *     from a 4-byte device error word. Device pointers must be 16-byte aligned.
+ *     from a 4-byte device error word and the fixed scratch array of
+ *     fibattn_bwd_noalloc (both static). Device pointers must be 16-byte aligned.
  *   - Work is enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default
  *     stream) and returns once launched; results are ready when the stream is.
  *   - Nothing is printed. Errors are returned as fibattn_status; kernel-side
@@ -48,7 +49,7 @@ typedef enum {
     FIBATTN_ERR_CAPACITY = 3,    /* an offset table does not fit the given capacity */
     FIBATTN_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
     FIBATTN_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (device error word) */
-    FIBATTN_ERR_SCRATCH_LIMIT = 6 /* fibattn_bwd_noalloc: call larger than its fixed scratch */
+    FIBATTN_ERR_SCRATCH_LIMIT = 6 /* fibattn_bwd_noalloc: workspace larger than its fixed array */
 } fibattn_status;
 
 typedef enum { FIBATTN_BASE_FIB = 0, FIBATTN_BASE_POW2 = 1 } fibattn_base;
@@ -128,40 +129,60 @@ FIBATTN_API fibattn_status fibattn_fwd(const void* q, const void* k, const void*
                            int32_t n_layers_call, void* cuda_stream);
 
 /*
+ * Workspace the backward needs for one call, in bytes (write it to *bytes):
+ *   D [Lc][B][H][T] float32 (D_i = dO_i . o_i), rounded up to 256 bytes, and for bf16
+ *   calls the (P, dS) pair of every (query, offset) diagonal entry,
+ *   [Lc][B][H][n_max][T] of 4 bytes (two bf16), n_max = the largest table size among the
+ *   call's layers at this (W, T).
+ * Errors: INVALID_ARG, UNSUPPORTED and CAPACITY as fibattn_bwd (same checks).
+ */
+FIBATTN_API fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int32_t T, int32_t d,
+                                                      int32_t dtype, int32_t W,
+                                                      const fibattn_schedule* sched,
+                                                      int32_t layer0, int32_t n_layers_call,
+                                                      uint64_t* bytes);
+
+/*
  * Backward from the saved forward (the analytic gradient of softmax attention over S_i):
  *   D_i = dO_i . o_i,  P_ij = exp(scale q_i.k_j - lse_i),  dS_ij = P_ij (dO_i . v_j - D_i),
  *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dO_i.
  *   q, k, v, o, dO : inputs as in fibattn_fwd; lse : the forward's lse.
  *   dq, dk, dv     : written (every element; no accumulation into old contents).
- *   delta_ws       : float32 [Lc][B][H][T] device scratch owned by the caller (holds D).
- * No atomics: each dk/dv row is summed by the one thread block that owns it.
- * Errors as fibattn_fwd.
+ *   workspace      : device scratch owned by the caller, 256-byte aligned, at least
+ *                    fibattn_bwd_workspace_size() bytes (workspace_bytes says how many);
+ *                    every byte read is first written by the same call.
+ * bf16 runs two tcgen05 tensor-core kernels (query owner: D and dq; key owner: dk, dv);
+ * f32 runs SIMT kernels. No atomics: each dq/dk/dv row is summed by the one thread block
+ * that owns it.
+ * Errors as fibattn_fwd, plus INVALID_ARG when workspace_bytes is too small.
  */
 FIBATTN_API fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                           float* delta_ws, int32_t B, int32_t H, int32_t T, int32_t d,
-                           int32_t dtype, int32_t W, float scale, const fibattn_schedule* sched,
-                           int32_t layer0, int32_t n_layers_call, void* cuda_stream);
+                           void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
+                           int32_t T, int32_t d, int32_t dtype, int32_t W, float scale,
+                           const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call,
+                           void* cuda_stream);
 
 /*
  * fibattn_bwd for callers that cannot allocate device memory. The paper has no
  * counterpart: this is a deployment variant of the backward above, identical in
- * arguments, results and errors except that delta_ws is not passed.
+ * arguments, results and errors except that no workspace is passed.
  * Some callers cannot call cudaMalloc: an operator hosted by a framework that owns the
  * device allocator and hands it no workspace, or a latency-critical loop where
- * cudaMalloc/cudaFree would synchronise the device. This entry point takes D's scratch
- * from a fixed file-scope __device__ array of FIBATTN_NOALLOC_MAX_ROWS floats (4 MiB,
- * held on every GPU that loads the library until the process exits) and allocates
- * nothing.
- *   - Calls with n_layers_call * B * H * T > FIBATTN_NOALLOC_MAX_ROWS return
- *     FIBATTN_ERR_SCRATCH_LIMIT without launching anything.
+ * cudaMalloc/cudaFree would synchronise the device. This entry point takes the backward's
+ * workspace from a fixed file-scope __device__ array of FIBATTN_NOALLOC_SCRATCH_BYTES
+ * (32 MiB, held on every GPU that loads the library until the process exits) and
+ * allocates nothing.
+ *   - Calls whose fibattn_bwd_workspace_size() exceeds FIBATTN_NOALLOC_SCRATCH_BYTES
+ *     return FIBATTN_ERR_SCRATCH_LIMIT without launching anything. The 16-layer
+ *     B=8, H=8, T=1024, W=64 bf16 training step (28 MiB) fits.
  *   - The first call on a device (that device current) looks up the array's device
  *     address with cudaGetSymbolAddress; make that first call before any stream capture.
  *   - All calls on a device share the array and it keeps the last call's contents (every
- *     entry is rewritten before it is read, so nothing needs clearing). Calls whose
- *     kernels can overlap on the GPU (unordered streams) race on it.
+ *     byte the backward reads is written earlier in the same call, so nothing needs
+ *     clearing). Calls whose kernels can overlap on the GPU (unordered streams) race on it.
  */
-#define FIBATTN_NOALLOC_MAX_ROWS (1 << 20)
+#define FIBATTN_NOALLOC_SCRATCH_BYTES (32ull << 20)
 FIBATTN_API fibattn_status fibattn_bwd_noalloc(const void* q, const void* k, const void* v,
                                                const void* o, const float* lse, const void* dO,
                                                void* dq, void* dk, void* dv, int32_t B, int32_t H,
@@ -201,6 +222,13 @@ FIBATTN_API const char* fibattn_status_string(fibattn_status status);
 FIBATTN_API fibattn_status fibattn_profile_enable(int32_t on);
 FIBATTN_API int32_t fibattn_profile_read(char* names, int32_t name_len, double* total_ms,
                                          int64_t* launches, int32_t cap);
+
+/*
+ * The cudaError_t value behind the most recent FIBATTN_ERR_CUDA returned by any call in
+ * the process (0 if none yet), and in *where (if not NULL) a static text naming the
+ * CUDA call that failed (-1 for a tensor-map encoding the driver rejected).
+ */
+FIBATTN_API int32_t fibattn_last_cuda_error(const char** where);
 
 /* Kernels launched by the library since it was loaded (always counted). */
 FIBATTN_API int64_t fibattn_launch_count(void);

@@ -22,14 +22,15 @@ import torch
 
 __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd",
            "keyset_debug", "poll_device_error", "status_string", "lib", "library_path",
-           "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_MAX_ROWS"]
+           "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+           "bwd_workspace_size", "last_cuda_error"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
 MAX_OFFSETS = 64
 
 OK, INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA_ERR, TIMEOUT, SCRATCH_LIMIT = range(7)
-NOALLOC_MAX_ROWS = 1 << 20
+NOALLOC_SCRATCH_BYTES = 32 << 20
 _BASES = {"fib": 0, "pow2": 1}
 _KINDS = {"fixed": 0, "linear": 1, "coprime": 2}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
@@ -37,7 +38,12 @@ _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 class FibAttnError(RuntimeError):
     def __init__(self, status: int, where: str):
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        msg = f"{where}: {status_string(status)} (status {status})"
+        self.cuda_error = None
+        if status == CUDA_ERR:
+            self.cuda_error, call = last_cuda_error()
+            msg += f"; CUDA error {self.cuda_error} in {call}"
+        super().__init__(msg)
         self.status = status
 
 
@@ -94,8 +100,11 @@ def lib():
         L.fibattn_offsets_device.argtypes = [sp, i32, i32, i32, i32, vp, vp, vp]
         L.fibattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, sp, i32,
                                   i32, vp]
-        L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
-                                  i32, f32, sp, i32, i32, vp]
+        u64 = ctypes.c_uint64
+        L.fibattn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, sp, i32, i32,
+                                                 ctypes.POINTER(u64)]
+        L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32, i32,
+                                  i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_keyset_debug.argtypes = [sp, i32, i32, i32, vp, vp]
@@ -108,13 +117,23 @@ def lib():
         L.fibattn_profile_read.argtypes = [ctypes.c_char_p, i32, ctypes.POINTER(ctypes.c_double),
                                            ctypes.POINTER(ctypes.c_int64), i32]
         L.fibattn_profile_read.restype = i32
+        L.fibattn_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
+        L.fibattn_last_cuda_error.restype = i32
         L.fibattn_launch_count.argtypes = []
         L.fibattn_launch_count.restype = ctypes.c_int64
         for name in ("fibattn_offsets", "fibattn_offsets_device", "fibattn_fwd", "fibattn_bwd",
+                     "fibattn_bwd_workspace_size",
                      "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
+
+
+def last_cuda_error() -> Tuple[int, str]:
+    """(cudaError_t value, failing call) behind the most recent CUDA_ERR status."""
+    where = ctypes.c_char_p()
+    code = lib().fibattn_last_cuda_error(ctypes.byref(where))
+    return int(code), (where.value or b"").decode()
 
 
 def status_string(status: int) -> str:
@@ -195,29 +214,49 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, sched: Schedu
     return o, lse
 
 
+def bwd_workspace_size(q: torch.Tensor, W: int, sched: Schedule, layer0: int = 0) -> int:
+    """Bytes of device workspace fibattn_bwd needs for tensors shaped like q."""
+    Lc, B, H, T, d = _shape(q)
+    if q.dtype not in _DTYPES:
+        raise ValueError("dtype must be float32 or bfloat16")
+    n = ctypes.c_uint64(0)
+    s = sched.to_c()
+    _check(lib().fibattn_bwd_workspace_size(B, H, T, d, _DTYPES[q.dtype], W, ctypes.byref(s),
+                                            layer0, Lc, ctypes.byref(n)),
+           "fibattn_bwd_workspace_size")
+    return int(n.value)
+
+
 def bwd(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
-        scale: Optional[float] = None, dq=None, dk=None, dv=None, delta=None):
-    """Sparse attention backward from the saved forward; returns (dq, dk, dv)."""
+        scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None):
+    """Sparse attention backward from the saved forward; returns (dq, dk, dv).
+    workspace: optional uint8 device tensor of at least bwd_workspace_size() bytes."""
     Lc, B, H, T, d = _shape(q)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
     _check_tensors(q, k, v, o, dO, dq, dk, dv)
-    if delta is None:
-        delta = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    need = bwd_workspace_size(q, W, sched, layer0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on q's device")
     s = sched.to_c()
     st = lib().fibattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
-                           _ptr(dk), _ptr(dv), _ptr(delta), B, H, T, d, _DTYPES[q.dtype], W,
-                           float(scale or 0.0), ctypes.byref(s), layer0, Lc, _stream(q))
+                           _ptr(dk), _ptr(dv), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), B, H, T, d,
+                           _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0, Lc,
+                           _stream(q))
     _check(st, "fibattn_bwd")
     return dq, dk, dv
 
 
 def bwd_noalloc(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
                 scale: Optional[float] = None, dq=None, dk=None, dv=None):
-    """Backward for callers that cannot allocate device memory: like bwd(), but the D
-    scratch is the library's fixed per-device array (fibattn_bwd_noalloc), so no delta
-    buffer is needed. Rejects Lc*B*H*T > NOALLOC_MAX_ROWS (FibAttnError SCRATCH_LIMIT).
+    """Backward for callers that cannot allocate device memory: like bwd(), but the
+    workspace is the library's fixed per-device array (fibattn_bwd_noalloc), so none is
+    passed. Rejects calls whose workspace exceeds NOALLOC_SCRATCH_BYTES (FibAttnError
+    SCRATCH_LIMIT).
     The first call on a device should come before any stream capture; calls whose
     kernels overlap on the GPU share the one scratch array and race."""
     Lc, B, H, T, d = _shape(q)

@@ -40,6 +40,32 @@ fibattn_status check_common(int32_t B, int32_t H, int32_t T, int32_t d, int32_t 
 
 size_t elt_size(int32_t dtype) { return dtype == FIBATTN_F32 ? 4 : 2; }
 
+// Layout of the backward workspace: D first, then (bf16 path) the (P, dS) pairs.
+struct BwdWorkspace {
+    uint64_t pds_offset;  // bytes
+    uint64_t total;       // bytes
+    int32_t n_max;        // table entries per layer slot of the pairs array
+};
+
+// Callers have validated the arguments (check_common), so every table builds.
+BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t dtype, int32_t W,
+                           const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
+    int32_t n_max = 0;
+    for (int32_t c = 0; c < n_layers_call; ++c) {
+        Alpha a;
+        int32_t n = 0;
+        if (layer_alpha(sched, layer0 + c, &a) == FIBATTN_OK &&
+            build_table(sched, a, W, T, nullptr, 0, &n) != FIBATTN_ERR_INVALID_ARG)
+            n_max = n > n_max ? n : n_max;
+    }
+    const uint64_t rows = (uint64_t)n_layers_call * B * H * T;
+    BwdWorkspace ws;
+    ws.pds_offset = (rows * 4 + 255) & ~(uint64_t)255;
+    ws.n_max = dtype == FIBATTN_BF16 ? n_max : 0;
+    ws.total = ws.pds_offset + rows * (uint64_t)ws.n_max * 4;
+    return ws;
+}
+
 }  // namespace
 
 extern "C" {
@@ -132,16 +158,34 @@ fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o,
     return FIBATTN_OK;
 }
 
-fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
-                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                           float* delta_ws, int32_t B, int32_t H, int32_t T, int32_t d,
-                           int32_t dtype, int32_t W, float scale, const fibattn_schedule* sched,
-                           int32_t layer0, int32_t n_layers_call, void* cuda_stream) {
-    const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta_ws};
-    for (const void* p : ptrs)
-        if (!p || !aligned16(p)) return FIBATTN_ERR_INVALID_ARG;
+fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int32_t T, int32_t d,
+                                          int32_t dtype, int32_t W, const fibattn_schedule* sched,
+                                          int32_t layer0, int32_t n_layers_call, uint64_t* bytes) {
+    if (!bytes) return FIBATTN_ERR_INVALID_ARG;
     fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (st != FIBATTN_OK) return st;
+    const BwdWorkspace ws = bwd_workspace(B, H, T, dtype, W, sched, layer0, n_layers_call);
+    *bytes = ws.total;
+    return FIBATTN_OK;
+}
+
+fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
+                           int32_t T, int32_t d, int32_t dtype, int32_t W, float scale,
+                           const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call,
+                           void* cuda_stream) {
+    const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return FIBATTN_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FIBATTN_ERR_INVALID_ARG;
+    fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
+    if (st != FIBATTN_OK) return st;
+    const BwdWorkspace ws = bwd_workspace(B, H, T, dtype, W, sched, layer0, n_layers_call);
+    if (workspace_bytes < ws.total) return FIBATTN_ERR_INVALID_ARG;
+    float* delta = static_cast<float*>(workspace);
+    uint32_t* pds = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.pds_offset);
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
     const int64_t per_layer = (int64_t)B * H * T;
     const size_t es = elt_size(dtype);
@@ -153,24 +197,40 @@ fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const vo
         AttnShape sh{(int64_t)B * H, T, W, scale, n};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t loff = (size_t)c * per_layer;
-        st = launch_bwd((const char*)q + off, (const char*)k + off, (const char*)v + off,
-                        (const char*)o + off, lse + loff, (const char*)dO + off, (char*)dq + off,
-                        (char*)dk + off, (char*)dv + off, delta_ws + loff, sh, t, dtype,
-                        as_stream(cuda_stream));
+        if (dtype == FIBATTN_F32) {
+            st = launch_bwd_simt_f32((const float*)((const char*)q + off),
+                                     (const float*)((const char*)k + off),
+                                     (const float*)((const char*)v + off),
+                                     (const float*)((const char*)o + off), lse + loff,
+                                     (const float*)((const char*)dO + off),
+                                     (float*)((char*)dq + off), (float*)((char*)dk + off),
+                                     (float*)((char*)dv + off), delta + loff, sh, t,
+                                     as_stream(cuda_stream));
+        } else {
+            st = launch_bwd_tc_bf16((const char*)q + off, (const char*)k + off,
+                                    (const char*)v + off, (const char*)o + off, lse + loff,
+                                    (const char*)dO + off, (char*)dq + off, (char*)dk + off,
+                                    (char*)dv + off, delta + loff, pds + loff * ws.n_max,
+                                    ws.n_max, sh, t, as_stream(cuda_stream));
+        }
         if (st != FIBATTN_OK) return st;
     }
     return FIBATTN_OK;
 }
 
 fibattn_status fibattn_poll_device_error(void* cuda_stream) {
-    if (cudaStreamSynchronize(as_stream(cuda_stream)) != cudaSuccess) return FIBATTN_ERR_CUDA;
-    if (cudaPeekAtLastError() != cudaSuccess) return FIBATTN_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(as_stream(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaStreamSynchronize");
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaPeekAtLastError");
     int32_t* w = device_error_word();
-    if (!w) return FIBATTN_ERR_CUDA;
+    if (!w) return cuda_fail(-1, "cudaGetSymbolAddress (error word)");
     int32_t h = 0;
-    if (cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FIBATTN_ERR_CUDA;
+    e = cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaMemcpy (error word)");
     if (h != kDevErrNone) {
-        if (cudaMemset(w, 0, sizeof(int32_t)) != cudaSuccess) return FIBATTN_ERR_CUDA;
+        e = cudaMemset(w, 0, sizeof(int32_t));
+        if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaMemset (error word)");
         return FIBATTN_ERR_TIMEOUT;
     }
     return FIBATTN_OK;

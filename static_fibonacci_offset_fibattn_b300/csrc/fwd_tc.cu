@@ -23,13 +23,13 @@
 // Epilogue: O = (O_band 2^(m_b-m) + O_off 2^(m_o-m)) / l, staged to smem, TMA-stored;
 //   lse = (m + log2 l) ln 2.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "internal.h"
 #include "tc_prims.cuh"
+#include "tmap.h"
 
 namespace fibattn {
 namespace {
@@ -432,35 +432,6 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
     }
 }
 
-// ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// [slices][T][64] bf16, box 64 x 64 rows, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)slices};
-    cuuint64_t strides[2] = {128, (cuuint64_t)T * 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)kChunk, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -471,12 +442,17 @@ fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, v
     const int64_t gx = (int64_t)tiles * sh.slices_per_layer;
     if (gx > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     FwdParams P;
-    if (!make_map(&P.tm_q, q, slices, sh.T) || !make_map(&P.tm_k, k, slices, sh.T) ||
-        !make_map(&P.tm_v, v, slices, sh.T) || !make_map(&P.tm_o, o, slices, sh.T))
-        return FIBATTN_ERR_CUDA;
-    P.lse = lse;
+    // the error-word lookup is a runtime call: it binds the device's primary context to this
+    // thread (a fresh thread may have none), which the tensor-map encoding below needs
     P.err = device_error_word();
-    if (!P.err) return FIBATTN_ERR_CUDA;
+    if (!P.err) return cuda_fail(-1, "cudaGetSymbolAddress (error word)");
+    const void* bases[4] = {q, k, v, o};
+    CUtensorMap* maps[4] = {&P.tm_q, &P.tm_k, &P.tm_v, &P.tm_o};
+    for (int m = 0; m < 4; ++m) {
+        const int r = make_bf16_rows_map(maps[m], bases[m], slices, sh.T);
+        if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (fwd)");
+    }
+    P.lse = lse;
     P.slices_per_layer = sh.slices_per_layer;
     P.T = sh.T;
     P.W = sh.W;
@@ -484,13 +460,14 @@ fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, v
     P.scale_log2 = sh.scale * 1.4426950408889634f;
     P.tabs = t;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FIBATTN_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaGetDevice");
     static bool attr_set[64] = {};
     if (dev < 0 || dev >= 64) return FIBATTN_ERR_UNSUPPORTED;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemAlloc) != cudaSuccess)
-            return FIBATTN_ERR_CUDA;
+        e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemAlloc);
+        if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaFuncSetAttribute (fwd)");
         attr_set[dev] = true;
     }
     dim3 grid((unsigned)gx, sh.n_layers);
@@ -498,7 +475,7 @@ fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, v
         KernelScope ks("fwd_tc_bf16", st);
         fwd_tc_kernel<<<grid, kThreads, kSmemAlloc, st>>>(P);
     }
-    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+    return launch_status("launch fwd_tc_bf16");
 }
 
 }  // namespace fibattn

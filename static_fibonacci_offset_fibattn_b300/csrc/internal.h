@@ -50,6 +50,12 @@ class KernelScope {
     int rec_;
 };
 
+// Records a failed CUDA call (error code and a static description of the call) for
+// fibattn_last_cuda_error and returns FIBATTN_ERR_CUDA.
+fibattn_status cuda_fail(int32_t code, const char* where);
+// Status of the kernel launch just issued on this thread: OK, or a recorded CUDA failure.
+fibattn_status launch_status(const char* where);
+
 // Device error word protocol (see fibattn_poll_device_error).
 enum DeviceError : int32_t { kDevErrNone = 0, kDevErrTimeout = 1 };
 int32_t* device_error_word();  // device address of the error word (current device)
@@ -77,9 +83,18 @@ fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v,
                                     cudaStream_t st);
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
-fibattn_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
-                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                          float* delta, const AttnShape& sh, const OffsetTables& t, int32_t dtype,
-                          cudaStream_t st);
+// SIMT backward (fp32 path): D into `delta`, then dQ, then dK/dV.
+fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* v, const float* o,
+                                   const float* lse, const float* dO, float* dq, float* dk,
+                                   float* dv, float* delta, const AttnShape& sh,
+                                   const OffsetTables& t, cudaStream_t st);
+
+// Tensor-core backward (bf16 path). Workspace: delta [slices][T] fp32 and pds
+// [slices][n_max][T] (P, dS) bf16 pairs, n_max >= every launch layer's table size.
+int32_t bwd_tc_n_max(const OffsetTables& t, int32_t n_layers);
+fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                  float* delta, uint32_t* pds, int32_t n_max, const AttnShape& sh,
+                                  const OffsetTables& t, cudaStream_t st);
 
 }  // namespace fibattn

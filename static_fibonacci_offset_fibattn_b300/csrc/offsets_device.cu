@@ -137,7 +137,7 @@ fibattn_status launch_offsets_device(const fibattn_schedule* s, int32_t layer0, 
     int blocks = (n + threads - 1) / threads;
     KernelScope ks("offsets_device", st);
     build_tables_kernel<<<blocks, threads, 0, st>>>(ds, layer0, n, W, T, d_tables, d_counts);
-    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+    return launch_status("launch offsets kernel");
 }
 
 fibattn_status launch_keyset(const OffsetTables& t, int32_t W, int32_t T, uint32_t* d_mask,
@@ -148,7 +148,7 @@ fibattn_status launch_keyset(const OffsetTables& t, int32_t W, int32_t T, uint32
     if (blocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     KernelScope ks("keyset_debug", st);
     keyset_kernel<<<(unsigned)blocks, threads, 0, st>>>(t, W, T, d_mask);
-    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+    return launch_status("launch offsets kernel");
 }
 
 }  // namespace fibattn

@@ -37,6 +37,8 @@ Profiler& prof() {
 }
 
 std::atomic<long long> g_launches{0};
+std::atomic<int32_t> g_last_cuda_error{0};
+std::atomic<const char*> g_last_cuda_where{""};
 
 cudaEvent_t take_event(Profiler& p) {
     if (!p.pool.empty()) {
@@ -59,6 +61,17 @@ int kernel_id(Profiler& p, const char* name) {
 }
 
 }  // namespace
+
+fibattn_status cuda_fail(int32_t code, const char* where) {
+    g_last_cuda_error.store(code, std::memory_order_relaxed);
+    g_last_cuda_where.store(where, std::memory_order_relaxed);
+    return FIBATTN_ERR_CUDA;
+}
+
+fibattn_status launch_status(const char* where) {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FIBATTN_OK : cuda_fail((int32_t)e, where);
+}
 
 KernelScope::KernelScope(const char* name, cudaStream_t st) : st_(st), rec_(-1) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -96,6 +109,11 @@ FIBATTN_API fibattn_status fibattn_profile_enable(int32_t on) {
 }
 
 FIBATTN_API int64_t fibattn_launch_count(void) { return g_launches.load(); }
+
+FIBATTN_API int32_t fibattn_last_cuda_error(const char** where) {
+    if (where) *where = g_last_cuda_where.load(std::memory_order_relaxed);
+    return g_last_cuda_error.load(std::memory_order_relaxed);
+}
 
 FIBATTN_API int32_t fibattn_profile_read(char* names, int32_t name_len, double* total_ms,
                                          int64_t* launches, int32_t cap) {

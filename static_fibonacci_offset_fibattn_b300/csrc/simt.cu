@@ -205,7 +205,7 @@ fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* 
     dim3 grid((unsigned)blocks, sh.n_layers);
     KernelScope ks("fwd_simt_f32", st);
     fwd_simt_kernel<float><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, o, lse, sh, t);
-    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+    return launch_status("launch SIMT kernel");
 }
 
 fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v, void* o,
@@ -219,7 +219,7 @@ fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v,
     KernelScope ks("fwd_simt_bf16", st);
     fwd_simt_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(
         (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
-    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+    return launch_status("launch SIMT kernel");
 }
 
 template <typename E>
@@ -244,20 +244,14 @@ static fibattn_status bwd_typed(const E* q, const E* k, const E* v, const E* o, 
         KernelScope ks("bwd_dkdv_simt", st);
         bwd_dkdv_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dk, dv, sh, t);
     }
-    return cudaGetLastError() == cudaSuccess ? FIBATTN_OK : FIBATTN_ERR_CUDA;
+    return launch_status("launch SIMT kernel");
 }
 
-fibattn_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
-                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                          float* delta, const AttnShape& sh, const OffsetTables& t, int32_t dtype,
-                          cudaStream_t st) {
-    if (dtype == FIBATTN_F32)
-        return bwd_typed<float>((const float*)q, (const float*)k, (const float*)v, (const float*)o,
-                                lse, (const float*)dO, (float*)dq, (float*)dk, (float*)dv, delta,
-                                sh, t, st);
-    typedef __nv_bfloat16 E;
-    return bwd_typed<E>((const E*)q, (const E*)k, (const E*)v, (const E*)o, lse, (const E*)dO,
-                        (E*)dq, (E*)dk, (E*)dv, delta, sh, t, st);
+fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* v, const float* o,
+                                   const float* lse, const float* dO, float* dq, float* dk,
+                                   float* dv, float* delta, const AttnShape& sh,
+                                   const OffsetTables& t, cudaStream_t st) {
+    return bwd_typed<float>(q, k, v, o, lse, dO, dq, dk, dv, delta, sh, t, st);
 }
 
 }  // namespace fibattn

@@ -146,14 +146,43 @@ def test_bwd_validates_before_launch():
     L = fa.lib()
     sc = fa.Schedule().to_c()
     ok = ctypes.c_void_p(256)
+    big = ctypes.c_uint64(1 << 40)
     args = [ok] * 10
     for bad in range(10):
         a = list(args)
         a[bad] = ctypes.c_void_p(0)
-        assert L.fibattn_bwd(*a, 1, 1, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
+        assert L.fibattn_bwd(*a, big, 1, 1, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
                              None) == fa.INVALID_ARG
-    assert L.fibattn_bwd(*args, 1, 1, 8, 32, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
+    assert L.fibattn_bwd(*args, big, 1, 1, 8, 32, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
                          None) == fa.UNSUPPORTED
+    # a workspace that is not 256-byte aligned, or too small, is rejected before any launch
+    a = list(args)
+    a[9] = ctypes.c_void_p(256 + 16)
+    assert L.fibattn_bwd(*a, big, 1, 1, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
+                         None) == fa.INVALID_ARG
+    assert L.fibattn_bwd(*args, ctypes.c_uint64(16), 1, 1, 8, 64, 1, 4, 0.0, ctypes.byref(sc),
+                         0, 1, None) == fa.INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("shape", [(1, 2, 256, 16), (8, 8, 1024, 64), (2, 8, 4096, 64),
+                                   (3, 1, 777, 6)])
+def test_bwd_workspace_size_layout(dtype, shape):
+    # D (4 bytes per row, rounded up to 256) and, for bf16, one 4-byte (P, dS) pair per
+    # row and table slot, n_max = the largest of the call's tables (from the oracle)
+    B, H, T, W = shape
+    sched = dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16,
+                 coprime_c=5)
+    sc = fa.Schedule(**sched).to_c()
+    n = ctypes.c_uint64(0)
+    for layer0, Lc in ((0, 16), (3, 5), (15, 1)):
+        assert fa.lib().fibattn_bwd_workspace_size(B, H, T, 64, dtype, W, ctypes.byref(sc),
+                                                   layer0, Lc, ctypes.byref(n)) == fa.OK
+        rows = Lc * B * H * T
+        sc_py = fa.Schedule(**sched)
+        n_max = max(len(_sched_to_oracle(sc_py, l, W, T)) for l in range(layer0, layer0 + Lc))
+        want = (rows * 4 + 255) // 256 * 256 + (rows * n_max * 4 if dtype == 1 else 0)
+        assert n.value == want
 
 
 def test_binding_refuses_cpu_tensors():
@@ -163,11 +192,21 @@ def test_binding_refuses_cpu_tensors():
 
 
 def test_bwd_noalloc_rejects_oversize_on_the_host():
-    # rows = Lc*B*H*T above the fixed scratch: SCRATCH_LIMIT, decided before any CUDA call
+    # a call whose workspace exceeds the fixed array: SCRATCH_LIMIT, decided before any
+    # CUDA call. 16 layers x B=16 x H=8 x T=1024 needs 4 + 4 * 6 bytes per row = 56 MiB.
     L = fa.lib()
-    sc = fa.Schedule().to_c()
+    sc = fa.Schedule("coprime", "fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16,
+                     coprime_c=5).to_c()
     ok = ctypes.c_void_p(256)
-    st = L.fibattn_bwd_noalloc(*([ok] * 9), 1, 1, fa.NOALLOC_MAX_ROWS + 1, 64, 1, 4, 0.0,
-                               ctypes.byref(sc), 0, 1, None)
+    n = ctypes.c_uint64(0)
+    assert L.fibattn_bwd_workspace_size(16, 8, 1024, 64, 1, 64, ctypes.byref(sc), 0, 16,
+                                        ctypes.byref(n)) == fa.OK
+    assert n.value > fa.NOALLOC_SCRATCH_BYTES
+    st = L.fibattn_bwd_noalloc(*([ok] * 9), 16, 8, 1024, 64, 1, 64, 0.0, ctypes.byref(sc), 0, 16,
+                               None)
     assert st == fa.SCRATCH_LIMIT
     assert "scratch" in fa.status_string(fa.SCRATCH_LIMIT)
+    # the 16-layer B=8 training-step shape fits (28 MiB)
+    assert L.fibattn_bwd_workspace_size(8, 8, 1024, 64, 1, 64, ctypes.byref(sc), 0, 16,
+                                        ctypes.byref(n)) == fa.OK
+    assert n.value <= fa.NOALLOC_SCRATCH_BYTES

@@ -250,8 +250,11 @@ BWD_EDGE = [
     (1, 2, 63, 6, SCHEDS[2]),
     (2, 1, 129, 12, SCHEDS[4]),
     (1, 1, 1000, 64, SCHEDS[5]),
-    (1, 1, 300, 300, SCHEDS[0]),
-    (1, 2, 517, 100, SCHEDS[1]),
+    (1, 1, 300, 300, SCHEDS[0]),       # W >= T: dense causal
+    (1, 2, 517, 100, SCHEDS[1]),       # W > 64
+    (1, 1, 1024, 1, SCHEDS[0]),        # window = the query itself
+    (1, 1, 2049, 64, SCHEDS[6]),       # last tile holds one row
+    (1, 1, 640, 16, SCHEDS[7]),        # alpha 7/3 over an uncapped Fibonacci base
 ]
 
 
@@ -287,3 +290,72 @@ def test_autograd_wrapper_matches_bwd():
     dq, dk, dv = fa.bwd(inp["q"][0], inp["k"][0], inp["v"][0], o2, lse, inp["dO"][0], 64, sc, 4)
     assert torch.equal(o, o2) and torch.equal(q.grad, dq) and torch.equal(k.grad, dk)
     assert torch.equal(v.grad, dv)
+
+
+def test_bwd_empty_table_is_sliding_window_gradient():
+    # no offsets at all (base_max < W): the backward of plain sliding-window attention
+    sched = dict(kind="fixed", base="fib", alpha=(1, 1), n_layers=1, base_max=10)
+    assert oracle_table(sched, 0, 16, 500) == []
+    inp = fi.draw((1, 1, 2, 500, 64), seed=23, scale=0.25, dtype="bf16", names=("q", "k", "v", "dO"))
+    dev = to_dev(inp)
+    sc = lib_schedule(sched)
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], 16, sc)
+    dq, dk, dv = fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], 16, sc)
+    ref = oracle_bwd_slices(inp, sched, 16, 0, [(0, 0, h) for h in range(2)])
+    for (l, b, h), (rq, rk, rv, ro, rl) in ref.items():
+        for got, want in ((dq, rq), (dk, rk), (dv, rv)):
+            assert max_abs(f64(got[l, b, h]), want) <= TOL["bf16"]
+
+
+def test_bwd_more_layers_than_one_launch_equals_per_layer_calls():
+    # 18 layers: the call is split into launches of 16 + 2 layers sharing one workspace
+    sched = dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=20)
+    sc = lib_schedule(sched)
+    inp = to_dev(fi.draw((18, 1, 2, 400, 64), seed=25, scale=0.25, dtype="bf16",
+                         names=("q", "k", "v", "dO")))
+    o, lse = fa.fwd(inp["q"], inp["k"], inp["v"], 64, sc, layer0=1)
+    dq, dk, dv = fa.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], 64, sc, layer0=1)
+    for c in (0, 15, 16, 17):
+        g = fa.bwd(inp["q"][c], inp["k"][c], inp["v"][c], o[c], lse[c], inp["dO"][c], 64, sc,
+                   layer0=1 + c)
+        assert torch.equal(g[0], dq[c]) and torch.equal(g[1], dk[c]) and torch.equal(g[2], dv[c])
+
+
+def test_bwd_deterministic():
+    inp = to_dev(fi.workload_inputs("c5", layers=range(2), B=2))
+    sc = lib_schedule(fi.WORKLOADS["c5"]["sched"])
+    o, lse = fa.fwd(inp["q"], inp["k"], inp["v"], 64, sc)
+    a = fa.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], 64, sc)
+    b = fa.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], 64, sc)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_fwd_bwd_from_a_fresh_host_thread():
+    # a host thread that has made no CUDA runtime call yet has no current context; the
+    # launchers must bind it before encoding their TMA tensor maps
+    import threading
+
+    inp = to_dev(fi.draw((1, 1, 2, 300, 64), seed=33, scale=0.25, dtype="bf16",
+                         names=("q", "k", "v", "dO")))
+    sc = lib_schedule(SCHEDS[2])
+    o0, l0 = fa.fwd(inp["q"], inp["k"], inp["v"], 64, sc, layer0=4)
+    g0 = fa.bwd(inp["q"], inp["k"], inp["v"], o0, l0, inp["dO"], 64, sc, layer0=4)
+    torch.cuda.synchronize()
+    out = {}
+
+    def work():
+        try:
+            o, l = fa.fwd(inp["q"], inp["k"], inp["v"], 64, sc, layer0=4)
+            g = fa.bwd(inp["q"], inp["k"], inp["v"], o, l, inp["dO"], 64, sc, layer0=4)
+            torch.cuda.synchronize()
+            out["res"] = (o, l, *g)
+        except Exception as e:  # reported on the main thread
+            out["err"] = e
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert "err" not in out, out.get("err")
+    for a, b in zip(out["res"], (o0, l0, *g0)):
+        assert torch.equal(a, b)

@@ -3,8 +3,8 @@
 Some callers cannot call cudaMalloc: an operator hosted by a framework that owns the
 device allocator and passes it no workspace, or a latency-critical loop where
 cudaMalloc/cudaFree would synchronise the device. fibattn_bwd needs a caller-allocated
-float32 scratch of Lc*B*H*T entries; fibattn_bwd_noalloc takes that scratch from a fixed
-per-device array inside the library instead. These tests call it through the C ABI, twice
+workspace (D per row and the (P, dS) pair of every diagonal entry); fibattn_bwd_noalloc
+takes it from a fixed 32 MiB per-device array inside the library instead. These tests call it through the C ABI, twice
 in a row (the array keeps the previous call's contents), and compare it with fibattn_bwd
 within the bf16 tolerance the parity tests use.
 
@@ -40,18 +40,20 @@ def _compare(x, layer0=0):
 
 
 def test_noalloc_matches_bwd_on_two_calls_in_a_row():
-    # two different inputs back to back: the second call must not see the first's D
+    # two different inputs back to back: the second call must not see the first's workspace
     _compare(_inputs((2, 2, 4, 1024, 64), seed=41), layer0=3)
     _compare(_inputs((3, 1, 2, 777, 64), seed=42), layer0=9)
 
 
 def test_noalloc_at_its_size_limit_and_beyond():
-    # exactly FIBATTN_NOALLOC_MAX_ROWS rows: 16 layers x 8 x 8 x 1024 (the training-step shape)
+    # the 16-layer training-step shape (B=8, H=8, T=1024) needs 28 MiB: it fits
     x = _inputs((16, 8, 8, 1024, 64), seed=43)
-    assert 16 * 8 * 8 * 1024 == fa.NOALLOC_MAX_ROWS
+    assert fa.bwd_workspace_size(x["q"], 64, SCHED) <= fa.NOALLOC_SCRATCH_BYTES
     _compare(x)
-    # one more row than the array holds: rejected before any launch
-    y = _inputs((1, 1, 1, fa.NOALLOC_MAX_ROWS + 1, 64), seed=44)
+    del x
+    # twice the batch needs 56 MiB: rejected before any launch
+    y = _inputs((16, 16, 8, 1024, 64), seed=44)
+    assert fa.bwd_workspace_size(y["q"], 64, SCHED) > fa.NOALLOC_SCRATCH_BYTES
     o = torch.empty_like(y["q"])
     lse = torch.empty(y["q"].shape[:-1], dtype=torch.float32, device="cuda")
     with pytest.raises(fa.FibAttnError) as e:
