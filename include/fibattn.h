@@ -129,11 +129,12 @@ FIBATTN_API fibattn_status fibattn_fwd(const void* q, const void* k, const void*
                            int32_t n_layers_call, void* cuda_stream);
 
 /*
- * Workspace the backward needs for one call, in bytes (write it to *bytes):
- *   D [Lc][B][H][T] float32 (D_i = dO_i . o_i), rounded up to 256 bytes, and for bf16
- *   calls the (P, dS) pair of every (query, offset) diagonal entry,
- *   [Lc][B][H][n_max][T] of 4 bytes (two bf16), n_max = the largest table size among the
- *   call's layers at this (W, T).
+ * Workspace the backward needs for one call, in bytes (write it to *bytes). f32 calls:
+ *   D [Lc][B][H][T] float32 (D_i = dO_i . o_i). bf16 calls, with rows padded to
+ *   T_pad = T rounded up to a multiple of 4: D and lse * log2(e), each [Lc][B][H][T_pad]
+ *   float32 and 256-byte aligned, then the (P, dS) pair (two bf16) of every (query, offset)
+ *   diagonal entry, [Lc][B][H][n_max][T_pad] indexed by the key row, n_max = the largest
+ *   table size among the call's layers at this (W, T).
  * Errors: INVALID_ARG, UNSUPPORTED and CAPACITY as fibattn_bwd (same checks).
  */
 FIBATTN_API fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int32_t T, int32_t d,
@@ -171,18 +172,18 @@ FIBATTN_API fibattn_status fibattn_bwd(const void* q, const void* k, const void*
  * device allocator and hands it no workspace, or a latency-critical loop where
  * cudaMalloc/cudaFree would synchronise the device. This entry point takes the backward's
  * workspace from a fixed file-scope __device__ array of FIBATTN_NOALLOC_SCRATCH_BYTES
- * (32 MiB, held on every GPU that loads the library until the process exits) and
+ * (40 MiB, held on every GPU that loads the library until the process exits) and
  * allocates nothing.
  *   - Calls whose fibattn_bwd_workspace_size() exceeds FIBATTN_NOALLOC_SCRATCH_BYTES
  *     return FIBATTN_ERR_SCRATCH_LIMIT without launching anything. The 16-layer
- *     B=8, H=8, T=1024, W=64 bf16 training step (28 MiB) fits.
+ *     B=8, H=8, T=1024, W=64 bf16 training step (32 MiB) fits.
  *   - The first call on a device (that device current) looks up the array's device
  *     address with cudaGetSymbolAddress; make that first call before any stream capture.
  *   - All calls on a device share the array and it keeps the last call's contents (every
  *     byte the backward reads is written earlier in the same call, so nothing needs
  *     clearing). Calls whose kernels can overlap on the GPU (unordered streams) race on it.
  */
-#define FIBATTN_NOALLOC_SCRATCH_BYTES (32ull << 20)
+#define FIBATTN_NOALLOC_SCRATCH_BYTES (40ull << 20)
 FIBATTN_API fibattn_status fibattn_bwd_noalloc(const void* q, const void* k, const void* v,
                                                const void* o, const float* lse, const void* dO,
                                                void* dq, void* dk, void* dv, int32_t B, int32_t H,

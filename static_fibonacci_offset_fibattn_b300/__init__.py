@@ -30,7 +30,7 @@ _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
 MAX_OFFSETS = 64
 
 OK, INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA_ERR, TIMEOUT, SCRATCH_LIMIT = range(7)
-NOALLOC_SCRATCH_BYTES = 32 << 20
+NOALLOC_SCRATCH_BYTES = 40 << 20
 _BASES = {"fib": 0, "pow2": 1}
 _KINDS = {"fixed": 0, "linear": 1, "coprime": 2}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}

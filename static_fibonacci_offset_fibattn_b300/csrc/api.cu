@@ -40,16 +40,30 @@ fibattn_status check_common(int32_t B, int32_t H, int32_t T, int32_t d, int32_t 
 
 size_t elt_size(int32_t dtype) { return dtype == FIBATTN_F32 ? 4 : 2; }
 
-// Layout of the backward workspace: D first, then (bf16 path) the (P, dS) pairs.
+// Layout of the backward workspace. f32 path: D [rows] (rows of T). bf16 path: rows padded to
+// T_pad = T rounded up to 4 (16-byte rows for bulk copies): D [rows_pad], lse*log2(e)
+// [rows_pad], then the (P, dS) pairs [slices][n_max][T_pad]; each array starts 256-aligned.
 struct BwdWorkspace {
-    uint64_t pds_offset;  // bytes
-    uint64_t total;       // bytes
-    int32_t n_max;        // table entries per layer slot of the pairs array
+    uint64_t lse2_offset;  // bytes
+    uint64_t pds_offset;   // bytes
+    uint64_t total;        // bytes
+    int32_t n_max;         // table entries per layer slot of the pairs array
+    int32_t T_pad;
 };
+
+uint64_t align256(uint64_t x) { return (x + 255) & ~(uint64_t)255; }
 
 // Callers have validated the arguments (check_common), so every table builds.
 BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t dtype, int32_t W,
                            const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
+    BwdWorkspace ws;
+    if (dtype != FIBATTN_BF16) {
+        ws.lse2_offset = ws.pds_offset = 0;
+        ws.total = (uint64_t)n_layers_call * B * H * T * 4;
+        ws.n_max = 0;
+        ws.T_pad = T;
+        return ws;
+    }
     int32_t n_max = 0;
     for (int32_t c = 0; c < n_layers_call; ++c) {
         Alpha a;
@@ -58,11 +72,12 @@ BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t dtype, int32
             build_table(sched, a, W, T, nullptr, 0, &n) != FIBATTN_ERR_INVALID_ARG)
             n_max = n > n_max ? n : n_max;
     }
-    const uint64_t rows = (uint64_t)n_layers_call * B * H * T;
-    BwdWorkspace ws;
-    ws.pds_offset = (rows * 4 + 255) & ~(uint64_t)255;
-    ws.n_max = dtype == FIBATTN_BF16 ? n_max : 0;
-    ws.total = ws.pds_offset + rows * (uint64_t)ws.n_max * 4;
+    ws.T_pad = (T + 3) & ~3;
+    const uint64_t rows_pad = (uint64_t)n_layers_call * B * H * ws.T_pad;
+    ws.n_max = n_max;
+    ws.lse2_offset = align256(rows_pad * 4);
+    ws.pds_offset = ws.lse2_offset + align256(rows_pad * 4);
+    ws.total = ws.pds_offset + rows_pad * (uint64_t)n_max * 4;
     return ws;
 }
 
@@ -185,7 +200,9 @@ fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const vo
     const BwdWorkspace ws = bwd_workspace(B, H, T, dtype, W, sched, layer0, n_layers_call);
     if (workspace_bytes < ws.total) return FIBATTN_ERR_INVALID_ARG;
     float* delta = static_cast<float*>(workspace);
+    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2_offset);
     uint32_t* pds = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.pds_offset);
+    const int64_t per_layer_pad = (int64_t)B * H * ws.T_pad;
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
     const int64_t per_layer = (int64_t)B * H * T;
     const size_t es = elt_size(dtype);
@@ -207,11 +224,13 @@ fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const vo
                                      (float*)((char*)dv + off), delta + loff, sh, t,
                                      as_stream(cuda_stream));
         } else {
+            const size_t poff = (size_t)c * per_layer_pad;
             st = launch_bwd_tc_bf16((const char*)q + off, (const char*)k + off,
                                     (const char*)v + off, (const char*)o + off, lse + loff,
                                     (const char*)dO + off, (char*)dq + off, (char*)dk + off,
-                                    (char*)dv + off, delta + loff, pds + loff * ws.n_max,
-                                    ws.n_max, sh, t, as_stream(cuda_stream));
+                                    (char*)dv + off, delta + poff, lse2 + poff,
+                                    pds + poff * ws.n_max, ws.n_max, sh, t,
+                                    as_stream(cuda_stream));
         }
         if (st != FIBATTN_OK) return st;
     }

@@ -9,7 +9,7 @@
 // fibattn_bwd.
 //
 // Properties a caller must know:
-//   - The array holds FIBATTN_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU that loads the
+//   - The array holds FIBATTN_NOALLOC_SCRATCH_BYTES (40 MiB) on every GPU that loads the
 //     library, for the life of the process. Calls whose workspace is larger are rejected
 //     with FIBATTN_ERR_SCRATCH_LIMIT before anything is launched.
 //   - Host code cannot use the array's name as a device address. The first call on each

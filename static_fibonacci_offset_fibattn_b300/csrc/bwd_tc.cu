@@ -19,7 +19,9 @@
 //   dQ += dS K (A = dS from TMEM, B = K chunk MN-major) accumulates in TMEM.
 //   Offsets (a diagonal per table entry): s = q.k_{i-o}, dp = dO.v_{i-o} by CUDA-core row
 //   dot products, dq += ds k_{i-o} in registers; (P, dS) of each (row, offset) pair is
-//   written to the workspace as a bf16 pair.
+//   written to the workspace as a bf16 pair, indexed by the key row i-o; D and lse log2(e)
+//   go to the workspace too (rows padded to a multiple of 4 so the second kernel can fetch
+//   them with 16-byte-aligned bulk copies).
 //   Epilogue: dq = scale (dQ_band + dq_off), bf16, TMA store.
 //
 // bwd_dkdv_tc (key owner; one CTA = 128 keys [j0, j0+128) of a slice, 320 threads)
@@ -30,9 +32,10 @@
 //   warp 9    : TMA loads of the shifted offset tiles Q[j0+o ..], dO[j0+o ..].
 //   Band, per 64-query chunk: S^T = K Q^T and dP^T = V dO^T into TMEM; row threads form
 //   P^T and dS^T (bf16, over S^T and dP^T); dV += P^T dO and dK += dS^T Q in TMEM.
-//   Offsets: key j receives dk_j += dS q_{j+o}, dv_j += P dO_{j+o} from the (P, dS) pairs
-//   the first kernel stored, so no dot product is recomputed.
-//   Epilogue: dk = scale (dK_band + dk_off), dv = dV_band + dv_off, bf16, TMA stores.
+//   Offsets: key j receives dk_j += dS q_{j+o} (first pass over the Q tiles of all offsets)
+//   and dv_j += P dO_{j+o} (second pass over the dO tiles) from the (P, dS) pairs the first
+//   kernel stored, so no dot product is recomputed; each pass is added into TMEM.
+//   Epilogue: dk = scale dK, dv = dV, bf16, TMA stores.
 //
 // Every mbarrier wait is bounded (tc::mbar_wait); a wait that runs out latches the device
 // error word, later waits return at once, and the CTA still releases its TMEM.
@@ -42,6 +45,7 @@
 #include <stdint.h>
 
 #include "internal.h"
+#include "ring.cuh"
 #include "tc_prims.cuh"
 #include "tmap.h"
 
@@ -61,11 +65,16 @@ struct BwdParams {
     CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs
     const __nv_bfloat16* o;               // forward output (for D)
     const float* lse;                     // [slices][T]
-    float* delta;                         // workspace: D [slices][T]
-    uint32_t* pds;                        // workspace: (P, dS) bf16 pairs [slices][n_max][T]
+    float* delta;                         // workspace: D [slices][T_pad]
+    float* lse2;                          // workspace: lse * log2(e) [slices][T_pad]
+    uint32_t* pds;                        // workspace: (P, dS) bf16 pairs [slices][n_max][T_pad],
+                                          // entry k of key row j = the pair (j + o_k, j)
     int32_t* err;
     int64_t slices_per_layer;
+    uint32_t slices_per_layer32;          // the same, for the persistent tile walk
+    uint32_t total_tiles;                 // tiles of the launch (<= INT32_MAX)
     int32_t T, W;
+    int32_t T_pad;                        // T rounded up to 4: rows of the workspace arrays
     int32_t tiles_per_slice;
     int32_t n_max;                        // offsets per layer slot in pds
     float scale;
@@ -104,7 +113,7 @@ constexpr int kNumBars = 10;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemAlloc = kOffTmemSlot + 16 + 1024;
 
-__global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
@@ -226,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ Bw
         const bool row_ok = i < T;
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const float sl2 = p.scale_log2;
-        const int64_t grow = zl * T + i;  // row index into lse / delta
+        const int64_t grow = zl * T + i;  // row index into lse
+        const int64_t wrow = zl * p.T_pad + i;  // row index into the workspace arrays
         const float lse2 = row_ok ? p.lse[grow] * kLog2e : 0.f;
 
         // D_i = dO_i . o_i (o read straight from global memory, dO from the tile)
@@ -254,7 +264,10 @@ __global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ Bw
             }
             D = (a0 + a1) + (a2 + a3);
         }
-        if (row_ok) p.delta[grow] = D;
+        if (row_ok) {
+            p.delta[wrow] = D;
+            p.lse2[wrow] = lse2;
+        }
 
         // ---- band: dS over the window, written back to TMEM as the dQ MMA's A operand
         for (int c = 0; c < n_chunks; ++c) {
@@ -299,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ Bw
 #pragma unroll
         for (int c = 0; c < 64; ++c) dq[c] = 0.f;
         uint32_t seq = 0;
-        const int64_t pds_row = (int64_t)z * p.n_max * T + i;
+        const int64_t pds_row = (int64_t)z * p.n_max * p.T_pad + i;
 #pragma unroll 1
         for (int k = 0; k < n_act; ++k) {
             const bool valid = row_ok && i - offs[k] >= 0;
@@ -342,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ Bw
             const float pr = valid ? ex2(sdot * sl2 - lse2) : 0.f;
             const float ds = pr * (dpd - D);
             const uint32_t pair = pack_bf16x2(pr, ds);  // lo = P, hi = dS
-            if (row_ok) p.pds[pds_row + (int64_t)k * T] = pair;
+            if (valid) p.pds[pds_row + (int64_t)k * p.T_pad - offs[k]] = pair;  // key row i - o
             const uint32_t dsb = pair >> 16;  // dS as bf16 in the low half
 #pragma unroll
             for (int c = 0; c < 32; ++c) axpy2_bf16(dsb, kw[c], dq[2 * c], dq[2 * c + 1]);
@@ -396,59 +409,72 @@ __global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ Bw
 namespace dkdv {
 
 constexpr int kThreads = 320;
-constexpr int kRowThreads = 256;
+constexpr int kRowWarps = 8;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColDK = 0, kColDV = 64, kColS = 128, kColP = 192;
+constexpr uint32_t kSlots = 6;
+constexpr int kMaxGroupChunks = 4;    // band chunks per K/V copy: 2 + 4 ring items
+constexpr uint32_t kFullArrivals = 1;  // the producer's arrival with the byte count
 
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kOffK + kTileBytes;
-constexpr uint32_t kOffBand = kOffV + kTileBytes;           // 2 stages x (Q 8 KB + dO 8 KB)
-constexpr uint32_t kOffRing = kOffBand + 4 * kChunkBytes;   // 2 x 16 KB
-constexpr uint32_t kOffLD = kOffRing + 2 * kTileBytes;      // 2 stages x (lse2[64], D[64])
-constexpr uint32_t kOffBar = kOffLD + 2 * 2 * kChunk * 4;
-// barriers: 0 K+V, 1-2 band full (32 arrivals + tx), 3 S^T/dP^T ready, 4 P^T/dS^T written
-// (256), 5 dK/dV MMAs done, 6-7 ring full, 8-9 ring empty (256)
-constexpr int kNumBars = 10;
+constexpr uint32_t kOffRing = 0;
+constexpr uint32_t kOffSide = kOffRing + kSlots * ring::kSlotBytes;  // [slot][128] 4-byte words
+constexpr uint32_t kOffBar = kOffSide + kSlots * 128 * 4;
+// barriers: FULL[kSlots], EMPTY[kSlots], S^T/dP^T ready, P^T/dS^T written (8 warps),
+// dK/dV MMAs done, TMEM free (8 warps)
+constexpr uint32_t kBarS = 2 * kSlots, kBarP = kBarS + 1, kBarM = kBarS + 2, kBarT = kBarS + 3;
+constexpr uint32_t kNumBars = kBarT + 1;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemAlloc = kOffTmemSlot + 16 + 1024;
 
-__global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ BwdParams p) {
+// Band queries [j0, min(T-1, j0+127+W-1)] in 64-query chunks, grouped by kMaxGroupChunks
+// (each group re-reads the K and V tiles, so no ring item waits on a later one); active
+// offsets o <= T-1-j0.
+struct Plan {
+    int32_t j0, q_lo, n_chunks, n_groups, n_act;
+    __device__ __forceinline__ int nch(int g) const {
+        return min(kMaxGroupChunks, n_chunks - g * kMaxGroupChunks);
+    }
+    __device__ __forceinline__ uint32_t band_items() const { return 2 * n_groups + n_chunks; }
+};
+
+__device__ __forceinline__ Plan make_plan(const BwdParams& p, int layer, int32_t j0) {
+    Plan pl;
+    pl.j0 = j0;
+    const int64_t qlast64 = (int64_t)j0 + kRows - 1 + p.W - 1;
+    const int32_t qlast = qlast64 < p.T - 1 ? (int32_t)qlast64 : p.T - 1;
+    pl.q_lo = j0 / kChunk;
+    pl.n_chunks = qlast / kChunk - pl.q_lo + 1;
+    pl.n_groups = (pl.n_chunks + kMaxGroupChunks - 1) / kMaxGroupChunks;
+    const int32_t* offs = p.tabs.off[layer];
+    int32_t n = 0;
+    for (int e = 0; e < p.tabs.count[layer]; ++e)
+        if (offs[e] <= p.T - 1 - j0) n = e + 1;
+    pl.n_act = n;
+    return pl;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int layer = blockIdx.y;
-    const int tile = blockIdx.x % p.tiles_per_slice;
-    const int64_t zl = (int64_t)layer * p.slices_per_layer + blockIdx.x / p.tiles_per_slice;
-    const int32_t z = (int32_t)zl;
     const int32_t T = p.T, W = p.W;
-    const int32_t j0 = tile * kRows;
-
-    const uint32_t B_KV = bar_at(sbase, kOffBar, 0);
-    auto B_BAND = [&](int s) { return bar_at(sbase, kOffBar, 1 + s); };
-    const uint32_t B_S = bar_at(sbase, kOffBar, 3), B_PDS = bar_at(sbase, kOffBar, 4);
-    const uint32_t B_MM = bar_at(sbase, kOffBar, 5);
-    auto B_FULL = [&](int s) { return bar_at(sbase, kOffBar, 6 + s); };
-    auto B_EMPTY = [&](int s) { return bar_at(sbase, kOffBar, 8 + s); };
-
-    // band queries [j0, min(T-1, j0+127+W-1)] in 64-query chunks; active offsets o <= T-1-j0
-    const int64_t qlast64 = (int64_t)j0 + kRows - 1 + W - 1;
-    const int32_t qlast = qlast64 < T - 1 ? (int32_t)qlast64 : T - 1;
-    const int32_t q_lo = j0 / kChunk;
-    const int32_t n_chunks = qlast / kChunk - q_lo + 1;
-    const int32_t* offs = p.tabs.off[layer];
-    int32_t n_act = 0;
-    for (int e = 0; e < p.tabs.count[layer]; ++e)
-        if (offs[e] <= T - 1 - j0) n_act = e + 1;
+    const ring::Ring rg{sbase + kOffRing, sbase + kOffBar, kSlots, kRowWarps};
+    auto bar = [&](uint32_t idx) { return sbase + kOffBar + 8u * idx; };
+    const uint32_t B_S = bar(kBarS), B_P = bar(kBarP), B_M = bar(kBarM), B_T = bar(kBarT);
+    auto side_addr = [&](uint32_t seq) { return sbase + kOffSide + rg.slot(seq) * 512u; };
+    auto side_ptr = [&](uint32_t seq) {
+        return reinterpret_cast<const float*>(smem + kOffSide + rg.slot(seq) * 512u);
+    };
+    auto slot_ptr = [&](uint32_t seq) { return smem + (rg.addr(seq) - sbase); };
 
     if (tid == 0) {
-        for (int b = 0; b < kNumBars; ++b) {
-            uint32_t cnt = 1;
-            if (b == 1 || b == 2) cnt = 32;
-            if (b == 4 || b >= 8) cnt = kRowThreads;
-            mbar_init(bar_at(sbase, kOffBar, b), cnt);
-        }
+        ring::init_ring_barriers(rg, kFullArrivals);
+        mbar_init(B_S, 1);
+        mbar_init(B_P, kRowWarps);
+        mbar_init(B_M, 1);
+        mbar_init(B_T, kRowWarps);
         fence_mbar_init();
     }
     if (warp == 8) {
@@ -461,241 +487,292 @@ __global__ void __launch_bounds__(kThreads, 2) kernel(const __grid_constant__ Bw
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
     bool aborted = false;
 
-    float* lds = reinterpret_cast<float*>(smem + kOffLD);  // [stage][lse2 64 | D 64]
-
-    if (warp == 8) {
-        // ------------------------------------------------ band loads + MMA issue (whole warp)
-        auto load_band = [&](int c) {
-            const int s = c & 1;
-            const int32_t y = (q_lo + c) * kChunk;
-            float* st = lds + s * 2 * kChunk;
-            for (int t = lane; t < kChunk; t += 32) {
-                const int32_t i = y + t;
-                const bool ok = i < T;
-                st[t] = ok ? p.lse[zl * T + i] * kLog2e : 0.f;
-                st[kChunk + t] = ok ? p.delta[zl * T + i] : 0.f;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(B_BAND(s), 2 * kChunkBytes);
-                const uint32_t dst = sbase + kOffBand + s * 2 * kChunkBytes;
-                tma_load_3d(dst, &p.tm_q, B_BAND(s), 0, y, z);
-                tma_load_3d(dst + kChunkBytes, &p.tm_do, B_BAND(s), 0, y, z);
-            } else {
-                mbar_arrive(B_BAND(s));
-            }
-        };
+    if (warp == 9) {
+        // ------------------------------------------------ producer (lane 0)
         if (lane == 0) {
             prefetch_tmap(&p.tm_q);
             prefetch_tmap(&p.tm_do);
             prefetch_tmap(&p.tm_k);
             prefetch_tmap(&p.tm_v);
-            mbar_arrive_expect_tx(B_KV, 2 * kTileBytes);
-            tma_load_3d(sbase + kOffK, &p.tm_k, B_KV, 0, j0, z);
-            tma_load_3d(sbase + kOffK + kChunkBytes, &p.tm_k, B_KV, 0, j0 + kChunk, z);
-            tma_load_3d(sbase + kOffV, &p.tm_v, B_KV, 0, j0, z);
-            tma_load_3d(sbase + kOffV + kChunkBytes, &p.tm_v, B_KV, 0, j0 + kChunk, z);
-        }
-        load_band(0);
-        if (n_chunks > 1) load_band(1);
-        if (lane == 0) mbar_wait(B_KV, 0, aborted, p.err);
-        const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
-        const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);
-        for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1;
-            if (lane == 0) {
-                const uint32_t qaddr = sbase + kOffBand + s * 2 * kChunkBytes;
-                const uint32_t gaddr = qaddr + kChunkBytes;
-                mbar_wait(B_BAND(s), (c >> 1) & 1, aborted, p.err);
-                if (c > 0) mbar_wait(B_MM, (c - 1) & 1, aborted, p.err);
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem + kColS, sdesc_sw128(sbase + kOffK + 32 * kk, 16, 1024),
-                           sdesc_sw128(qaddr + 32 * kk, 16, 1024), idesc_s, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem + kColP, sdesc_sw128(sbase + kOffV + 32 * kk, 16, 1024),
-                           sdesc_sw128(gaddr + 32 * kk, 16, 1024), idesc_s, kk > 0);
-                mma_commit(B_S);
-                mbar_wait(B_PDS, c & 1, aborted, p.err);
-                tc_fence_after();
-                // P^T / dS^T of queries 32h..32h+31 sit in columns [32h, 32h+16) of their block
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t acol = 32 * (kk >> 1) + 8 * (kk & 1);
-                    const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tmem + kColDV, tmem + kColS + acol,
-                           sdesc_sw128(gaddr + 2048 * kk, 0, 1024), idesc_o, acc);
-                    mma_ts(tmem + kColDK, tmem + kColP + acol,
-                           sdesc_sw128(qaddr + 2048 * kk, 0, 1024), idesc_o, acc);
-                }
-                mma_commit(B_MM);
-                if (c + 2 < n_chunks) mbar_wait(B_MM, c & 1, aborted, p.err);
-            }
-            __syncwarp();
-            if (c + 2 < n_chunks) load_band(c + 2);
-        }
-        if (lane == 0) mbar_wait(B_MM, (n_chunks - 1) & 1, aborted, p.err);
-    } else if (warp == 9) {
-        if (lane == 0 && n_act > 0) {
+            prefetch_tmap(&p.tm_dk);
+            prefetch_tmap(&p.tm_dv);
             uint32_t seq = 0;
-            for (int k = 0; k < n_act; ++k) {
-                const int32_t y = j0 + offs[k];
-                for (int h = 0; h < 2; ++h, ++seq) {
-                    const CUtensorMap* map = h == 0 ? &p.tm_q : &p.tm_do;
-                    const int s = seq & 1;
-                    mbar_wait(B_EMPTY(s), ((seq >> 1) & 1) ^ 1, aborted, p.err);
-                    mbar_arrive_expect_tx(B_FULL(s), kTileBytes);
-                    tma_load_3d(sbase + kOffRing + s * kTileBytes, map, B_FULL(s), 0, y, z);
-                    tma_load_3d(sbase + kOffRing + s * kTileBytes + kChunkBytes, map, B_FULL(s), 0,
-                                y + kChunk, z);
+            const int32_t Tp = p.T_pad;
+            for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
+                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer32);
+                const Plan pl = make_plan(p, tl.layer, tl.row0);
+                const int32_t z = (int32_t)tl.zl;
+                const float* l2_row = p.lse2 + tl.zl * Tp;
+                const float* d_row = p.delta + tl.zl * Tp;
+                for (int g = 0; g < pl.n_groups; ++g) {
+                    // K and V tiles
+                    for (int h = 0; h < 2; ++h, ++seq) {
+                        if (!rg.acquire(seq, aborted, p.err)) continue;
+                        const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
+                        mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes);
+                        tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, pl.j0, z);
+                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, pl.j0 + kChunk, z);
+                    }
+                    // band chunks: Q and dO rows qb.., with lse*log2(e) and D of those rows
+                    for (int c = 0; c < pl.nch(g); ++c, ++seq) {
+                        if (!rg.acquire(seq, aborted, p.err)) continue;
+                        const int32_t qb = (pl.q_lo + g * kMaxGroupChunks + c) * kChunk;
+                        const uint32_t side_bytes = 4u * (uint32_t)min(kChunk, Tp - qb);
+                        mbar_arrive_expect_tx(rg.full(seq), 2 * kChunkBytes + 2 * side_bytes);
+                        tma_load_3d(rg.addr(seq), &p.tm_q, rg.full(seq), 0, qb, z);
+                        tma_load_3d(rg.addr(seq) + kChunkBytes, &p.tm_do, rg.full(seq), 0, qb, z);
+                        bulk_load(side_addr(seq), l2_row + qb, side_bytes, rg.full(seq));
+                        bulk_load(side_addr(seq) + 256, d_row + qb, side_bytes, rg.full(seq));
+                    }
                 }
+                // Q_o of every offset, then dO_o of every offset; both carry the (P, dS) pairs of
+                // the tile's key rows as side data
+                const int32_t* offs = p.tabs.off[tl.layer];
+                const uint32_t pair_bytes = 4u * (uint32_t)min(kRows, Tp - pl.j0);
+                for (int h = 0; h < 2; ++h) {
+                    for (int k = 0; k < pl.n_act; ++k, ++seq) {
+                        if (!rg.acquire(seq, aborted, p.err)) continue;
+                        const int32_t y = pl.j0 + offs[k];
+                        const CUtensorMap* map = h == 0 ? &p.tm_q : &p.tm_do;
+                        mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + pair_bytes);
+                        tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, z);
+                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, z);
+                        bulk_load(side_addr(seq), p.pds + ((int64_t)z * p.n_max + k) * Tp + pl.j0,
+                                  pair_bytes, rg.full(seq));
+                    }
+                }
+                // staging slots of the dK and dV tiles
+                for (int h = 0; h < 2; ++h, ++seq)
+                    if (rg.acquire(seq, aborted, p.err)) rg.publish_empty(seq);
             }
-            for (uint32_t q = seq > 2 ? seq - 2 : 0; q < seq; ++q)
-                mbar_wait(B_FULL(q & 1), (q >> 1) & 1, aborted, p.err);
+            // teardown: the last fills have landed (no copy may still be writing this CTA's
+            // shared memory when it exits) and every slot's last use has been released
+            for (uint32_t q = seq > kSlots ? seq - kSlots : 0; q < seq; ++q)
+                rg.wait_full(q, aborted, p.err);
+            for (uint32_t q = seq > kSlots ? seq - kSlots : 0; q < seq; ++q)
+                rg.acquire(q + kSlots, aborted, p.err);
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------ MMA issue
+        if (lane == 0) {
+            uint32_t seq = 0, mcount = 0, tcount = 0;
+            const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
+            const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);
+            // descriptors of shared address sbase; an operand at sbase + x adds x >> 4
+            const uint64_t dkm = sdesc_sw128(sbase, 16, 1024), dmn = sdesc_sw128(sbase, 0, 1024);
+            for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x, ++tcount) {
+                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer32);
+                const Plan pl = make_plan(p, tl.layer, tl.row0);
+                if (tcount > 0) mbar_wait(B_T, (tcount - 1) & 1, aborted, p.err);
+                int cg = 0;  // chunk index within the tile
+                for (int g = 0; g < pl.n_groups; ++g) {
+                    const int nch = pl.nch(g);
+                    const uint32_t kseq = seq, vseq = seq + 1, bseq = seq + 2;
+                    seq += 2 + nch;
+                    rg.wait_full(kseq, aborted, p.err);
+                    rg.wait_full(vseq, aborted, p.err);
+                    const uint32_t kaddr = rg.addr(kseq), vaddr = rg.addr(vseq);
+                    for (int c = 0; c < nch; ++c, ++cg, ++mcount) {
+                        const uint32_t qaddr = rg.addr(bseq + c), gaddr = qaddr + kChunkBytes;
+                        rg.wait_full(bseq + c, aborted, p.err);
+                        // S^T/dP^T columns hold the previous chunk's P^T/dS^T until its MMAs finish
+                        if (cg > 0) mbar_wait(B_M, (mcount - 1) & 1, aborted, p.err);
+                        tc_fence_after();
+                        const uint64_t dk_a = dkm + ((kaddr - sbase) >> 4), dv_a = dkm + ((vaddr - sbase) >> 4);
+                        const uint64_t dq_b = dkm + ((qaddr - sbase) >> 4), dg_b = dkm + ((gaddr - sbase) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + kColS, dk_a + 2 * kk, dq_b + 2 * kk, idesc_s, kk > 0);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + kColP, dv_a + 2 * kk, dg_b + 2 * kk, idesc_s, kk > 0);
+                        mma_commit(B_S);
+                        if (c == nch - 1) {
+                            rg.release_mma(kseq);
+                            rg.release_mma(vseq);
+                        }
+                        mbar_wait(B_P, mcount & 1, aborted, p.err);
+                        tc_fence_after();
+                        // P^T / dS^T of queries 32h..32h+31 sit in columns [32h, 32h+16) of their block
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t acol = 32 * (kk >> 1) + 8 * (kk & 1);
+                            const uint32_t acc = (cg > 0 || kk > 0) ? 1u : 0u;
+                            mma_ts(tmem + kColDV, tmem + kColS + acol,
+                                   dmn + ((gaddr - sbase) >> 4) + 128 * kk, idesc_o, acc);
+                            mma_ts(tmem + kColDK, tmem + kColP + acol,
+                                   dmn + ((qaddr - sbase) >> 4) + 128 * kk, idesc_o, acc);
+                        }
+                        mma_commit(B_M);
+                        rg.release_mma(bseq + c);
+                    }
+                }
+                seq += 2 * pl.n_act + 2;
+            }
+            if (mcount > 0) mbar_wait(B_M, (mcount - 1) & 1, aborted, p.err);
         }
     } else {
         // ------------------------------------------------ row threads: key row r, dim half h
         const int q4 = warp & 3, h = warp >> 2;
         const int r = 32 * q4 + lane;
-        const int32_t j = j0 + r;
-        const bool row_ok = j < T;
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const float sl2 = p.scale_log2;
+        uint32_t seq = 0, mcount = 0;
+        for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
+            const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer32);
+            const Plan pl = make_plan(p, tl.layer, tl.row0);
+            const int32_t j0 = pl.j0;
+            const int32_t j = j0 + r;
+            const bool row_ok = j < T;
+            const int32_t* offs = p.tabs.off[tl.layer];
 
-        // ---- band: P^T and dS^T of this thread's 32 query columns
-        for (int c = 0; c < n_chunks; ++c) {
-            const int32_t qb = (q_lo + c) * kChunk + 32 * h;  // first query of my columns
-            mbar_wait(B_S, c & 1, aborted, p.err);
+            // ---- band: P^T and dS^T of this thread's 32 query columns, 16 at a time
+            for (int g = 0; g < pl.n_groups; ++g) {
+                const int nch = pl.nch(g);
+                const uint32_t bseq = seq + 2;
+                seq += 2 + nch;
+                for (int c = 0; c < nch; ++c, ++mcount) {
+                    const int32_t qb = (pl.q_lo + g * kMaxGroupChunks + c) * kChunk + 32 * h;
+                    mbar_wait(B_S, mcount & 1, aborted, p.err);
+                    rg.wait_full(bseq + c, aborted, p.err);  // lse*log2(e) / D side data
+                    tc_fence_after();
+                    const int32_t klo = j0 + 32 * q4;
+                    const bool need = (qb + 31 - klo >= 0) && (qb - (klo + 31) < W) && qb < T;
+                    const float* L = side_ptr(bseq + c) + 32 * h;
+                    const float* Dd = L + kChunk;
+                    const int32_t dist0 = qb - j;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t col = 32 * h + 16 * half;
+                        uint32_t pp[8], pd[8];
+                        if (need) {
+                            uint32_t sv[16], dv[16];
+                            tmem_ld16(tmem + lane_base + kColS + col, sv);
+                            tmem_ld16(tmem + lane_base + kColP + col, dv);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                const int ee = 16 * half + e;
+                                const bool ok0 = row_ok && (uint32_t)(dist0 + ee) < (uint32_t)W && qb + ee < T;
+                                const bool ok1 = row_ok && (uint32_t)(dist0 + ee + 1) < (uint32_t)W && qb + ee + 1 < T;
+                                const float p0 = ok0 ? ex2(__uint_as_float(sv[e]) * sl2 - L[ee]) : 0.f;
+                                const float p1 = ok1 ? ex2(__uint_as_float(sv[e + 1]) * sl2 - L[ee + 1]) : 0.f;
+                                pp[e >> 1] = pack_bf16x2(p0, p1);
+                                pd[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - Dd[ee]),
+                                                         p1 * (__uint_as_float(dv[e + 1]) - Dd[ee + 1]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) pp[e] = pd[e] = 0u;
+                        }
+                        // packed over the columns this thread already read (16*half .. +16)
+                        tmem_st8(tmem + lane_base + kColS + 32 * h + 8 * half, pp);
+                        tmem_st8(tmem + lane_base + kColP + 32 * h + 8 * half, pd);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B_P);
+                }
+            }
+
+            // ---- offsets, first pass: dk_j += dS q_{j+o} over my 32 dims, then folded into the
+            // dK accumulator in TMEM (the band's MMAs are done with it)
+            mbar_wait(B_M, (mcount - 1) & 1, aborted, p.err);
             tc_fence_after();
-            const int32_t klo = j0 + 32 * q4;
-            const bool need = (qb + 31 - klo >= 0) && (qb - (klo + 31) < W) && qb < T;
-            uint32_t pp[16], pd[16];
-            if (need) {
-                uint32_t sv[32], dv[32];
-                tmem_ld32(tmem + lane_base + kColS + 32 * h, sv);
-                tmem_ld32(tmem + lane_base + kColP + 32 * h, dv);
-                tmem_ld_wait();
-                const float* L = lds + (c & 1) * 2 * kChunk + 32 * h;
-                const float* Dd = L + kChunk;
-                const int32_t dist0 = qb - j;
+            float acc[32];
+            for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const bool ok0 = row_ok && (uint32_t)(dist0 + e) < (uint32_t)W && qb + e < T;
-                    const bool ok1 = row_ok && (uint32_t)(dist0 + e + 1) < (uint32_t)W && qb + e + 1 < T;
-                    const float p0 = ok0 ? ex2(__uint_as_float(sv[e]) * sl2 - L[e]) : 0.f;
-                    const float p1 = ok1 ? ex2(__uint_as_float(sv[e + 1]) * sl2 - L[e + 1]) : 0.f;
-                    pp[e >> 1] = pack_bf16x2(p0, p1);
-                    pd[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - Dd[e]),
-                                             p1 * (__uint_as_float(dv[e + 1]) - Dd[e + 1]));
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) pp[e] = pd[e] = 0u;
-            }
-            tmem_st16(tmem + lane_base + kColS + 32 * h, pp);
-            tmem_st16(tmem + lane_base + kColP + 32 * h, pd);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(B_PDS);
-        }
-
-        // ---- offsets: dk_j += dS q_{j+o}, dv_j += P dO_{j+o} over my 32 dims
-        float dk[32], dv[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) dk[c] = dv[c] = 0.f;
-        const uint32_t* pds = p.pds + (int64_t)z * p.n_max * T;
-        uint32_t seq = 0;
-        uint32_t nxt = 0;
-        if (n_act > 0 && row_ok && j + offs[0] < T) nxt = pds[j + offs[0]];
+                for (int c = 0; c < 32; ++c) acc[c] = 0.f;
 #pragma unroll 1
-        for (int k = 0; k < n_act; ++k) {
-            const uint32_t pair = nxt;
-            if (k + 1 < n_act) {
-                const int32_t i1 = j + offs[k + 1];
-                nxt = (row_ok && i1 < T) ? pds[(int64_t)(k + 1) * T + i1] : 0u;
-            }
-            const uint32_t pb = pair & 0xFFFFu, dsb = pair >> 16;
-            int s = seq & 1;
-            mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
-            {
-                const uint8_t* row = smem + kOffRing + s * kTileBytes;
+                for (int k = 0; k < pl.n_act; ++k) {
+                    rg.wait_full(seq, aborted, p.err);
+                    const uint32_t pair = (row_ok && j + offs[k] < T)
+                                              ? reinterpret_cast<const uint32_t*>(side_ptr(seq))[r] : 0u;
+                    const uint32_t sc = pass == 0 ? pair >> 16 : pair & 0xFFFFu;  // dS or P (bf16)
+                    const uint8_t* row = slot_ptr(seq);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(row + sw128_off(r, 4 * h + c));
-                    axpy2_bf16(dsb, x.x, dk[8 * c + 0], dk[8 * c + 1]);
-                    axpy2_bf16(dsb, x.y, dk[8 * c + 2], dk[8 * c + 3]);
-                    axpy2_bf16(dsb, x.z, dk[8 * c + 4], dk[8 * c + 5]);
-                    axpy2_bf16(dsb, x.w, dk[8 * c + 6], dk[8 * c + 7]);
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(row + sw128_off(r, 4 * h + c));
+                        axpy2_bf16(sc, x.x, acc[8 * c + 0], acc[8 * c + 1]);
+                        axpy2_bf16(sc, x.y, acc[8 * c + 2], acc[8 * c + 3]);
+                        axpy2_bf16(sc, x.z, acc[8 * c + 4], acc[8 * c + 5]);
+                        axpy2_bf16(sc, x.w, acc[8 * c + 6], acc[8 * c + 7]);
+                    }
+                    rg.release_warp(seq, lane);
+                    ++seq;
+                }
+                // add into TMEM: dK columns [32h, +32) after the first pass, dV after the second
+                if (pl.n_act > 0) {
+                    const uint32_t col = (pass == 0 ? kColDK : kColDV) + 32 * h;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_base + col + 16 * q, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            v[c] = __float_as_uint(__uint_as_float(v[c]) + acc[16 * q + c]);
+                        tmem_st16(tmem + lane_base + col + 16 * q, v);
+                    }
+                    tmem_st_wait();
                 }
             }
-            mbar_arrive(B_EMPTY(s));
-            ++seq;
-            s = seq & 1;
-            mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
-            {
-                const uint8_t* row = smem + kOffRing + s * kTileBytes;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(row + sw128_off(r, 4 * h + c));
-                    axpy2_bf16(pb, x.x, dv[8 * c + 0], dv[8 * c + 1]);
-                    axpy2_bf16(pb, x.y, dv[8 * c + 2], dv[8 * c + 3]);
-                    axpy2_bf16(pb, x.z, dv[8 * c + 4], dv[8 * c + 5]);
-                    axpy2_bf16(pb, x.w, dv[8 * c + 6], dv[8 * c + 7]);
-                }
-            }
-            mbar_arrive(B_EMPTY(s));
-            ++seq;
-        }
 
-        // ---- epilogue: dk = scale (band + offsets) into the K tile, dv into the V tile
-        mbar_wait(B_MM, (n_chunks - 1) & 1, aborted, p.err);
-        tc_fence_after();
-        {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kColDK + 32 * h, v);
-            tmem_ld_wait();
-            uint8_t* st = smem + kOffK;
+            // ---- epilogue: dk = scale * dK, dv = dV (band + offsets), staged, TMA stores
+            const uint32_t kst = seq, vst = seq + 1;
+            seq += 2;
+            rg.wait_full(kst, aborted, p.err);
+            rg.wait_full(vst, aborted, p.err);
+            {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kColDK + 32 * h, v);
+                tmem_ld_wait();
+                uint8_t* st = slot_ptr(kst);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int e = 8 * c;
-                uint4 w;
-                w.x = pack_bf16x2((__uint_as_float(v[e + 0]) + dk[e + 0]) * p.scale,
-                                  (__uint_as_float(v[e + 1]) + dk[e + 1]) * p.scale);
-                w.y = pack_bf16x2((__uint_as_float(v[e + 2]) + dk[e + 2]) * p.scale,
-                                  (__uint_as_float(v[e + 3]) + dk[e + 3]) * p.scale);
-                w.z = pack_bf16x2((__uint_as_float(v[e + 4]) + dk[e + 4]) * p.scale,
-                                  (__uint_as_float(v[e + 5]) + dk[e + 5]) * p.scale);
-                w.w = pack_bf16x2((__uint_as_float(v[e + 6]) + dk[e + 6]) * p.scale,
-                                  (__uint_as_float(v[e + 7]) + dk[e + 7]) * p.scale);
-                *reinterpret_cast<uint4*>(st + sw128_off(r, 4 * h + c)) = w;
-            }
-            tmem_ld32(tmem + lane_base + kColDV + 32 * h, v);
-            tmem_ld_wait();
-            st = smem + kOffV;
+                for (int c = 0; c < 4; ++c) {
+                    const int e = 8 * c;
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * p.scale, __uint_as_float(v[e + 1]) * p.scale);
+                    w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
+                    w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * p.scale, __uint_as_float(v[e + 5]) * p.scale);
+                    w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * p.scale, __uint_as_float(v[e + 7]) * p.scale);
+                    *reinterpret_cast<uint4*>(st + sw128_off(r, 4 * h + c)) = w;
+                }
+                tmem_ld32(tmem + lane_base + kColDV + 32 * h, v);
+                tmem_ld_wait();
+                st = slot_ptr(vst);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int e = 8 * c;
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(v[e + 0]) + dv[e + 0], __uint_as_float(v[e + 1]) + dv[e + 1]);
-                w.y = pack_bf16x2(__uint_as_float(v[e + 2]) + dv[e + 2], __uint_as_float(v[e + 3]) + dv[e + 3]);
-                w.z = pack_bf16x2(__uint_as_float(v[e + 4]) + dv[e + 4], __uint_as_float(v[e + 5]) + dv[e + 5]);
-                w.w = pack_bf16x2(__uint_as_float(v[e + 6]) + dv[e + 6], __uint_as_float(v[e + 7]) + dv[e + 7]);
-                *reinterpret_cast<uint4*>(st + sw128_off(r, 4 * h + c)) = w;
+                for (int c = 0; c < 4; ++c) {
+                    const int e = 8 * c;
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(v[e + 0]), __uint_as_float(v[e + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+                    *reinterpret_cast<uint4*>(st + sw128_off(r, 4 * h + c)) = w;
+                }
             }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (tid == 0 && !aborted) {
-            tma_store_3d(&p.tm_dk, sbase + kOffK, 0, j0, z);
-            tma_store_3d(&p.tm_dv, sbase + kOffV, 0, j0, z);
-            if (j0 + kChunk < T) {
-                tma_store_3d(&p.tm_dk, sbase + kOffK + kChunkBytes, 0, j0 + kChunk, z);
-                tma_store_3d(&p.tm_dv, sbase + kOffV + kChunkBytes, 0, j0 + kChunk, z);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B_T);  // TMEM free for the next tile's MMAs
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (tid == 0) {
+                if (!aborted) {
+                    const int32_t z = (int32_t)tl.zl;
+                    tma_store_3d(&p.tm_dk, rg.addr(kst), 0, j0, z);
+                    tma_store_3d(&p.tm_dv, rg.addr(vst), 0, j0, z);
+                    if (j0 + kChunk < T) {
+                        tma_store_3d(&p.tm_dk, rg.addr(kst) + kChunkBytes, 0, j0 + kChunk, z);
+                        tma_store_3d(&p.tm_dv, rg.addr(vst) + kChunkBytes, 0, j0 + kChunk, z);
+                    }
+                    tma_store_commit();
+                    tma_store_wait_read0();
+                }
+                rg.release_stage(kst);
+                rg.release_stage(vst);
             }
-            tma_store_commit();
-            tma_store_wait_read0();
         }
     }
 
@@ -724,21 +801,15 @@ fibattn_status set_smem(const void* fn, uint32_t bytes, bool (&done)[64]) {
 
 }  // namespace
 
-int32_t bwd_tc_n_max(const OffsetTables& t, int32_t n_layers) {
-    int32_t n = 0;
-    for (int l = 0; l < n_layers; ++l) n = t.count[l] > n ? t.count[l] : n;
-    return n;
-}
-
 fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, const void* o,
                                   const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                                  float* delta, uint32_t* pds, int32_t n_max, const AttnShape& sh,
-                                  const OffsetTables& t, cudaStream_t st) {
+                                  float* delta, float* lse2, uint32_t* pds, int32_t n_max,
+                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
     const int64_t slices = sh.slices_per_layer * sh.n_layers;
     if (slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     const int32_t tiles = (sh.T + kRows - 1) / kRows;
     const int64_t gx = (int64_t)tiles * sh.slices_per_layer;
-    if (gx > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    if (gx > 0x7fffffff || (int64_t)tiles * slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     BwdParams P;
     // the error-word lookup is a runtime call: it binds the device's primary context to this
     // thread (a fresh thread, e.g. autograd's, may have none), which the encoding needs
@@ -753,30 +824,44 @@ fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, c
     P.o = static_cast<const __nv_bfloat16*>(o);
     P.lse = lse;
     P.delta = delta;
+    P.lse2 = lse2;
     P.pds = pds;
     P.slices_per_layer = sh.slices_per_layer;
+    P.slices_per_layer32 = (uint32_t)sh.slices_per_layer;
+    P.total_tiles = (uint32_t)((int64_t)tiles * slices);
     P.T = sh.T;
     P.W = sh.W;
+    P.T_pad = (sh.T + 3) & ~3;
     P.tiles_per_slice = tiles;
     P.n_max = n_max;
     P.scale = sh.scale;
     P.scale_log2 = sh.scale * kLog2e;
     P.tabs = t;
     static bool dq_set[64] = {}, dkdv_set[64] = {};
-    fibattn_status s0 = set_smem((const void*)dq::kernel, dq::kSmemAlloc, dq_set);
+    static int n_sm[64] = {};
+    fibattn_status s0 = set_smem((const void*)dq::bwd_dq_tc_kernel, dq::kSmemAlloc, dq_set);
     if (s0 != FIBATTN_OK) return s0;
-    s0 = set_smem((const void*)dkdv::kernel, dkdv::kSmemAlloc, dkdv_set);
+    s0 = set_smem((const void*)dkdv::bwd_dkdv_tc_kernel, dkdv::kSmemAlloc, dkdv_set);
     if (s0 != FIBATTN_OK) return s0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return FIBATTN_ERR_UNSUPPORTED;
+    if (n_sm[dev] == 0) {
+        e = cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaDeviceGetAttribute");
+    }
+    const int64_t pgrid = (int64_t)P.total_tiles < 2LL * n_sm[dev] ? (int64_t)P.total_tiles : 2LL * n_sm[dev];
     dim3 grid((unsigned)gx, sh.n_layers);
     {
         KernelScope ks("bwd_dq_tc", st);
-        dq::kernel<<<grid, dq::kThreads, dq::kSmemAlloc, st>>>(P);
+        dq::bwd_dq_tc_kernel<<<grid, dq::kThreads, dq::kSmemAlloc, st>>>(P);
     }
     s0 = launch_status("launch bwd_dq_tc");
     if (s0 != FIBATTN_OK) return s0;
     {
         KernelScope ks("bwd_dkdv_tc", st);
-        dkdv::kernel<<<grid, dkdv::kThreads, dkdv::kSmemAlloc, st>>>(P);
+        dkdv::bwd_dkdv_tc_kernel<<<(unsigned)pgrid, dkdv::kThreads, dkdv::kSmemAlloc, st>>>(P);
     }
     return launch_status("launch bwd_dkdv_tc");
 }

@@ -89,12 +89,12 @@ fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* 
                                    float* dv, float* delta, const AttnShape& sh,
                                    const OffsetTables& t, cudaStream_t st);
 
-// Tensor-core backward (bf16 path). Workspace: delta [slices][T] fp32 and pds
-// [slices][n_max][T] (P, dS) bf16 pairs, n_max >= every launch layer's table size.
-int32_t bwd_tc_n_max(const OffsetTables& t, int32_t n_layers);
+// Tensor-core backward (bf16 path). Workspace rows are padded to T_pad = T rounded up to 4:
+// delta and lse2 [slices][T_pad] fp32, pds [slices][n_max][T_pad] (P, dS) bf16 pairs indexed
+// by key row, n_max >= every launch layer's table size.
 fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, const void* o,
                                   const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                                  float* delta, uint32_t* pds, int32_t n_max, const AttnShape& sh,
-                                  const OffsetTables& t, cudaStream_t st);
+                                  float* delta, float* lse2, uint32_t* pds, int32_t n_max,
+                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
 
 }  // namespace fibattn

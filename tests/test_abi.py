@@ -168,20 +168,25 @@ def test_bwd_validates_before_launch():
 @pytest.mark.parametrize("shape", [(1, 2, 256, 16), (8, 8, 1024, 64), (2, 8, 4096, 64),
                                    (3, 1, 777, 6)])
 def test_bwd_workspace_size_layout(dtype, shape):
-    # D (4 bytes per row, rounded up to 256) and, for bf16, one 4-byte (P, dS) pair per
-    # row and table slot, n_max = the largest of the call's tables (from the oracle)
+    # f32: D (4 bytes per row). bf16: rows padded to a multiple of 4; D and lse*log2(e)
+    # (4 bytes per padded row each, each array 256-aligned) and one 4-byte (P, dS) pair per
+    # padded row and table slot, n_max = the largest of the call's tables (from the oracle)
     B, H, T, W = shape
     sched = dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16,
                  coprime_c=5)
     sc = fa.Schedule(**sched).to_c()
     n = ctypes.c_uint64(0)
+    a256 = lambda x: (x + 255) // 256 * 256
     for layer0, Lc in ((0, 16), (3, 5), (15, 1)):
         assert fa.lib().fibattn_bwd_workspace_size(B, H, T, 64, dtype, W, ctypes.byref(sc),
                                                    layer0, Lc, ctypes.byref(n)) == fa.OK
-        rows = Lc * B * H * T
         sc_py = fa.Schedule(**sched)
         n_max = max(len(_sched_to_oracle(sc_py, l, W, T)) for l in range(layer0, layer0 + Lc))
-        want = (rows * 4 + 255) // 256 * 256 + (rows * n_max * 4 if dtype == 1 else 0)
+        if dtype == 0:
+            want = Lc * B * H * T * 4
+        else:
+            rows = Lc * B * H * ((T + 3) // 4 * 4)
+            want = 2 * a256(rows * 4) + rows * n_max * 4
         assert n.value == want
 
 
@@ -193,7 +198,7 @@ def test_binding_refuses_cpu_tensors():
 
 def test_bwd_noalloc_rejects_oversize_on_the_host():
     # a call whose workspace exceeds the fixed array: SCRATCH_LIMIT, decided before any
-    # CUDA call. 16 layers x B=16 x H=8 x T=1024 needs 4 + 4 * 6 bytes per row = 56 MiB.
+    # CUDA call. 16 layers x B=16 x H=8 x T=1024 needs 4 + 4 + 4 * 6 bytes per row = 64 MiB.
     L = fa.lib()
     sc = fa.Schedule("coprime", "fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16,
                      coprime_c=5).to_c()
@@ -206,7 +211,7 @@ def test_bwd_noalloc_rejects_oversize_on_the_host():
                                None)
     assert st == fa.SCRATCH_LIMIT
     assert "scratch" in fa.status_string(fa.SCRATCH_LIMIT)
-    # the 16-layer B=8 training-step shape fits (28 MiB)
+    # the 16-layer B=8 training-step shape fits (32 MiB)
     assert L.fibattn_bwd_workspace_size(8, 8, 1024, 64, 1, 64, ctypes.byref(sc), 0, 16,
                                         ctypes.byref(n)) == fa.OK
     assert n.value <= fa.NOALLOC_SCRATCH_BYTES
