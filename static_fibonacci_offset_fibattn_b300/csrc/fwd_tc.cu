@@ -53,10 +53,15 @@ constexpr uint32_t kSlots = 6;
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffBar = kOffRing + kSlots * ring::kSlotBytes;
 // barriers: FULL[kSlots], EMPTY[kSlots], then S ready, P written (4 warps), PV done,
-// TMEM free (4 warps); then the TMEM address word. The Q slot is released by the row warps
-// once they hold their q rows (the S MMAs reading it are complete by then).
-constexpr uint32_t kBarS = 2 * kSlots, kBarP = kBarS + 1, kBarO = kBarS + 2, kBarT = kBarS + 3;
-constexpr uint32_t kNumBars = kBarT + 1;
+// TMEM free (4 warps), band items landed; then the TMEM address word. The Q slot is released
+// by the row warps once they hold their q rows (the S MMAs reading it are complete by then).
+// The row threads skip the MMA warp's ring items; before they wait on the offset slots
+// (whose previous use may be a band slot) they wait for "band items landed", which the MMA
+// warp signals once it has waited for every band item of the tile -- a parity wait is only
+// exact when the slot's previous use is known to have landed.
+constexpr uint32_t kBarS = 2 * kSlots, kBarP = kBarS + 1, kBarO = kBarS + 2, kBarT = kBarS + 3,
+                   kBarL = kBarS + 4;
+constexpr uint32_t kNumBars = kBarL + 1;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffTmemSlot + 16;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -119,7 +124,8 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
 
     const ring::Ring rg{sbase + kOffRing, sbase + kOffBar, kSlots, 4};  // 4 row warps
     auto bar = [&](uint32_t idx) { return sbase + kOffBar + 8u * idx; };
-    const uint32_t B_S = bar(kBarS), B_P = bar(kBarP), B_O = bar(kBarO), B_T = bar(kBarT);
+    const uint32_t B_S = bar(kBarS), B_P = bar(kBarP), B_O = bar(kBarO), B_T = bar(kBarT),
+                   B_L = bar(kBarL);
     auto slot_ptr = [&](uint32_t seq) { return smem + (rg.addr(seq) - sbase); };
 
     if (tid == 0) {
@@ -128,6 +134,7 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
         mbar_init(B_P, 4);
         mbar_init(B_O, 1);
         mbar_init(B_T, 4);
+        mbar_init(B_L, 1);
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -232,6 +239,7 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
                     mbar_wait(B_P, gcount & 1, aborted, p.err);
                     tc_fence_after();
                     for (int j = 0; j < ns; ++j) rg.wait_full(vseq + j, aborted, p.err);
+                    if (g == pl.n_groups - 1) mbar_arrive(B_L);  // every band item has landed
                     tc_fence_after();
                     for (int kk = 0; kk < nch * (kChunk / 16); ++kk) {
                         const int c = kk >> 2;
@@ -357,6 +365,7 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
                 }
             }
             rg.release_warp(qseq, lane);
+            mbar_wait(B_L, tcount & 1, aborted, p.err);
             float m_o = m_b, l_o = 0.f;
             float oacc[64];
 #pragma unroll

@@ -23,17 +23,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-int make_bf16_rows_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
+namespace {
+
+int make_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T, uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return -1;
     cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)slices};
     cuuint64_t strides[2] = {128, (cuuint64_t)T * 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)kTmaBoxRows, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return (int)r;
+}
+
+}  // namespace
+
+int make_bf16_rows_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
+    return make_map(m, base, slices, T, kTmaBoxRows);
+}
+
+int make_bf16_tile_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
+    return make_map(m, base, slices, T, 2 * kTmaBoxRows);
 }
 
 }  // namespace fibattn
