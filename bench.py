@@ -101,16 +101,18 @@ def src_hash(fn):
         return None
 
 
-def committed_traffic(kernel):
-    """Bytes per query token from the committed ncu summary, or None when absent or when
-    the kernel's source changed since the counters were taken."""
+def committed_traffic(kernel, workload):
+    """Bytes per query token of `kernel` on `workload` from the committed ncu summary, or
+    None when absent or when the kernel's source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
     want = src_hash(KERNEL_SRC.get(kernel, ""))
     for line in open(path):
+        if line.startswith("#"):
+            continue
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if f.get("kernel") == kernel and f.get("src") == want:
+        if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == want:
             return float(f["bytes_per_token"])
     return None
 
@@ -277,7 +279,7 @@ def run_ours(a, spec, world, rank, local):
         algo = ALGO_BYTES.get(dom, 0) * per_launch_tokens
         avg_s = ms / n / 1e3
         achieved = algo / avg_s / 1e9
-        traffic_pt = committed_traffic(dom)
+        traffic_pt = committed_traffic(dom, a.workload)
         roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
