@@ -13,7 +13,8 @@
 //   warps 0-3 : one thread per query row (TMEM lane = row).
 //   warp 4    : TMEM allocation, TMA loads of Q, dO and the band K/V chunks, tcgen05.mma.
 //   warp 5    : TMA loads of the shifted offset tiles K[i0-o ..], V[i0-o ..] into a ring.
-//   Preamble: D_i from o_i and dO_i (written to the workspace for the second kernel).
+//   Preamble: D_i from o_i (the first item of the offset ring) and dO_i, written to the
+//   workspace for the second kernel.
 //   Band, per 64-key chunk: S = Q K^T and dP = dO V^T (M=128, N=64) into TMEM; each row
 //   thread forms dS = P (dP - D) in fp32 and writes it back as bf16 over S; then
 //   dQ += dS K (A = dS from TMEM, B = K chunk MN-major) accumulates in TMEM.
@@ -63,7 +64,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // inputs, 3D {64, T, slices}, box {64, 64, 1}
     CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs
-    const __nv_bfloat16* o;               // forward output (for D)
+    CUtensorMap tm_o;                     // forward output (for D)
     const float* lse;                     // [slices][T]
     float* delta;                         // workspace: D [slices][T_pad]
     float* lse2;                          // workspace: lse * log2(e) [slices][T_pad]
@@ -211,8 +212,13 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
             mbar_wait(B_DQ, (n_chunks - 1) & 1, aborted, p.err);
         }
     } else if (warp == 5) {
-        if (lane == 0 && n_act > 0) {
-            uint32_t seq = 0;
+        // ring items: the O tile (for D), then K_o and V_o per active offset
+        if (lane == 0) {
+            prefetch_tmap(&p.tm_o);
+            mbar_arrive_expect_tx(B_FULL(0), kTileBytes);
+            tma_load_3d(sbase + kOffRing, &p.tm_o, B_FULL(0), 0, i0, z);
+            tma_load_3d(sbase + kOffRing + kChunkBytes, &p.tm_o, B_FULL(0), 0, i0 + kChunk, z);
+            uint32_t seq = 1;
             for (int k = 0; k < n_act; ++k) {
                 const int32_t y = i0 - offs[k];
                 for (int h = 0; h < 2; ++h, ++seq) {
@@ -239,30 +245,25 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
         const int64_t wrow = zl * p.T_pad + i;  // row index into the workspace arrays
         const float lse2 = row_ok ? p.lse[grow] * kLog2e : 0.f;
 
-        // D_i = dO_i . o_i (o read straight from global memory, dO from the tile)
-        uint4 orow[8];
-        if (row_ok) {
-            const uint4* op = reinterpret_cast<const uint4*>(p.o + grow * 64);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) orow[c] = __ldg(op + c);
-        } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        // D_i = dO_i . o_i (dO from its tile, o from the first ring item)
         mbar_wait(B_QDO, 0, aborted, p.err);
         uint32_t gw[32];  // dO row (bf16 pairs)
         load_row_sw(smem + kOffDO, r, gw);
         float D;
         {
+            mbar_wait(B_FULL(0), 0, aborted, p.err);
+            const uint8_t* orow = smem + kOffRing;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                fma2_bf16(gw[4 * c + 0], orow[c].x, a0, a1);
-                fma2_bf16(gw[4 * c + 1], orow[c].y, a2, a3);
-                fma2_bf16(gw[4 * c + 2], orow[c].z, a0, a1);
-                fma2_bf16(gw[4 * c + 3], orow[c].w, a2, a3);
+                const uint4 x = *reinterpret_cast<const uint4*>(orow + sw128_off(r, c));
+                fma2_bf16(gw[4 * c + 0], x.x, a0, a1);
+                fma2_bf16(gw[4 * c + 1], x.y, a2, a3);
+                fma2_bf16(gw[4 * c + 2], x.z, a0, a1);
+                fma2_bf16(gw[4 * c + 3], x.w, a2, a3);
             }
             D = (a0 + a1) + (a2 + a3);
+            mbar_arrive(B_EMPTY(0));
         }
         if (row_ok) {
             p.delta[wrow] = D;
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
         float dq[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) dq[c] = 0.f;
-        uint32_t seq = 0;
+        uint32_t seq = 1;  // ring item 0 was the O tile
         const int64_t pds_row = (int64_t)z * p.n_max * p.T_pad + i;
 #pragma unroll 1
         for (int k = 0; k < n_act; ++k) {
@@ -815,13 +816,12 @@ fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, c
     // thread (a fresh thread, e.g. autograd's, may have none), which the encoding needs
     P.err = device_error_word();
     if (!P.err) return cuda_fail(-1, "cudaGetSymbolAddress (error word)");
-    const void* bases[7] = {q, k, v, dO, dq, dk, dv};
-    CUtensorMap* maps[7] = {&P.tm_q, &P.tm_k, &P.tm_v, &P.tm_do, &P.tm_dq, &P.tm_dk, &P.tm_dv};
-    for (int m = 0; m < 7; ++m) {
+    const void* bases[8] = {q, k, v, dO, dq, dk, dv, o};
+    CUtensorMap* maps[8] = {&P.tm_q, &P.tm_k, &P.tm_v, &P.tm_do, &P.tm_dq, &P.tm_dk, &P.tm_dv, &P.tm_o};
+    for (int m = 0; m < 8; ++m) {
         const int r = make_bf16_rows_map(maps[m], bases[m], slices, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (bwd)");
     }
-    P.o = static_cast<const __nv_bfloat16*>(o);
     P.lse = lse;
     P.delta = delta;
     P.lse2 = lse2;
