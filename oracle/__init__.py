@@ -16,7 +16,9 @@ formula, the schedule endpoints and the coprime multiset, the power-of-two
 offsets the pages name at 4x length, dense causal attention (W >= T), sliding
 window attention (empty table), the library masked-attention routine with a
 brute-force mask, V = 1, Q = 0, the first query, and central finite differences
-plus autograd for the backward.
+plus autograd for the backward; for fractional offsets, the integer-alpha reduction,
+values linear in position, keys linear in position (closed-form scores), and
+continuity at integer alpha.
 """
 from __future__ import annotations
 
@@ -28,7 +30,7 @@ import numpy as np
 
 from . import schedule
 from .schedule import (FIB, POW2, FIXED, LINEAR, COPRIME, alpha_for_layer, fibonacci_base,
-                       key_set, layer_table, offset_table, round_half_up)
+                       frac_distances, key_set, layer_table, offset_table, round_half_up)
 
 _lib = None
 
@@ -50,6 +52,9 @@ def lib():
         L.oracle_bwd.restype = ctypes.c_int
         L.oracle_key_set.argtypes = [i64, i64, ip, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]
         L.oracle_key_set.restype = i64
+        L.oracle_fwd_frac.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, ctypes.c_double,
+                                      dp, ip, i64, ip, ctypes.c_int]
+        L.oracle_fwd_frac.restype = ctypes.c_int
         L.oracle_threads.argtypes = [ctypes.c_int]
         L.oracle_threads.restype = ctypes.c_int
         _lib = L
@@ -134,6 +139,38 @@ def fwd(q, k, v, W: int, tables, scale: float | None = None, n_threads: int = 0)
     return out.reshape(shape), lse.reshape(shape[:-1])
 
 
+def fwd_frac(q, k, v, W: int, dist_tables, scale: float | None = None, n_threads: int = 0):
+    """Forward with fractional offsets in fp64: dist_tables is one list of real distances
+    (schedule.frac_distances) per index of the leading axis, or one list for all slices.
+    Returns (out, lse)."""
+    qs, shape = _as_slices(q)
+    ks, _ = _as_slices(k)
+    vs, _ = _as_slices(v)
+    T, d = shape[-2], shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    n_slices = qs.shape[0]
+    per_layer = len(dist_tables) > 0 and isinstance(dist_tables[0], (list, tuple, np.ndarray))
+    tabs = [list(map(float, t)) for t in dist_tables] if per_layer else [list(map(float, dist_tables))]
+    if per_layer and (len(shape) < 3 or len(tabs) != shape[0]):
+        raise ValueError("need one distance list per index of the leading axis")
+    tos = np.repeat(np.arange(len(tabs), dtype=np.int32), n_slices // len(tabs))
+    cap = max([1] + [len(t) for t in tabs])
+    arr = np.zeros((len(tabs), cap), dtype=np.float64)
+    cnt = np.zeros(len(tabs), dtype=np.int32)
+    for r, t in enumerate(tabs):
+        arr[r, :len(t)] = t
+        cnt[r] = len(t)
+    out = np.zeros_like(qs)
+    lse = np.zeros(qs.shape[:-1], dtype=np.float64)
+    rc = lib().oracle_fwd_frac(_dptr(qs), _dptr(ks), _dptr(vs), _dptr(out), _dptr(lse), n_slices,
+                               T, d, int(W), float(scale), _dptr(arr), _iptr(cnt), cap,
+                               _iptr(tos), int(n_threads))
+    if rc:
+        raise MemoryError("oracle_fwd_frac failed")
+    return out.reshape(shape), lse.reshape(shape[:-1])
+
+
 def bwd(q, k, v, dout, W: int, tables, scale: float | None = None, n_threads: int = 0):
     """Sparse attention backward in fp64. Returns (dq, dk, dv, out, lse)."""
     qs, shape = _as_slices(q)
@@ -160,5 +197,5 @@ def bwd(q, k, v, dout, W: int, tables, scale: float | None = None, n_threads: in
 
 
 __all__ = ["schedule", "FIB", "POW2", "FIXED", "LINEAR", "COPRIME", "alpha_for_layer",
-           "fibonacci_base", "key_set", "key_set_c", "layer_table", "offset_table",
-           "round_half_up", "fwd", "bwd", "threads", "lib"]
+           "fibonacci_base", "frac_distances", "key_set", "key_set_c", "layer_table",
+           "offset_table", "round_half_up", "fwd", "fwd_frac", "bwd", "threads", "lib"]

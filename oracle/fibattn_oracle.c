@@ -22,6 +22,14 @@
  *   dQ_i = scale * sum_j dS_ij k_j,  dK_j += scale * dS_ij q_i,  dV_j += P_ij dO_i.
  * RoPE is applied before the gather on the pages; here Q and K arrive rotated.
  *
+ * Fractional ("learned") offsets (same page, "Implementacao" under Arquitetura: to let the
+ * gradient reach alpha when offsets are not integers, keys and values are linearly
+ * interpolated between rows): with real distances d_k = alpha * f_k, query i attends its
+ * window plus, for every d_k <= i, one interpolated key/value at position p = i - d_k:
+ *   lo = floor(p), w = p - lo,  k~ = (1 - w) k[lo] + w k[lo + 1],  v~ likewise
+ * (lo + 1 <= i - W + 1 <= i because d_k >= W). Softmax over the window keys and the
+ * interpolated keys together, as above.
+ *
  * Layout: every tensor is [n_slices][T][d] row-major float64; lse is [n_slices][T].
  * Slices are independent; OpenMP runs them in parallel when built with -fopenmp.
  */
@@ -122,6 +130,54 @@ static void bwd_slice(const double* q, const double* k, const double* v, const d
     }
 }
 
+/* Forward of one slice with fractional offsets (dists: n_dist real distances, ascending). */
+static void fwd_frac_slice(const double* q, const double* k, const double* v, double* out,
+                           double* lse, int64_t T, int64_t d, int64_t W, double scale,
+                           const double* dists, int n_dist, double* s, double* keyv, double* valv) {
+    for (int64_t i = 0; i < T; ++i) {
+        /* materialise the attended keys and values of query i */
+        int64_t n = 0;
+        int64_t lo_w = i - W + 1;
+        if (lo_w < 0) lo_w = 0;
+        for (int64_t j = lo_w; j <= i; ++j, ++n) {
+            memcpy(keyv + n * d, k + j * d, sizeof(double) * (size_t)d);
+            memcpy(valv + n * d, v + j * d, sizeof(double) * (size_t)d);
+        }
+        for (int t = 0; t < n_dist; ++t) {
+            double pos = (double)i - dists[t];
+            if (pos < 0.0) continue;
+            int64_t lo = (int64_t)floor(pos);
+            double w = pos - (double)lo;
+            for (int64_t c = 0; c < d; ++c) {
+                double khi = w != 0.0 ? k[(lo + 1) * d + c] : 0.0;
+                double vhi = w != 0.0 ? v[(lo + 1) * d + c] : 0.0;
+                keyv[n * d + c] = (1.0 - w) * k[lo * d + c] + w * khi;
+                valv[n * d + c] = (1.0 - w) * v[lo * d + c] + w * vhi;
+            }
+            ++n;
+        }
+        /* softmax attention over them */
+        double m = -INFINITY;
+        for (int64_t a = 0; a < n; ++a) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < d; ++c) acc += q[i * d + c] * keyv[a * d + c];
+            s[a] = scale * acc;
+            if (s[a] > m) m = s[a];
+        }
+        double l = 0.0;
+        for (int64_t a = 0; a < n; ++a) {
+            s[a] = exp(s[a] - m);
+            l += s[a];
+        }
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t a = 0; a < n; ++a) acc += s[a] * valv[a * d + c];
+            out[i * d + c] = acc / l;
+        }
+        lse[i] = m + log(l);
+    }
+}
+
 static int set_threads(int n_threads) {
 #ifdef _OPENMP
     if (n_threads > 0) omp_set_num_threads(n_threads);
@@ -196,6 +252,38 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
         }
         free(keys);
         free(s);
+    }
+    return err;
+}
+
+/* Forward with fractional offsets over n_slices slices; dists is [n_tables][cap] doubles. */
+int oracle_fwd_frac(const double* q, const double* k, const double* v, double* out, double* lse,
+                    int64_t n_slices, int64_t T, int64_t d, int64_t W, double scale,
+                    const double* dists, const int32_t* counts, int64_t cap,
+                    const int32_t* table_of_slice, int n_threads) {
+    set_threads(n_threads);
+    int err = 0;
+#pragma omp parallel
+    {
+        int64_t nk = T + cap + 1;
+        double* s = (double*)malloc(sizeof(double) * (size_t)nk);
+        double* keyv = (double*)malloc(sizeof(double) * (size_t)(nk * d));
+        double* valv = (double*)malloc(sizeof(double) * (size_t)(nk * d));
+        if (!s || !keyv || !valv) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic)
+            for (int64_t sl = 0; sl < n_slices; ++sl) {
+                int32_t t = table_of_slice[sl];
+                fwd_frac_slice(q + sl * T * d, k + sl * T * d, v + sl * T * d, out + sl * T * d,
+                               lse + sl * T, T, d, W, scale, dists + (int64_t)t * cap, counts[t],
+                               s, keyv, valv);
+            }
+        }
+        free(s);
+        free(keyv);
+        free(valv);
     }
     return err;
 }
