@@ -6,12 +6,16 @@ backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
 (B=8, H=8, T=1024, d=64), W=64, coprime reassignment (l -> 5l mod 16) of the linear
 stagger alpha 0.5 -> 2.0, bf16, forward + backward.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
 (weak scaling: the (layer, batch, head) slices are independent, no collective on the
 data path); value = all ranks' query tokens / max-over-ranks time.
+
+c3f is the fractional-offset (learned-alpha) forward on the c3 shape; its line adds
+"static_counterpart", the static forward of c3 (same shape and alpha range) timed in the
+same process, and their latency ratio.
 """
 from __future__ import annotations
 
@@ -41,6 +45,8 @@ UNIT = "query-tokens/s"
 # are on-chip reuse, not compulsory traffic.
 ALGO_BYTES = {
     "fwd_tc_bf16": 3 * 128 + 128 + 4,          # q, k, v in; o, lse out
+    "fwd_frac_tc_bf16": 3 * 128 + 128 + 4,     # the same for fractional offsets
+    "fwd_frac_simt_f32": 3 * 256 + 256 + 4,
     "fwd_simt_bf16": 3 * 128 + 128 + 4,
     "fwd_simt_f32": 3 * 256 + 256 + 4,
     "bwd_delta_simt": 2 * 256 + 4,              # fp32: o, dO in; D out
@@ -52,6 +58,7 @@ ALGO_BYTES = {
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
+    "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu",
     "bwd_delta_simt": "simt.cu", "bwd_dq_simt": "simt.cu", "bwd_dkdv_simt": "simt.cu",
     "bwd_dq_tc": "bwd_tc.cu", "bwd_dkdv_tc": "bwd_tc.cu",
 }
@@ -62,7 +69,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="c5", choices=["c5", "c4", "c2", "c3", "c3p"])
+    ap.add_argument("--workload", default="c5", choices=["c5", "c4", "c2", "c3", "c3p", "c3f"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -199,7 +206,9 @@ def run_ours(a, spec, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     L = fa.lib()
-    sched = fa.Schedule(**spec["sched"])
+    frac = "alphas" in spec
+    sched = None if frac else fa.Schedule(**spec["sched"])
+    alphas = fi.frac_alphas(spec) if frac else None
     inp = fi.workload_inputs(a.workload)
     d_in = {n: t.to(dev) for n, t in inp.items()}
     W = spec["W"]
@@ -215,7 +224,10 @@ def run_ours(a, spec, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def step(x):
-        fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
+        if frac:
+            fa.fwd_frac(x["q"], x["k"], x["v"], W, alphas, spec["base"], out=o, lse=lse)
+        else:
+            fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
         if train:
             fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched, dq=dq, dk=dk, dv=dv,
                    workspace=ws)
@@ -293,7 +305,31 @@ def run_ours(a, spec, world, rank, local):
     # ---- end to end through the public API, host buffers, copies inside the timed region
     e2e = None
     if not a.no_e2e:
-        e2e = run_e2e(fa, a, spec, inp, sched, dev, stream, world)
+        e2e = run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas)
+
+    # ---- fractional workload: the static forward of the same shape, timed the same way
+    counterpart = None
+    if frac:
+        cname = "c3"
+        cspec = fi.WORKLOADS[cname]
+        csched = fa.Schedule(**cspec["sched"])
+        cin = {n: t.to(dev) for n, t in fi.workload_inputs(cname).items()}
+        for _ in range(a.warmup):
+            fa.fwd(cin["q"], cin["k"], cin["v"], cspec["W"], csched, out=o, lse=lse)
+            flush.fill_(1.0)
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(a.steps)]
+        for s, e in cev:
+            s.record(stream)
+            fa.fwd(cin["q"], cin["k"], cin["v"], cspec["W"], csched, out=o, lse=lse)
+            e.record(stream)
+            flush.fill_(1.0)
+        torch.cuda.synchronize(dev)
+        fa.poll_device_error(dev)
+        cms = sum(s.elapsed_time(e) for s, e in cev) / a.steps
+        counterpart = {"workload": f"{cname}: {cspec['desc']}", "ms_per_step": round(cms, 4),
+                       "frac_over_static": round(ms_per_step / cms, 3)}
+        del cin
 
     out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -301,12 +337,16 @@ def run_ours(a, spec, world, rank, local):
            "data": "synthetic (seeded N(0,1)*scale inputs shaped like the pages' model; no dataset)",
            "config": {"workload": f"{a.workload}: {spec['desc']}", "layers": spec["Lc"],
                       "B": spec["B"], "H": spec["H"], "T": spec["T"], "d_head": spec["d"],
-                      "W": spec["W"], "schedule": spec["sched"], "passes": list(spec["passes"]),
+                      "W": spec["W"], "passes": list(spec["passes"]),
+                      **({"base": spec["base"], "alphas": [round(x, 6) for x in alphas]} if frac
+                         else {"schedule": spec["sched"]}),
                       "parallelism": f"replicas x{world} (independent batches, no collective)",
                       "l2": "inputs larger than L2 and L2 flushed between steps (outside the "
                             "timed event pairs)"},
            "roofline": roof, "kernels": kernels, "gpu_launches": int(launches),
            "clocks": clk.summary(), "e2e": e2e}
+    if counterpart:
+        out["static_counterpart"] = counterpart
     return out
 
 
@@ -319,7 +359,7 @@ def clock_index(local):
     return local
 
 
-def run_e2e(fa, a, spec, inp, sched, dev, stream, world):
+def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None):
     pinned = {n: t.pin_memory() for n, t in inp.items()}
     W = spec["W"]
     train = "bwd" in spec["passes"]
@@ -335,7 +375,10 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world):
 
     def step():
         x = {n: t.to(dev, non_blocking=True) for n, t in pinned.items()}
-        o, lse = fa.fwd(x["q"], x["k"], x["v"], W, sched)
+        if alphas is not None:
+            o, lse = fa.fwd_frac(x["q"], x["k"], x["v"], W, alphas, spec["base"])
+        else:
+            o, lse = fa.fwd(x["q"], x["k"], x["v"], W, sched)
         res = {"o": o, "lse": lse}
         if train:
             dq, dk, dv = fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched)
@@ -375,7 +418,8 @@ def oracle_sample(spec, n_slices, n_threads=0):
 
     import oracle
 
-    sc = spec["sched"]
+    sc = spec.get("sched")
+    alphas = fi.frac_alphas(spec) if "alphas" in spec else None
     T, W = spec["T"], spec["W"]
     layers = sorted({(i * 7) % spec["Lc"] for i in range(n_slices)})
     name = [k for k, v in fi.WORKLOADS.items() if v is spec][0]
@@ -392,12 +436,17 @@ def oracle_sample(spec, n_slices, n_threads=0):
     t0 = time.perf_counter()
     done = 0
     for li, l in enumerate(layers):
-        tab = oracle.layer_table(sc["base"], sc["kind"], l, sc["n_layers"], W, T,
-                                 sc.get("base_max", 0), **kw_of())
         picks = per_layer[l]
         if not picks:
             continue
         g = lambda n: np.stack([f64(inp[n][li, b, h]) for b, h in picks])
+        if alphas is not None:
+            dists = oracle.frac_distances(alphas[l], spec["base"], W, T)
+            oracle.fwd_frac(g("q"), g("k"), g("v"), W, dists, None, n_threads)
+            done += len(picks) * T
+            continue
+        tab = oracle.layer_table(sc["base"], sc["kind"], l, sc["n_layers"], W, T,
+                                 sc.get("base_max", 0), **kw_of())
         if "bwd" in spec["passes"]:
             oracle.bwd(g("q"), g("k"), g("v"), g("dO"), W, tab, None, n_threads)
         else:
@@ -407,9 +456,14 @@ def oracle_sample(spec, n_slices, n_threads=0):
 
 
 def calibrate_slices(spec, target_s):
-    """Slices of oracle work that take about target_s seconds on this host."""
-    sec, toks, _ = oracle_sample(spec, 4)
-    per_slice = sec / 4
+    """Slices of oracle work that take about target_s seconds on this host. The probe runs
+    two slices per OpenMP thread, so that its per-slice time includes the parallel speed-up
+    the full sample gets."""
+    import oracle
+
+    n0 = max(4, 2 * oracle.threads(0))
+    sec, toks, _ = oracle_sample(spec, n0)
+    per_slice = sec / n0
     return max(1, int(target_s / max(per_slice, 1e-6)))
 
 
@@ -434,7 +488,8 @@ def run_reference(a, spec, world, rank):
             "data": "synthetic (same seeded inputs as the GPU arm)",
             "config": {"workload": f"{a.workload}: {spec['desc']}", "layers": spec["Lc"],
                        "B": spec["B"], "H": spec["H"], "T": spec["T"], "d_head": spec["d"],
-                       "W": spec["W"], "schedule": spec["sched"]},
+                       "W": spec["W"], "schedule": spec.get("sched"),
+                       "alphas": fi.frac_alphas(spec) if "alphas" in spec else None},
             "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,

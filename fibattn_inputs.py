@@ -79,7 +79,21 @@ WORKLOADS = {
                W=64, seed=4, scale=0.125, names=("q", "k", "v", "dO"), passes=("fwd", "bwd"),
                sched=dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
                           n_layers=16, coprime_c=5)),
+    "c3f": dict(desc="16-layer stack, fractional (learned-style) alphas in [0.5, 2.0], bf16",
+                dtype="bf16", Lc=16, B=8, H=8, T=1024, d=64, W=64, seed="per_layer:2",
+                scale=0.125, names=("q", "k", "v"), passes=("fwd",), base="fib",
+                alphas=dict(lo=0.5, hi=2.0, seed=7)),
 }
+
+
+def frac_alphas(spec):
+    """Per-layer float32 alphas of a fractional-offset workload: Lc uniform draws in
+    [lo, hi) from their own generator, sorted ascending (deeper layers reach further, as
+    in a stagger). Returns a list of Python floats holding float32 values."""
+    a = spec["alphas"]
+    g = torch.Generator("cpu").manual_seed(int(a["seed"]))
+    x = torch.rand(spec["Lc"], generator=g, dtype=torch.float32) * (a["hi"] - a["lo"]) + a["lo"]
+    return [float(v) for v in torch.sort(x).values]
 
 
 def seed_of(spec):

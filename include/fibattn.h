@@ -129,6 +129,40 @@ FIBATTN_API fibattn_status fibattn_fwd(const void* q, const void* k, const void*
                            int32_t n_layers_call, void* cuda_stream);
 
 /*
+ * Fractional-offset table of one real alpha: the learned-alpha variant of the pages
+ * (Metodologia / Arquitetura, "Implementacao": keys and values are linearly interpolated
+ * between rows so that the gradient reaches alpha when alpha * F is not an integer).
+ * Real distances d = (double)alpha * F for the base values F of `base` / `base_max` (as in
+ * fibattn_schedule), kept when W <= d <= T - 1, ascending. Entry n: ceil_out[n] = ceil(d),
+ * w_out[n] = (float)(ceil(d) - d), the weight of the row after i - ceil(d) (0 for an
+ * integer d). alpha: finite, 0 < alpha <= FIBATTN_RATIO_MAX.
+ * Errors: INVALID_ARG (null with cap > 0, W < 1, T < 1, bad base, bad alpha), CAPACITY (more
+ * than `cap` entries; *n_out then holds the needed count).
+ */
+FIBATTN_API fibattn_status fibattn_frac_offsets(float alpha, int32_t base, int64_t base_max,
+                                                int32_t W, int32_t T, int32_t* ceil_out,
+                                                float* w_out, int32_t cap, int32_t* n_out);
+
+/*
+ * Forward with fractional offsets (same page and passage): query i of call-layer c attends
+ * its window i-W+1..i and, for every distance d of alphas[c]'s table (fibattn_frac_offsets)
+ * with i >= d, the key and value interpolated at the real position i - d:
+ *     x~ = (1 - w) x[i - ceil(d)] + w x[i - ceil(d) + 1],  w = ceil(d) - d,
+ * with softmax over all of them. An integer alpha gives exactly the static forward's
+ * attended set (fibattn_fwd with alpha num/1).
+ *   alphas : host float [n_layers_call], read during the call.
+ *   base, base_max : as in fibattn_schedule. Other arguments as fibattn_fwd.
+ * bf16 runs on the tcgen05 forward kernel in its fractional mode; f32 on a SIMT kernel.
+ * Errors: INVALID_ARG (also a bad alpha or base), UNSUPPORTED, CAPACITY (a table above
+ * FIBATTN_MAX_OFFSETS), CUDA.
+ */
+FIBATTN_API fibattn_status fibattn_fwd_frac(const void* q, const void* k, const void* v, void* o,
+                                            float* lse, int32_t B, int32_t H, int32_t T,
+                                            int32_t d, int32_t dtype, int32_t W, float scale,
+                                            int32_t base, int64_t base_max, const float* alphas,
+                                            int32_t n_layers_call, void* cuda_stream);
+
+/*
  * Workspace the backward needs for one call, in bytes (write it to *bytes). f32 calls:
  *   D [Lc][B][H][T] float32 (D_i = dO_i . o_i). bf16 calls, with rows padded to
  *   T_pad = T rounded up to a multiple of 4: D and lse * log2(e), each [Lc][B][H][T_pad]

@@ -23,7 +23,7 @@ import torch
 __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd",
            "keyset_debug", "poll_device_error", "status_string", "lib", "library_path",
            "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
-           "bwd_workspace_size", "last_cuda_error"]
+           "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
@@ -101,6 +101,11 @@ def lib():
         L.fibattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, sp, i32,
                                   i32, vp]
         u64 = ctypes.c_uint64
+        i64 = ctypes.c_int64
+        L.fibattn_frac_offsets.argtypes = [f32, i32, i64, i32, i32, ctypes.POINTER(i32),
+                                           ctypes.POINTER(f32), i32, ctypes.POINTER(i32)]
+        L.fibattn_fwd_frac.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                       i64, ctypes.POINTER(f32), i32, vp]
         L.fibattn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, sp, i32, i32,
                                                  ctypes.POINTER(u64)]
         L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32, i32,
@@ -123,7 +128,8 @@ def lib():
         L.fibattn_launch_count.restype = ctypes.c_int64
         for name in ("fibattn_offsets", "fibattn_offsets_device", "fibattn_fwd", "fibattn_bwd",
                      "fibattn_bwd_workspace_size",
-                     "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error"):
+                     "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error",
+                     "fibattn_frac_offsets", "fibattn_fwd_frac"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -211,6 +217,38 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, sched: Schedu
                            _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0, Lc,
                            _stream(q))
     _check(st, "fibattn_fwd")
+    return o, lse
+
+
+def frac_offsets(alpha: float, W: int, T: int, base: str = "fib", base_max: int = 0):
+    """Fractional-offset table of a real alpha (fibattn_frac_offsets): (ceil(d) list, weight
+    list) for the distances d = alpha * F kept by the table rule, alpha taken as float32."""
+    cap = MAX_OFFSETS
+    cbuf = (ctypes.c_int32 * cap)()
+    wbuf = (ctypes.c_float * cap)()
+    n = ctypes.c_int32(0)
+    _check(lib().fibattn_frac_offsets(float(alpha), _BASES[base], int(base_max), W, T, cbuf, wbuf,
+                                      cap, ctypes.byref(n)), "fibattn_frac_offsets")
+    return list(cbuf[: n.value]), list(wbuf[: n.value])
+
+
+def fwd_frac(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, alphas: Sequence[float],
+             base: str = "fib", base_max: int = 0, scale: Optional[float] = None,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """Forward with fractional offsets (learned alphas, one float per call-layer, linear
+    interpolation between key/value rows); returns (o, lse)."""
+    Lc, B, H, T, d = _shape(q)
+    if len(alphas) != Lc:
+        raise ValueError("need one alpha per layer of the call")
+    o = torch.empty_like(q) if out is None else out
+    _check_tensors(q, k, v, o)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    a = (ctypes.c_float * Lc)(*[float(x) for x in alphas])
+    st = lib().fibattn_fwd_frac(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, d,
+                                _DTYPES[q.dtype], W, float(scale or 0.0), _BASES[base],
+                                int(base_max), a, Lc, _stream(q))
+    _check(st, "fibattn_fwd_frac")
     return o, lse
 
 

@@ -173,6 +173,58 @@ fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o,
     return FIBATTN_OK;
 }
 
+fibattn_status fibattn_frac_offsets(float alpha, int32_t base, int64_t base_max, int32_t W,
+                                    int32_t T, int32_t* ceil_out, float* w_out, int32_t cap,
+                                    int32_t* n_out) {
+    if (!n_out || cap < 0 || (cap > 0 && (!ceil_out || !w_out))) return FIBATTN_ERR_INVALID_ARG;
+    return build_frac_table(base, base_max, alpha, W, T, ceil_out, w_out, cap, n_out);
+}
+
+fibattn_status fibattn_fwd_frac(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype,
+                                int32_t W, float scale, int32_t base, int64_t base_max,
+                                const float* alphas, int32_t n_layers_call, void* cuda_stream) {
+    if (!q || !k || !v || !o || !lse || !alphas) return FIBATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FIBATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 1 || W < 1 || n_layers_call < 1 || n_layers_call > FIBATTN_LAYERS_MAX)
+        return FIBATTN_ERR_INVALID_ARG;
+    if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
+    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    const int64_t per_layer = (int64_t)B * H * T;
+    if (per_layer > ((int64_t)1 << 34) || per_layer * n_layers_call > ((int64_t)1 << 40))
+        return FIBATTN_ERR_INVALID_ARG;
+    // every layer's table is validated before anything is launched
+    for (int32_t c = 0; c < n_layers_call; ++c) {
+        int32_t n = 0;
+        fibattn_status st = build_frac_table(base, base_max, alphas[c], W, T, nullptr, nullptr, 0, &n);
+        if (st == FIBATTN_ERR_INVALID_ARG) return st;
+        if (n > kMaxOffsets) return FIBATTN_ERR_CAPACITY;
+    }
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    const size_t es = elt_size(dtype);
+    for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
+        const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
+        FracTables t;
+        fibattn_status st = build_frac_launch_tables(base, base_max, alphas + c, n, W, T, &t);
+        if (st != FIBATTN_OK) return st;
+        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        const size_t off = (size_t)c * per_layer * d * es;
+        const char* qc = (const char*)q + off;
+        const char* kc = (const char*)k + off;
+        const char* vc = (const char*)v + off;
+        char* oc = (char*)o + off;
+        float* lc = lse + (size_t)c * per_layer;
+        if (dtype == FIBATTN_F32)
+            st = launch_fwd_frac_simt_f32((const float*)qc, (const float*)kc, (const float*)vc,
+                                          (float*)oc, lc, sh, t, as_stream(cuda_stream));
+        else
+            st = launch_fwd_frac_tc_bf16(qc, kc, vc, oc, lc, sh, t, as_stream(cuda_stream));
+        if (st != FIBATTN_OK) return st;
+    }
+    return FIBATTN_OK;
+}
+
 fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int32_t T, int32_t d,
                                           int32_t dtype, int32_t W, const fibattn_schedule* sched,
                                           int32_t layer0, int32_t n_layers_call, uint64_t* bytes) {

@@ -435,7 +435,6 @@ struct Plan {
     __device__ __forceinline__ int nch(int g) const {
         return min(kMaxGroupChunks, n_chunks - g * kMaxGroupChunks);
     }
-    __device__ __forceinline__ uint32_t band_items() const { return 2 * n_groups + n_chunks; }
 };
 
 __device__ __forceinline__ Plan make_plan(const BwdParams& p, int layer, int32_t j0) {

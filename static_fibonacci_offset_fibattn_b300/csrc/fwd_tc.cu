@@ -26,6 +26,16 @@
 //   maxima and are merged once in the epilogue.
 // Epilogue: O = (O_band 2^(m_b-m) + O_off 2^(m_o-m)) / l, staged in a ring slot,
 //   TMA-stored; lse = (m + log2 l) ln 2.
+//
+// Fractional offsets (the learned-alpha variant; Metodologia / Arquitetura, "Implementacao":
+// keys and values linearly interpolated between rows so that the gradient reaches alpha)
+// reuse the same kernel (kFrac): a real distance d is held as c = ceil(d) and the weight
+// w = c - d of the row after i - c, and query i >= c attends
+//   k~ = (1 - w) k_{i-c} + w k_{i-c+1},  v~ likewise.
+// Each shifted item then also carries the 8 rows after its 128-row tile (a 17 KB slot), so
+// that row r finds both of its rows, r and r + 1, in the slot; the score is the lerp of the
+// two row dot products and the value update two axpys with p (1 - w) and p w. A distance
+// with w = 0 takes the static code path, so integer alphas give the static results.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -50,8 +60,12 @@ constexpr uint32_t kTmemO = 192;    // O accumulator columns [192, 256)
 constexpr uint32_t kChunkBytes = kChunk * 128;  // 8 KB
 constexpr uint32_t kSlots = 6;
 
-constexpr uint32_t kOffRing = 0;
-constexpr uint32_t kOffBar = kOffRing + kSlots * ring::kSlotBytes;
+// shared memory: the ring slots, then the barriers, then the TMEM address word
+template <bool kFrac>
+struct Layout {
+    static constexpr uint32_t kSlot = ring::kSlotBytes + (kFrac ? 1024u : 0u);
+    static constexpr uint32_t kOffBar = kSlots * kSlot;
+};
 // barriers: FULL[kSlots], EMPTY[kSlots], then S ready, P written (4 warps), PV done,
 // TMEM free (4 warps), band items landed; then the TMEM address word. The Q slot is released
 // by the row warps once they hold their q rows (the S MMAs reading it are complete by then).
@@ -62,9 +76,10 @@ constexpr uint32_t kOffBar = kOffRing + kSlots * ring::kSlotBytes;
 constexpr uint32_t kBarS = 2 * kSlots, kBarP = kBarS + 1, kBarO = kBarS + 2, kBarT = kBarS + 3,
                    kBarL = kBarS + 4;
 constexpr uint32_t kNumBars = kBarL + 1;
-constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffTmemSlot + 16;
-constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+template <bool kFrac>
+__host__ __device__ constexpr uint32_t tmem_slot_off() { return Layout<kFrac>::kOffBar + kNumBars * 8; }
+template <bool kFrac>
+__host__ __device__ constexpr uint32_t smem_alloc() { return tmem_slot_off<kFrac>() + 16 + 1024; }  // + alignment slack
 
 struct FwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3D {64, T, slices}, box {64, 64, 1}, 128B swizzle
@@ -75,7 +90,16 @@ struct FwdParams {
     int32_t T, W;
     int32_t tiles_per_slice;
     float scale_log2;  // scale * log2(e)
-    OffsetTables tabs;
+    OffsetTables tabs;          // fractional mode: ceil(d) of each real distance d
+};
+
+template <bool kFrac>
+struct FwdArgs : FwdParams {};
+
+template <>
+struct FwdArgs<true> : FwdParams {
+    CUtensorMap tm_k8, tm_v8;  // 8-row boxes: the rows just past a shifted tile
+    float w[kMaxLayersPerLaunch][kMaxOffsets];  // weight ceil(d) - d of the later row
 };
 
 // The band and offset extents of one tile; every role derives the same item sequence.
@@ -111,8 +135,11 @@ __device__ __forceinline__ Plan make_plan(const FwdParams& p, int layer, int32_t
     return pl;
 }
 
+template <bool kFrac>
 __global__ void __launch_bounds__(kThreads, 2)
-fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
+    using L = Layout<kFrac>;
+    constexpr uint32_t kOffTmemSlot = tmem_slot_off<kFrac>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
@@ -122,8 +149,8 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
     const int lane = tid & 31;
     const int32_t T = p.T, W = p.W;
 
-    const ring::Ring rg{sbase + kOffRing, sbase + kOffBar, kSlots, 4};  // 4 row warps
-    auto bar = [&](uint32_t idx) { return sbase + kOffBar + 8u * idx; };
+    const ring::Ring rg{sbase, sbase + L::kOffBar, kSlots, 4, L::kSlot};  // 4 row warps
+    auto bar = [&](uint32_t idx) { return sbase + L::kOffBar + 8u * idx; };
     const uint32_t B_S = bar(kBarS), B_P = bar(kBarP), B_O = bar(kBarO), B_T = bar(kBarT),
                    B_L = bar(kBarL);
     auto slot_ptr = [&](uint32_t seq) { return smem + (rg.addr(seq) - sbase); };
@@ -154,6 +181,10 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
             prefetch_tmap(&p.tm_k);
             prefetch_tmap(&p.tm_v);
             prefetch_tmap(&p.tm_o);
+            if constexpr (kFrac) {
+                prefetch_tmap(&p.tm_k8);
+                prefetch_tmap(&p.tm_v8);
+            }
             uint32_t seq = 0;
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
                 const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer);
@@ -181,16 +212,23 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
                         }
                     }
                 }
-                // offsets: K_o then V_o
+                // offsets: K_o then V_o (fractional w != 0: plus the 8 rows after the tile)
                 const int32_t* offs = p.tabs.off[tl.layer];
                 for (int k = 0; k < pl.n_act; ++k) {
                     const int32_t y = pl.i0 - offs[k];
+                    bool side = false;
+                    if constexpr (kFrac) side = p.w[tl.layer][k] != 0.f;
                     for (int h = 0; h < 2; ++h, ++seq) {
                         const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
                         if (!rg.acquire(seq, aborted, p.err)) continue;
-                        mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes);
+                        mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + (side ? 1024u : 0u));
                         tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, z);
                         tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, z);
+                        if constexpr (kFrac) {
+                            if (side)
+                                tma_load_3d(rg.addr(seq) + ring::kSlotBytes, h == 0 ? &p.tm_k8 : &p.tm_v8,
+                                            rg.full(seq), 0, y + kRows, z);
+                        }
                     }
                 }
                 // output staging slot
@@ -373,6 +411,9 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
 #pragma unroll 1
             for (int k = 0; k < pl.n_act; ++k) {
                 const bool valid = i - offs[k] >= 0;
+                float wk = 0.f;  // weight of row r + 1 (fractional mode); uniform over the CTA
+                if constexpr (kFrac) wk = p.w[tl.layer][k];
+                const bool lerp = kFrac && wk != 0.f;
                 rg.wait_full(seq, aborted, p.err);
                 const uint8_t* krow = slot_ptr(seq);
                 float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -384,9 +425,23 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
                     fma2_bf16(qw[4 * c + 2], w.z, a0, a1);
                     fma2_bf16(qw[4 * c + 3], w.w, a2, a3);
                 }
+                float s = (a0 + a1) + (a2 + a3);
+                if (lerp) {
+                    // row r + 1 of the item (row 128 is the first of the 8 extra rows)
+                    float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r + 1, c));
+                        fma2_bf16(qw[4 * c + 0], w.x, b0, b1);
+                        fma2_bf16(qw[4 * c + 1], w.y, b2, b3);
+                        fma2_bf16(qw[4 * c + 2], w.z, b0, b1);
+                        fma2_bf16(qw[4 * c + 3], w.w, b2, b3);
+                    }
+                    s = fmaf(wk, ((b0 + b1) + (b2 + b3)) - s, s);
+                }
                 rg.release_warp(seq, lane);
                 ++seq;
-                const float sc = valid ? ((a0 + a1) + (a2 + a3)) * sl2 : -INFINITY;
+                const float sc = valid ? s * sl2 : -INFINITY;
                 if (sc > m_o + 8.f) {
                     const float corr = m_o == -INFINITY ? 0.f : ex2(m_o - sc);
                     l_o *= corr;
@@ -396,7 +451,8 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
                 }
                 const float pk = valid ? ex2(sc - m_o) : 0.f;
                 l_o += pk;
-                const uint32_t pb = pack_bf16x2(pk, 0.f);
+                const float phi = pk * wk;  // fractional mode: the later row's share
+                const uint32_t pb = pack_bf16x2(lerp ? pk - phi : pk, 0.f);
                 rg.wait_full(seq, aborted, p.err);
                 const uint8_t* vrow = slot_ptr(seq);
 #pragma unroll
@@ -406,6 +462,17 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
                     axpy2_bf16(pb, w.y, oacc[8 * c + 2], oacc[8 * c + 3]);
                     axpy2_bf16(pb, w.z, oacc[8 * c + 4], oacc[8 * c + 5]);
                     axpy2_bf16(pb, w.w, oacc[8 * c + 6], oacc[8 * c + 7]);
+                }
+                if (lerp) {
+                    const uint32_t ph = pack_bf16x2(phi, 0.f);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(vrow + sw128_off(r + 1, c));
+                        axpy2_bf16(ph, w.x, oacc[8 * c + 0], oacc[8 * c + 1]);
+                        axpy2_bf16(ph, w.y, oacc[8 * c + 2], oacc[8 * c + 3]);
+                        axpy2_bf16(ph, w.z, oacc[8 * c + 4], oacc[8 * c + 5]);
+                        axpy2_bf16(ph, w.w, oacc[8 * c + 6], oacc[8 * c + 7]);
+                    }
                 }
                 rg.release_warp(seq, lane);
                 ++seq;
@@ -473,12 +540,16 @@ fwd_tc_kernel(const __grid_constant__ FwdParams p) {
 
 }  // namespace
 
-fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
-                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
+namespace {
+
+template <bool kFrac>
+fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const AttnShape& sh, const OffsetTables& t,
+                          const float (*w)[kMaxOffsets], const char* name, cudaStream_t st) {
     const int64_t slices = sh.slices_per_layer * sh.n_layers;
     const int32_t tiles = (sh.T + kRows - 1) / kRows;
     if (slices > 0x7fffffff || (int64_t)tiles * slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
-    FwdParams P;
+    FwdArgs<kFrac> P;
     // the error-word lookup is a runtime call: it binds the device's primary context to this
     // thread (a fresh thread may have none), which the tensor-map encoding below needs
     P.err = device_error_word();
@@ -488,6 +559,13 @@ fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, v
     for (int m = 0; m < 4; ++m) {
         const int r = make_bf16_rows_map(maps[m], bases[m], slices, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (fwd)");
+    }
+    if constexpr (kFrac) {
+        int r = make_bf16_rows8_map(&P.tm_k8, k, slices, sh.T);
+        if (r == 0) r = make_bf16_rows8_map(&P.tm_v8, v, slices, sh.T);
+        if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (fwd, 8-row box)");
+        for (int l = 0; l < kMaxLayersPerLaunch; ++l)
+            for (int e = 0; e < kMaxOffsets; ++e) P.w[l][e] = w[l][e];
     }
     P.lse = lse;
     P.slices_per_layer = (uint32_t)sh.slices_per_layer;
@@ -504,8 +582,8 @@ fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, v
     static int n_sm[64] = {};
     if (dev < 0 || dev >= 64) return FIBATTN_ERR_UNSUPPORTED;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemAlloc);
+        e = cudaFuncSetAttribute(fwd_tc_kernel<kFrac>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_alloc<kFrac>());
         if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaFuncSetAttribute (fwd)");
         e = cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaDeviceGetAttribute");
@@ -513,10 +591,23 @@ fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, v
     }
     const int64_t grid = (int64_t)P.total_tiles < 2LL * n_sm[dev] ? (int64_t)P.total_tiles : 2LL * n_sm[dev];
     {
-        KernelScope ks("fwd_tc_bf16", st);
-        fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, st>>>(P);
+        KernelScope ks(name, st);
+        fwd_tc_kernel<kFrac><<<(unsigned)grid, kThreads, smem_alloc<kFrac>(), st>>>(P);
     }
-    return launch_status("launch fwd_tc_bf16");
+    return launch_status(name);
+}
+
+}  // namespace
+
+fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
+    return launch_fwd<false>(q, k, v, o, lse, sh, t, nullptr, "fwd_tc_bf16", st);
+}
+
+fibattn_status launch_fwd_frac_tc_bf16(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, const AttnShape& sh, const FracTables& t,
+                                       cudaStream_t st) {
+    return launch_fwd<true>(q, k, v, o, lse, sh, t.c, t.w, "fwd_frac_tc_bf16", st);
 }
 
 }  // namespace fibattn

@@ -20,6 +20,14 @@ struct OffsetTables {
     int32_t off[kMaxLayersPerLaunch][kMaxOffsets];  // ascending, each in [W, T-1]
 };
 
+// Fractional-offset tables of one launch (the learned-alpha variant): for every real distance
+// d = alpha * F kept by the table rule, `c.off` holds ceil(d) (ascending, possibly repeated)
+// and `w` the interpolation weight ceil(d) - d in [0, 1) of the row after i - ceil(d).
+struct FracTables {
+    OffsetTables c;
+    float w[kMaxLayersPerLaunch][kMaxOffsets];
+};
+
 // An exact alpha = num / den of one layer (num, den > 0, already reduced).
 struct Alpha {
     int64_t num, den;
@@ -31,6 +39,14 @@ fibattn_status layer_alpha(const fibattn_schedule* s, int32_t layer, Alpha* out)
 // Host offset table of one layer under an exact alpha (see fibattn_offsets).
 fibattn_status build_table(const fibattn_schedule* s, Alpha a, int32_t W, int32_t T, int32_t* out,
                            int32_t cap, int32_t* n_out);
+
+// Fractional-offset table of one real alpha (see fibattn_frac_offsets).
+fibattn_status build_frac_table(int32_t base, int64_t base_max, float alpha, int32_t W, int32_t T,
+                                int32_t* c_out, float* w_out, int32_t cap, int32_t* n_out);
+
+// Builds FracTables for n launch layers with alphas[0..n).
+fibattn_status build_frac_launch_tables(int32_t base, int64_t base_max, const float* alphas,
+                                        int32_t n, int32_t W, int32_t T, FracTables* t);
 
 // Builds OffsetTables for launch layers [layer0, layer0 + n).
 fibattn_status build_launch_tables(const fibattn_schedule* s, int32_t layer0, int32_t n, int32_t W,
@@ -83,6 +99,13 @@ fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v,
                                     cudaStream_t st);
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
+// Fractional-offset forwards (the learned-alpha variant): fp32 SIMT and bf16 tensor cores.
+fibattn_status launch_fwd_frac_simt_f32(const float* q, const float* k, const float* v, float* o,
+                                        float* lse, const AttnShape& sh, const FracTables& t,
+                                        cudaStream_t st);
+fibattn_status launch_fwd_frac_tc_bf16(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, const AttnShape& sh, const FracTables& t,
+                                       cudaStream_t st);
 // SIMT backward (fp32 path): D into `delta`, then dQ, then dK/dV.
 fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* v, const float* o,
                                    const float* lse, const float* dO, float* dq, float* dk,

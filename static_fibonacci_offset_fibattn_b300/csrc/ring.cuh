@@ -4,7 +4,8 @@
 // (consecutive tiles are consecutive 128-row blocks of one slice, so the CTAs in flight at
 // any moment touch a narrow band of slices and their re-reads stay in L2).
 //
-// All shared-memory operands go through one in-order ring of 16 KB slots: a producer warp
+// All shared-memory operands go through one in-order ring of slots (16 KB: 128 rows of 128
+// bytes, or 17 KB where an item carries 8 extra rows after its tile): a producer warp
 // walks the same per-tile item sequence as the consumers and fills slot (seq % slots) once
 // the previous use of that slot has been released. A FULL barrier expects the producer's
 // arrival with the TMA byte count (and, where a slot carries per-row side data copied by
@@ -58,14 +59,15 @@ struct Ring {
     uint32_t full0;           // shared address of FULL[0]; EMPTY[i] follows the FULL array
     uint32_t slots;
     uint32_t empty_arrivals;  // = the kernel's number of row warps
+    uint32_t slot_bytes = kSlotBytes;  // slot stride, a multiple of 1024
 
     __device__ __forceinline__ uint32_t slot(uint32_t seq) const { return seq % slots; }
-    __device__ __forceinline__ uint32_t addr(uint32_t seq) const { return base + slot(seq) * kSlotBytes; }
+    __device__ __forceinline__ uint32_t addr(uint32_t seq) const { return base + slot(seq) * slot_bytes; }
     __device__ __forceinline__ uint32_t full(uint32_t seq) const { return full0 + 8u * slot(seq); }
     __device__ __forceinline__ uint32_t empty(uint32_t seq) const { return full0 + 8u * (slots + slot(seq)); }
     __device__ __forceinline__ uint32_t parity(uint32_t seq) const { return (seq / slots) & 1u; }
 
-    __device__ __forceinline__ uint32_t addr_at(const Pos& q) const { return base + q.slot * kSlotBytes; }
+    __device__ __forceinline__ uint32_t addr_at(const Pos& q) const { return base + q.slot * slot_bytes; }
     __device__ __forceinline__ uint32_t full_at(const Pos& q) const { return full0 + 8u * q.slot; }
     __device__ __forceinline__ uint32_t empty_at(const Pos& q) const { return full0 + 8u * (slots + q.slot); }
     __device__ __forceinline__ bool acquire_at(const Pos& q, bool& aborted, int32_t* err) const {

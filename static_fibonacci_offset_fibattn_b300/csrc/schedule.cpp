@@ -7,6 +7,11 @@
 //   Metodologia / Controles: the power-of-two base.
 // Alphas are exact rationals; offsets are alpha * F rounded half up with integer
 // arithmetic only, so host and device agree bit for bit.
+// The learned-alpha variant (Metodologia / Arquitetura, "Implementacao": linear
+// interpolation between key/value rows so that the gradient reaches alpha) takes a real
+// float alpha instead: d = alpha * F in double (exact for F < 2^29), kept when
+// W <= d <= T - 1, stored as ceil(d) and the weight ceil(d) - d of the following row.
+#include <math.h>
 #include <stdint.h>
 
 #include "internal.h"
@@ -105,6 +110,63 @@ fibattn_status build_table(const fibattn_schedule* s, Alpha a, int32_t W, int32_
     }
     *n_out = n;
     return n > cap ? FIBATTN_ERR_CAPACITY : FIBATTN_OK;
+}
+
+fibattn_status build_frac_table(int32_t base, int64_t base_max, float alpha, int32_t W, int32_t T,
+                                int32_t* c_out, float* w_out, int32_t cap, int32_t* n_out) {
+    if (W < 1 || T < 1 || cap < 0 || base_max < 0) return FIBATTN_ERR_INVALID_ARG;
+    if (base != FIBATTN_BASE_FIB && base != FIBATTN_BASE_POW2) return FIBATTN_ERR_INVALID_ARG;
+    if (!(alpha > 0.f) || !(alpha <= (float)FIBATTN_RATIO_MAX)) return FIBATTN_ERR_INVALID_ARG;
+    const bool fib = base == FIBATTN_BASE_FIB;
+    const double a = (double)alpha;
+    int32_t n = 0;
+    auto keep = [&](double d) {
+        if (d < (double)W || d > (double)T - 1) return;
+        if (n < cap) {
+            const double c = ceil(d);
+            c_out[n] = (int32_t)c;
+            w_out[n] = (float)(c - d);
+        }
+        ++n;
+    };
+    if (fib) {
+        const int64_t fmax = base_max > 0 ? base_max : 987;
+        for (int64_t f = 1, g = 2; f <= fmax;) {
+            if (a * (double)f > (double)T - 1) break;  // d grows with F: nothing further fits
+            keep(a * (double)f);
+            const int64_t h = f + g;
+            f = g;
+            g = h;
+        }
+    } else {
+        for (int64_t f = 1; a * (double)f <= (double)T - 1 && (base_max <= 0 || f <= base_max);) {
+            keep(a * (double)f);
+            if (f > INT64_MAX / 2) break;
+            f *= 2;
+        }
+    }
+    *n_out = n;
+    return n > cap ? FIBATTN_ERR_CAPACITY : FIBATTN_OK;
+}
+
+fibattn_status build_frac_launch_tables(int32_t base, int64_t base_max, const float* alphas,
+                                        int32_t n, int32_t W, int32_t T, FracTables* t) {
+    if (!alphas || n < 1 || n > kMaxLayersPerLaunch) return FIBATTN_ERR_INVALID_ARG;
+    for (int c = 0; c < kMaxLayersPerLaunch; ++c) {
+        t->c.count[c] = 0;
+        for (int e = 0; e < kMaxOffsets; ++e) {
+            t->c.off[c][e] = -1;
+            t->w[c][e] = 0.f;
+        }
+    }
+    for (int c = 0; c < n; ++c) {
+        int32_t cnt = 0;
+        fibattn_status st = build_frac_table(base, base_max, alphas[c], W, T, t->c.off[c], t->w[c],
+                                             kMaxOffsets, &cnt);
+        if (st != FIBATTN_OK) return st;
+        t->c.count[c] = cnt;
+    }
+    return FIBATTN_OK;
 }
 
 fibattn_status build_launch_tables(const fibattn_schedule* s, int32_t layer0, int32_t n, int32_t W,

@@ -94,6 +94,58 @@ fwd_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
     if (lane == 0) lse[slice * sh.T + i] = m + logf(l);
 }
 
+// Fractional offsets (the learned-alpha variant; Metodologia / Arquitetura, "Implementacao"):
+// each real distance d, held as c = ceil(d) and w = c - d, contributes for i >= c one key and
+// value interpolated between rows i - c and i - c + 1: x~ = (1 - w) x_{i-c} + w x_{i-c+1}.
+template <typename E>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+fwd_frac_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
+                     E* __restrict__ o, float* __restrict__ lse, AttnShape sh,
+                     const __grid_constant__ FracTables tab) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int layer = blockIdx.y;
+    if (row >= rows) return;
+    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int32_t i = (int32_t)(row % sh.T);
+    const int64_t base = slice * sh.T * kD;
+    const float2 qv = Io<E>::ld(q + base + (int64_t)i * kD + 2 * lane);
+
+    float m = -INFINITY, l = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
+    auto visit = [&](float2 kv, float2 vv) {
+        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y) * sh.scale;
+        const float mn = fmaxf(m, s);
+        const float corr = expf(m - mn);  // m = -inf on the first key: corr = 0
+        const float p = expf(s - mn);
+        l = l * corr + p;
+        acc.x = acc.x * corr + p * vv.x;
+        acc.y = acc.y * corr + p * vv.y;
+        m = mn;
+    };
+    auto row_of = [&](const E* x, int32_t j) { return Io<E>::ld(x + base + (int64_t)j * kD + 2 * lane); };
+    const int n_off = tab.c.count[layer];
+    for (int e = n_off - 1; e >= 0; --e) {
+        const int32_t j = i - tab.c.off[layer][e];
+        if (j < 0) continue;
+        const float w = tab.w[layer][e];
+        float2 kv = row_of(k, j), vv = row_of(v, j);
+        if (w != 0.f) {  // j + 1 <= i - W + 1 <= i: inside the sequence
+            const float2 k1 = row_of(k, j + 1), v1 = row_of(v, j + 1);
+            kv = make_float2((1.f - w) * kv.x + w * k1.x, (1.f - w) * kv.y + w * k1.y);
+            vv = make_float2((1.f - w) * vv.x + w * v1.x, (1.f - w) * vv.y + w * v1.y);
+        }
+        visit(kv, vv);
+    }
+    const int32_t j0 = i - sh.W + 1 > 0 ? i - sh.W + 1 : 0;
+    for (int32_t j = j0; j <= i; ++j) visit(row_of(k, j), row_of(v, j));
+
+    const float inv = 1.f / l;
+    Io<E>::st(o + base + (int64_t)i * kD + 2 * lane, make_float2(acc.x * inv, acc.y * inv));
+    if (lane == 0) lse[slice * sh.T + i] = m + logf(l);
+}
+
 // ---------------------------------------------------------------- backward
 // D_i = dO_i . O_i
 template <typename E>
@@ -219,6 +271,18 @@ fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v,
     KernelScope ks("fwd_simt_bf16", st);
     fwd_simt_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(
         (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
+    return launch_status("launch SIMT kernel");
+}
+
+fibattn_status launch_fwd_frac_simt_f32(const float* q, const float* k, const float* v, float* o,
+                                        float* lse, const AttnShape& sh, const FracTables& t,
+                                        cudaStream_t st) {
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    dim3 grid((unsigned)blocks, sh.n_layers);
+    KernelScope ks("fwd_frac_simt_f32", st);
+    fwd_frac_simt_kernel<float><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, o, lse, sh, t);
     return launch_status("launch SIMT kernel");
 }
 

@@ -44,6 +44,10 @@ int make_bf16_rows_map(CUtensorMap* m, const void* base, int64_t slices, int32_t
     return make_map(m, base, slices, T, kTmaBoxRows);
 }
 
+int make_bf16_rows8_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
+    return make_map(m, base, slices, T, 8);
+}
+
 int make_bf16_tile_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
     return make_map(m, base, slices, T, 2 * kTmaBoxRows);
 }
