@@ -30,7 +30,8 @@ import numpy as np
 
 from . import schedule
 from .schedule import (FIB, POW2, FIXED, LINEAR, COPRIME, alpha_for_layer, fibonacci_base,
-                       frac_distances, key_set, layer_table, offset_table, round_half_up)
+                       frac_bases, frac_distances, key_set, layer_table, offset_table,
+                       round_half_up)
 
 _lib = None
 
@@ -55,6 +56,9 @@ def lib():
         L.oracle_fwd_frac.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, ctypes.c_double,
                                       dp, ip, i64, ip, ctypes.c_int]
         L.oracle_fwd_frac.restype = ctypes.c_int
+        L.oracle_bwd_frac.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64,
+                                      ctypes.c_double, dp, ip, i64, ip, ctypes.c_int]
+        L.oracle_bwd_frac.restype = ctypes.c_int
         L.oracle_threads.argtypes = [ctypes.c_int]
         L.oracle_threads.restype = ctypes.c_int
         _lib = L
@@ -139,17 +143,7 @@ def fwd(q, k, v, W: int, tables, scale: float | None = None, n_threads: int = 0)
     return out.reshape(shape), lse.reshape(shape[:-1])
 
 
-def fwd_frac(q, k, v, W: int, dist_tables, scale: float | None = None, n_threads: int = 0):
-    """Forward with fractional offsets in fp64: dist_tables is one list of real distances
-    (schedule.frac_distances) per index of the leading axis, or one list for all slices.
-    Returns (out, lse)."""
-    qs, shape = _as_slices(q)
-    ks, _ = _as_slices(k)
-    vs, _ = _as_slices(v)
-    T, d = shape[-2], shape[-1]
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
-    n_slices = qs.shape[0]
+def _frac_tables(dist_tables, shape, n_slices):
     per_layer = len(dist_tables) > 0 and isinstance(dist_tables[0], (list, tuple, np.ndarray))
     tabs = [list(map(float, t)) for t in dist_tables] if per_layer else [list(map(float, dist_tables))]
     if per_layer and (len(shape) < 3 or len(tabs) != shape[0]):
@@ -161,6 +155,21 @@ def fwd_frac(q, k, v, W: int, dist_tables, scale: float | None = None, n_threads
     for r, t in enumerate(tabs):
         arr[r, :len(t)] = t
         cnt[r] = len(t)
+    return arr, cnt, cap, tos
+
+
+def fwd_frac(q, k, v, W: int, dist_tables, scale: float | None = None, n_threads: int = 0):
+    """Forward with fractional offsets in fp64: dist_tables is one list of real distances
+    (schedule.frac_distances) per index of the leading axis, or one list for all slices.
+    Returns (out, lse)."""
+    qs, shape = _as_slices(q)
+    ks, _ = _as_slices(k)
+    vs, _ = _as_slices(v)
+    T, d = shape[-2], shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    n_slices = qs.shape[0]
+    arr, cnt, cap, tos = _frac_tables(dist_tables, shape, n_slices)
     out = np.zeros_like(qs)
     lse = np.zeros(qs.shape[:-1], dtype=np.float64)
     rc = lib().oracle_fwd_frac(_dptr(qs), _dptr(ks), _dptr(vs), _dptr(out), _dptr(lse), n_slices,
@@ -169,6 +178,33 @@ def fwd_frac(q, k, v, W: int, dist_tables, scale: float | None = None, n_threads
     if rc:
         raise MemoryError("oracle_fwd_frac failed")
     return out.reshape(shape), lse.reshape(shape[:-1])
+
+
+def bwd_frac(q, k, v, dout, W: int, dist_tables, scale: float | None = None, n_threads: int = 0):
+    """Backward with fractional offsets in fp64 (tables as in fwd_frac). Returns
+    (dq, dk, dv, out, lse, dd) where dd[..., t] = dL/dd_t of each slice for the loss
+    L = sum(dout * out); dL/dalpha of a layer is sum over its slices of sum_t f_t dd[..., t]."""
+    qs, shape = _as_slices(q)
+    ks, _ = _as_slices(k)
+    vs, _ = _as_slices(v)
+    gs, _ = _as_slices(dout)
+    T, d = shape[-2], shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    n_slices = qs.shape[0]
+    arr, cnt, cap, tos = _frac_tables(dist_tables, shape, n_slices)
+    dq, dk, dv, out = (np.zeros_like(qs) for _ in range(4))
+    lse = np.zeros(qs.shape[:-1], dtype=np.float64)
+    dd = np.zeros((n_slices, cap), dtype=np.float64)
+    rc = lib().oracle_bwd_frac(_dptr(qs), _dptr(ks), _dptr(vs), _dptr(gs), _dptr(dq), _dptr(dk),
+                               _dptr(dv), _dptr(out), _dptr(lse), _dptr(dd), n_slices, T, d,
+                               int(W), float(scale), _dptr(arr), _iptr(cnt), cap, _iptr(tos),
+                               int(n_threads))
+    if rc:
+        raise MemoryError("oracle_bwd_frac failed")
+    r = lambda a: a.reshape(shape)
+    return (r(dq), r(dk), r(dv), r(out), lse.reshape(shape[:-1]),
+            dd.reshape(tuple(shape[:-2]) + (cap,)))
 
 
 def bwd(q, k, v, dout, W: int, tables, scale: float | None = None, n_threads: int = 0):
@@ -198,4 +234,5 @@ def bwd(q, k, v, dout, W: int, tables, scale: float | None = None, n_threads: in
 
 __all__ = ["schedule", "FIB", "POW2", "FIXED", "LINEAR", "COPRIME", "alpha_for_layer",
            "fibonacci_base", "frac_distances", "key_set", "key_set_c", "layer_table",
-           "offset_table", "round_half_up", "fwd", "fwd_frac", "bwd", "threads", "lib"]
+           "offset_table", "round_half_up", "fwd", "fwd_frac", "bwd", "bwd_frac", "frac_bases",
+           "threads", "lib"]

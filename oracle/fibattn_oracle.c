@@ -29,6 +29,13 @@
  *   lo = floor(p), w = p - lo,  k~ = (1 - w) k[lo] + w k[lo + 1],  v~ likewise
  * (lo + 1 <= i - W + 1 <= i because d_k >= W). Softmax over the window keys and the
  * interpolated keys together, as above.
+ * Its backward is the same softmax gradient with the interpolated rows in place of k_j and
+ * v_j, the interpolation weights carried to the two rows (dk[lo] += (1 - w) g, dk[lo+1] +=
+ * w g, likewise dv), and the derivative with respect to each distance d: p = i - d, so
+ * dk~/dd = k[lo] - k[lo+1] and dv~/dd = v[lo] - v[lo+1] on the segment holding p (at an
+ * integer p that is the segment [p, p+1], the derivative for d decreasing), giving
+ *   dL/dd = sum_i [ dS_i scale q_i.(k[lo] - k[lo+1]) + P_i dO_i.(v[lo] - v[lo+1]) ],
+ * and dL/dalpha = sum_k f_k dL/dd_k (chain rule through d_k = alpha f_k).
  *
  * Layout: every tensor is [n_slices][T][d] row-major float64; lse is [n_slices][T].
  * Slices are independent; OpenMP runs them in parallel when built with -fopenmp.
@@ -178,6 +185,70 @@ static void fwd_frac_slice(const double* q, const double* k, const double* v, do
     }
 }
 
+/* Backward of one slice with fractional offsets: dq, dk, dv and dd[n_dist] = dL/dd per
+ * distance, from the forward's out and lse (computed by fwd_frac_slice, fp64). */
+static void bwd_frac_slice(const double* q, const double* k, const double* v, const double* dout,
+                           const double* out, const double* lse, double* dq, double* dk,
+                           double* dv, double* dd, int64_t T, int64_t d, int64_t W, double scale,
+                           const double* dists, int n_dist, double* kt, double* vt) {
+    memset(dk, 0, sizeof(double) * (size_t)(T * d));
+    memset(dv, 0, sizeof(double) * (size_t)(T * d));
+    for (int t = 0; t < n_dist; ++t) dd[t] = 0.0;
+    for (int64_t i = 0; i < T; ++i) {
+        const double* qi = q + i * d;
+        const double* gi = dout + i * d;
+        double Di = 0.0;
+        for (int64_t c = 0; c < d; ++c) Di += gi[c] * out[i * d + c];
+        for (int64_t c = 0; c < d; ++c) dq[i * d + c] = 0.0;
+        /* window keys: the plain softmax gradient */
+        int64_t lo_w = i - W + 1;
+        if (lo_w < 0) lo_w = 0;
+        for (int64_t j = lo_w; j <= i; ++j) {
+            double sij = 0.0, dpij = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                sij += qi[c] * k[j * d + c];
+                dpij += gi[c] * v[j * d + c];
+            }
+            double pij = exp(scale * sij - lse[i]);
+            double dsij = pij * (dpij - Di);
+            for (int64_t c = 0; c < d; ++c) {
+                dq[i * d + c] += scale * dsij * k[j * d + c];
+                dk[j * d + c] += scale * dsij * qi[c];
+                dv[j * d + c] += pij * gi[c];
+            }
+        }
+        /* interpolated keys */
+        for (int t = 0; t < n_dist; ++t) {
+            double pos = (double)i - dists[t];
+            if (pos < 0.0) continue;
+            int64_t lo = (int64_t)floor(pos);
+            double w = pos - (double)lo;
+            int64_t hi = lo + 1; /* <= i - W + 1 <= i */
+            for (int64_t c = 0; c < d; ++c) {
+                kt[c] = (1.0 - w) * k[lo * d + c] + w * k[hi * d + c];
+                vt[c] = (1.0 - w) * v[lo * d + c] + w * v[hi * d + c];
+            }
+            double s = 0.0, dp = 0.0, sdiff = 0.0, vdiff = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                s += qi[c] * kt[c];
+                dp += gi[c] * vt[c];
+                sdiff += qi[c] * (k[lo * d + c] - k[hi * d + c]);
+                vdiff += gi[c] * (v[lo * d + c] - v[hi * d + c]);
+            }
+            double P = exp(scale * s - lse[i]);
+            double dS = P * (dp - Di);
+            for (int64_t c = 0; c < d; ++c) {
+                dq[i * d + c] += scale * dS * kt[c];
+                dk[lo * d + c] += (1.0 - w) * scale * dS * qi[c];
+                dk[hi * d + c] += w * scale * dS * qi[c];
+                dv[lo * d + c] += (1.0 - w) * P * gi[c];
+                dv[hi * d + c] += w * P * gi[c];
+            }
+            dd[t] += dS * scale * sdiff + P * vdiff;
+        }
+    }
+}
+
 static int set_threads(int n_threads) {
 #ifdef _OPENMP
     if (n_threads > 0) omp_set_num_threads(n_threads);
@@ -279,6 +350,44 @@ int oracle_fwd_frac(const double* q, const double* k, const double* v, double* o
                 fwd_frac_slice(q + sl * T * d, k + sl * T * d, v + sl * T * d, out + sl * T * d,
                                lse + sl * T, T, d, W, scale, dists + (int64_t)t * cap, counts[t],
                                s, keyv, valv);
+            }
+        }
+        free(s);
+        free(keyv);
+        free(valv);
+    }
+    return err;
+}
+
+/* Backward with fractional offsets. out/lse are written (the forward, fp64); dd is
+ * [n_slices][cap]: dL/dd of each slice's distances. */
+int oracle_bwd_frac(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv, double* out, double* lse, double* dd,
+                    int64_t n_slices, int64_t T, int64_t d, int64_t W, double scale,
+                    const double* dists, const int32_t* counts, int64_t cap,
+                    const int32_t* table_of_slice, int n_threads) {
+    set_threads(n_threads);
+    int err = 0;
+#pragma omp parallel
+    {
+        int64_t nk = T + cap + 1;
+        double* s = (double*)malloc(sizeof(double) * (size_t)nk);
+        double* keyv = (double*)malloc(sizeof(double) * (size_t)(nk * d));
+        double* valv = (double*)malloc(sizeof(double) * (size_t)(nk * d));
+        if (!s || !keyv || !valv) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic)
+            for (int64_t sl = 0; sl < n_slices; ++sl) {
+                int32_t t = table_of_slice[sl];
+                const double* ds = dists + (int64_t)t * cap;
+                const int64_t o3 = sl * T * d;
+                fwd_frac_slice(q + o3, k + o3, v + o3, out + o3, lse + sl * T, T, d, W, scale, ds,
+                               counts[t], s, keyv, valv);
+                bwd_frac_slice(q + o3, k + o3, v + o3, dout + o3, out + o3, lse + sl * T, dq + o3,
+                               dk + o3, dv + o3, dd + sl * cap, T, d, W, scale, ds, counts[t],
+                               keyv, valv);
             }
         }
         free(s);

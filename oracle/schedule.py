@@ -131,6 +131,22 @@ def key_set(i: int, W: int, table) -> list:
     return sorted(ks)
 
 
+def frac_bases(alpha: float, base: str, W: int, T: int, base_max: int = 0):
+    """The base values F behind frac_distances, in the same order."""
+    if not alpha > 0:
+        raise ValueError("alpha must be > 0")
+    if base == FIB:
+        fs = fibonacci_base(base_max)
+    elif base == POW2:
+        fs, f = [], 1
+        while float(alpha) * f <= T - 1 and (base_max <= 0 or f <= base_max):
+            fs.append(f)
+            f *= 2
+    else:
+        raise ValueError(f"unknown base {base!r}")
+    return [f for f in fs if W <= float(alpha) * f <= T - 1]
+
+
 def frac_distances(alpha: float, base: str, W: int, T: int, base_max: int = 0):
     """Real offset distances d_k = alpha * F of a fractional ("learned") alpha: the pages'
     learned variant interpolates keys between rows instead of rounding (Metodologia /

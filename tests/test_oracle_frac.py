@@ -173,3 +173,113 @@ def test_per_layer_distance_lists():
         o1, l1 = oracle.fwd_frac(q[l], k[l], v[l], W, tabs[l])
         np.testing.assert_array_equal(out[l], o1)
         np.testing.assert_array_equal(lse[l], l1)
+
+
+# ------------------------------------------------------------------ backward
+
+
+def torch_frac_loss(q, k, v, dout, W, alpha, bases, scale):
+    """Sum(dout * out) of the vectorised statement, with alpha a leaf tensor: the position
+    i - alpha F is split into a detached floor and a weight that carries the gradient."""
+    T = q.shape[-2]
+    i = torch.arange(T, dtype=torch.float64)
+    dist = i[:, None] - i[None, :]
+    win = (dist >= 0) & (dist < W)
+    s_parts = [(q @ k.transpose(-1, -2) * scale).masked_fill(~win, -math.inf)]
+    v_parts = []
+    for f in bases:
+        pos = i - alpha * f
+        ok = pos.detach() >= 0
+        lo = torch.floor(pos.detach()).clamp(min=0)
+        w = torch.where(ok, pos - lo, torch.zeros_like(pos))
+        lo = lo.long()
+        hi = (lo + 1).clamp(max=T - 1)
+        kt = (1 - w)[:, None] * k[..., lo, :] + w[:, None] * k[..., hi, :]
+        vt = (1 - w)[:, None] * v[..., lo, :] + w[:, None] * v[..., hi, :]
+        s = (q * kt).sum(-1) * scale
+        s_parts.append(s.masked_fill(~ok, -math.inf)[..., None])
+        v_parts.append(vt)
+    s_all = torch.cat(s_parts, dim=-1)
+    p = torch.softmax(s_all, dim=-1)
+    out = p[..., :T] @ v
+    for t, vt in enumerate(v_parts):
+        out = out + p[..., T + t, None] * vt
+    return (dout * out).sum()
+
+
+@pytest.mark.parametrize("alpha,base,W,T,d", [(1.37, S.FIB, 16, 256, 16), (0.61, S.FIB, 3, 130, 8),
+                                              (2.718, S.POW2, 5, 300, 8), (1.0, S.FIB, 8, 200, 8)])
+def test_bwd_frac_matches_autograd(alpha, base, W, T, d):
+    a = f32(alpha)
+    dists = oracle.frac_distances(a, base, W, T)
+    bases = oracle.frac_bases(a, base, W, T)
+    assert [a * f for f in bases] == dists
+    q, k, v, g = (rnd((2, T, d), s) for s in (21, 22, 23, 24))
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv, out, lse, dd = oracle.bwd_frac(q, k, v, g, W, dists, scale)
+    t = [torch.tensor(x, requires_grad=True) for x in (q, k, v)]
+    at = torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    loss = torch_frac_loss(*t, torch.from_numpy(g), W, at, bases, scale)
+    loss.backward()
+    np.testing.assert_allclose(dq, t[0].grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, t[1].grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, t[2].grad.numpy(), rtol=0, atol=1e-11)
+    dalpha = float((dd[:, : len(bases)] * np.array(bases, dtype=np.float64)).sum())
+    assert abs(dalpha - at.grad.item()) <= 1e-9 * max(1.0, abs(dalpha))
+
+
+def test_bwd_frac_central_differences():
+    T, d, W, alpha = 150, 8, 6, f32(1.37)
+    q, k, v, g = (rnd((T, d), s) for s in (31, 32, 33, 34))
+    dists = oracle.frac_distances(alpha, S.FIB, W, T)
+    bases = oracle.frac_bases(alpha, S.FIB, W, T)
+    dq, dk, dv, _, _, dd = oracle.bwd_frac(q, k, v, g, W, dists)
+    loss = lambda q_, k_, v_, ds: float((g * oracle.fwd_frac(q_, k_, v_, W, ds)[0]).sum())
+    h = 1e-6
+    # alpha: no distance is within h * F of an integer, so the segment stays the same
+    assert all(min(x - math.floor(x), math.ceil(x) - x) > 1e-3 for x in dists)
+    up = [(alpha + h) * f for f in bases]
+    dn = [(alpha - h) * f for f in bases]
+    fd = (loss(q, k, v, up) - loss(q, k, v, dn)) / (2 * h)
+    dalpha = float((dd[: len(bases)] * np.array(bases, dtype=np.float64)).sum())
+    assert abs(fd - dalpha) <= 1e-6 * max(1.0, abs(dalpha))
+    # each distance on its own
+    for t in range(len(dists)):
+        up = list(dists); up[t] += h
+        dn = list(dists); dn[t] -= h
+        fd = (loss(q, k, v, up) - loss(q, k, v, dn)) / (2 * h)
+        assert abs(fd - dd[t]) <= 1e-6 * max(1.0, abs(dd[t])), t
+    # a few entries of q, k, v, among them rows that only an interpolated key reaches
+    lo = int(math.floor(100 - dists[2]))
+    for name, arr, grad, idx in (("q", q, dq, (100, 3)), ("k", k, dk, (lo, 5)),
+                                 ("k", k, dk, (lo + 1, 0)), ("v", v, dv, (lo, 2)),
+                                 ("v", v, dv, (lo + 1, 7)), ("k", k, dk, (140, 1))):
+        a1, a2 = arr.copy(), arr.copy()
+        a1[idx] += h
+        a2[idx] -= h
+        args1 = [a1 if n == name else x for n, x in (("q", q), ("k", k), ("v", v))]
+        args2 = [a2 if n == name else x for n, x in (("q", q), ("k", k), ("v", v))]
+        fd = (loss(*args1, dists) - loss(*args2, dists)) / (2 * h)
+        assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(grad[idx])), (name, idx)
+
+
+@pytest.mark.parametrize("alpha,base", [(1.0, S.FIB), (2.0, S.POW2)])
+def test_bwd_frac_integer_alpha_reduces_to_static(alpha, base):
+    T, d, W = 220, 16, 10
+    q, k, v, g = (rnd((2, T, d), s) for s in (41, 42, 43, 44))
+    dists = oracle.frac_distances(alpha, base, W, T)
+    dq, dk, dv, out, lse, _ = oracle.bwd_frac(q, k, v, g, W, dists)
+    rq, rk, rv, ro, rl = oracle.bwd(q, k, v, g, W, S.offset_table(base, Fraction(alpha), W, T))
+    for a, b in ((dq, rq), (dk, rk), (dv, rv), (out, ro), (lse, rl)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_bwd_frac_gradient_sums():
+    # every query's probabilities sum to 1 and the interpolation weights sum to 1, so
+    # sum_j dv_j = sum_i dO_i; sum_k dS_ik = 0 for every query, so sum_j dk_j = 0.
+    T, d, W = 300, 8, 5
+    q, k, v, g = (rnd((3, T, d), s) for s in (51, 52, 53, 54))
+    dists = oracle.frac_distances(f32(0.83), S.FIB, W, T)
+    _, dk, dv, _, _, _ = oracle.bwd_frac(q, k, v, g, W, dists)
+    np.testing.assert_allclose(dv.sum(axis=1), g.sum(axis=1), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, rtol=0, atol=1e-10)
