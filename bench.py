@@ -6,16 +6,17 @@ backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
 (B=8, H=8, T=1024, d=64), W=64, coprime reassignment (l -> 5l mod 16) of the linear
 stagger alpha 0.5 -> 2.0, bf16, forward + backward.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f|c5f]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
 (weak scaling: the (layer, batch, head) slices are independent, no collective on the
 data path); value = all ranks' query tokens / max-over-ranks time.
 
-c3f is the fractional-offset (learned-alpha) forward on the c3 shape; its line adds
-"static_counterpart", the static forward of c3 (same shape and alpha range) timed in the
-same process, and their latency ratio.
+c3f / c5f are the fractional-offset (learned-alpha) forward / training step (with the
+gradient of every layer's alpha) on the c3 / c5 shapes; their lines add
+"static_counterpart", the static c3 / c5 step (same shape and alpha range) timed in the
+same process, and the latency ratio.
 """
 from __future__ import annotations
 
@@ -54,11 +55,18 @@ ALGO_BYTES = {
     "bwd_dkdv_simt": 4 * 256 + 8 + 2 * 256,     # fp32: q, k, v, dO, lse, D in; dk, dv out
     "bwd_dq_tc": 5 * 128 + 4 + 128,             # q, k, v, o, dO, lse in; dq out
     "bwd_dkdv_tc": 4 * 128 + 4 + 2 * 128,       # q, k, v, dO, lse in; dk, dv out
+    "bwd_dq_frac_tc": 5 * 128 + 4 + 128 + 4,    # as bwd_dq_tc, plus the dalpha partial out
+    "bwd_dkdv_frac_tc": 4 * 128 + 4 + 2 * 128,
+    "bwd_dq_frac_simt": 4 * 256 + 8 + 256 + 4,
+    "bwd_dkdv_frac_simt": 4 * 256 + 8 + 2 * 256,
+    "dalpha_reduce": 4,                         # the dalpha partials in
 }
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
     "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu",
+    "bwd_dq_frac_tc": "bwd_tc.cu", "bwd_dkdv_frac_tc": "bwd_tc.cu",
+    "bwd_dq_frac_simt": "simt.cu", "bwd_dkdv_frac_simt": "simt.cu", "dalpha_reduce": "simt.cu",
     "bwd_delta_simt": "simt.cu", "bwd_dq_simt": "simt.cu", "bwd_dkdv_simt": "simt.cu",
     "bwd_dq_tc": "bwd_tc.cu", "bwd_dkdv_tc": "bwd_tc.cu",
 }
@@ -69,7 +77,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="c5", choices=["c5", "c4", "c2", "c3", "c3p", "c3f"])
+    ap.add_argument("--workload", default="c5",
+                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -217,8 +226,10 @@ def run_ours(a, spec, world, rank, local):
     lse = torch.empty(d_in["q"].shape[:-1], dtype=torch.float32, device=dev)
     if train:
         dq, dk, dv = (torch.empty_like(d_in["q"]) for _ in range(3))
-        ws = torch.empty(max(1, fa.bwd_workspace_size(d_in["q"], W, sched)), dtype=torch.uint8,
-                         device=dev)
+        need = (fa.bwd_frac_workspace_size(d_in["q"], W, alphas, spec["base"]) if frac
+                else fa.bwd_workspace_size(d_in["q"], W, sched))
+        ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
+        dalpha = torch.empty(spec["Lc"], dtype=torch.float32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -226,8 +237,11 @@ def run_ours(a, spec, world, rank, local):
     def step(x):
         if frac:
             fa.fwd_frac(x["q"], x["k"], x["v"], W, alphas, spec["base"], out=o, lse=lse)
-        else:
-            fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
+            if train:
+                fa.bwd_frac(x["q"], x["k"], x["v"], o, lse, x["dO"], W, alphas, spec["base"],
+                            dq=dq, dk=dk, dv=dv, dalpha=dalpha, workspace=ws)
+            return
+        fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
         if train:
             fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched, dq=dq, dk=dk, dv=dv,
                    workspace=ws)
@@ -307,21 +321,31 @@ def run_ours(a, spec, world, rank, local):
     if not a.no_e2e:
         e2e = run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas)
 
-    # ---- fractional workload: the static forward of the same shape, timed the same way
+    # ---- fractional workload: the static step of the same shape, timed the same way
     counterpart = None
     if frac:
-        cname = "c3"
+        cname = "c5" if train else "c3"
         cspec = fi.WORKLOADS[cname]
         csched = fa.Schedule(**cspec["sched"])
         cin = {n: t.to(dev) for n, t in fi.workload_inputs(cname).items()}
-        for _ in range(a.warmup):
+        if train:
+            cws = torch.empty(max(1, fa.bwd_workspace_size(cin["q"], cspec["W"], csched)),
+                              dtype=torch.uint8, device=dev)
+
+        def cstep():
             fa.fwd(cin["q"], cin["k"], cin["v"], cspec["W"], csched, out=o, lse=lse)
+            if train:
+                fa.bwd(cin["q"], cin["k"], cin["v"], o, lse, cin["dO"], cspec["W"], csched,
+                       dq=dq, dk=dk, dv=dv, workspace=cws)
+
+        for _ in range(a.warmup):
+            cstep()
             flush.fill_(1.0)
         cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(a.steps)]
         for s, e in cev:
             s.record(stream)
-            fa.fwd(cin["q"], cin["k"], cin["v"], cspec["W"], csched, out=o, lse=lse)
+            cstep()
             e.record(stream)
             flush.fill_(1.0)
         torch.cuda.synchronize(dev)
@@ -367,8 +391,10 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None):
     shapes = {"o": inp["q"].shape, "lse": inp["q"].shape[:-1]}
     if train:
         shapes.update(dq=inp["q"].shape, dk=inp["q"].shape, dv=inp["q"].shape)
+        if alphas is not None:
+            shapes["dalpha"] = (spec["Lc"],)
     for n, shp in shapes.items():
-        dt = torch.float32 if n == "lse" else inp["q"].dtype
+        dt = torch.float32 if n in ("lse", "dalpha") else inp["q"].dtype
         outs_host[n] = torch.empty(shp, dtype=dt).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
@@ -380,7 +406,11 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None):
         else:
             o, lse = fa.fwd(x["q"], x["k"], x["v"], W, sched)
         res = {"o": o, "lse": lse}
-        if train:
+        if train and alphas is not None:
+            dq, dk, dv, da = fa.bwd_frac(x["q"], x["k"], x["v"], o, lse, x["dO"], W, alphas,
+                                         spec["base"])
+            res.update(dq=dq, dk=dk, dv=dv, dalpha=da)
+        elif train:
             dq, dk, dv = fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched)
             res.update(dq=dq, dk=dk, dv=dv)
         for n, t in res.items():
@@ -442,7 +472,10 @@ def oracle_sample(spec, n_slices, n_threads=0):
         g = lambda n: np.stack([f64(inp[n][li, b, h]) for b, h in picks])
         if alphas is not None:
             dists = oracle.frac_distances(alphas[l], spec["base"], W, T)
-            oracle.fwd_frac(g("q"), g("k"), g("v"), W, dists, None, n_threads)
+            if "bwd" in spec["passes"]:
+                oracle.bwd_frac(g("q"), g("k"), g("v"), g("dO"), W, dists, None, n_threads)
+            else:
+                oracle.fwd_frac(g("q"), g("k"), g("v"), W, dists, None, n_threads)
             done += len(picks) * T
             continue
         tab = oracle.layer_table(sc["base"], sc["kind"], l, sc["n_layers"], W, T,
@@ -456,15 +489,14 @@ def oracle_sample(spec, n_slices, n_threads=0):
 
 
 def calibrate_slices(spec, target_s):
-    """Slices of oracle work that take about target_s seconds on this host. The probe runs
-    two slices per OpenMP thread, so that its per-slice time includes the parallel speed-up
-    the full sample gets."""
+    """Slices of oracle work that take about target_s seconds on this host. The sample is
+    spread over the workload's layers and each layer's slices run in parallel, so the probe
+    gives every layer two slices per OpenMP thread; its rate is then scaled to the target."""
     import oracle
 
-    n0 = max(4, 2 * oracle.threads(0))
+    n0 = max(4, 2 * oracle.threads(0) * spec["Lc"])
     sec, toks, _ = oracle_sample(spec, n0)
-    per_slice = sec / n0
-    return max(1, int(target_s / max(per_slice, 1e-6)))
+    return max(1, int(target_s * n0 / max(sec, 1e-6)))
 
 
 def run_reference(a, spec, world, rank):

@@ -83,6 +83,10 @@ WORKLOADS = {
                 dtype="bf16", Lc=16, B=8, H=8, T=1024, d=64, W=64, seed="per_layer:2",
                 scale=0.125, names=("q", "k", "v"), passes=("fwd",), base="fib",
                 alphas=dict(lo=0.5, hi=2.0, seed=7)),
+    "c5f": dict(desc="training step fwd+bwd (with dL/dalpha), 16 layers, fractional "
+                     "(learned-style) alphas in [0.5, 2.0], bf16", dtype="bf16", Lc=16, B=8, H=8,
+                T=1024, d=64, W=64, seed=4, scale=0.125, names=("q", "k", "v", "dO"),
+                passes=("fwd", "bwd"), base="fib", alphas=dict(lo=0.5, hi=2.0, seed=7)),
 }
 
 

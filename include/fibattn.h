@@ -163,6 +163,45 @@ FIBATTN_API fibattn_status fibattn_fwd_frac(const void* q, const void* k, const 
                                             int32_t n_layers_call, void* cuda_stream);
 
 /*
+ * Workspace of fibattn_bwd_frac for one call, in bytes: the static backward's layout
+ * (fibattn_bwd_workspace_size, with n_max = the largest fractional table of the call's
+ * layers) followed, 256-byte aligned, by the per-query dalpha partials [Lc][B][H][T] float32.
+ * Errors as fibattn_fwd_frac.
+ */
+FIBATTN_API fibattn_status fibattn_bwd_frac_workspace_size(int32_t B, int32_t H, int32_t T,
+                                                           int32_t d, int32_t dtype, int32_t W,
+                                                           int32_t base, int64_t base_max,
+                                                           const float* alphas,
+                                                           int32_t n_layers_call, uint64_t* bytes);
+
+/*
+ * Backward of fibattn_fwd_frac (same passage): the gradient reaches alpha through the
+ * interpolation weights. With k~ = (1 - w) k[lo] + w k[lo + 1] (lo = i - ceil(d)), v~ likewise:
+ *   P = exp(scale q_i.k~ - lse_i),  dS = P (dO_i.v~ - D_i),
+ *   dq_i += scale dS k~,  dk[lo] += (1 - w) scale dS q_i,  dk[lo + 1] += w scale dS q_i,
+ *   dv[lo] += (1 - w) P dO_i,  dv[lo + 1] += w P dO_i,
+ *   dL/dd = sum_i dS scale q_i.(k[lo] - k[lo + 1]) + P dO_i.(v[lo] - v[lo + 1])
+ *   (the derivative on the segment [lo, lo + 1]: for an integer d, that for d decreasing),
+ *   dalpha[c] = sum_k F_k dL/dd_k over the distances of call-layer c, for the loss whose
+ *   gradient with respect to o is dO.
+ *   dq, dk, dv : written as in fibattn_bwd.
+ *   dalpha     : float32 device [n_layers_call], written (4-byte aligned).
+ *   workspace  : 256-byte aligned, at least fibattn_bwd_frac_workspace_size() bytes.
+ *   Other arguments as fibattn_fwd_frac / fibattn_bwd. The per-layer sums run in a fixed
+ *   order (deterministic). bf16 runs the tcgen05 backward kernels in their fractional mode;
+ *   f32 runs SIMT kernels.
+ * Errors as fibattn_fwd_frac, plus INVALID_ARG when workspace_bytes is too small.
+ */
+FIBATTN_API fibattn_status fibattn_bwd_frac(const void* q, const void* k, const void* v,
+                                            const void* o, const float* lse, const void* dO,
+                                            void* dq, void* dk, void* dv, float* dalpha,
+                                            void* workspace, uint64_t workspace_bytes, int32_t B,
+                                            int32_t H, int32_t T, int32_t d, int32_t dtype,
+                                            int32_t W, float scale, int32_t base,
+                                            int64_t base_max, const float* alphas,
+                                            int32_t n_layers_call, void* cuda_stream);
+
+/*
  * Workspace the backward needs for one call, in bytes (write it to *bytes). f32 calls:
  *   D [Lc][B][H][T] float32 (D_i = dO_i . o_i). bf16 calls, with rows padded to
  *   T_pad = T rounded up to a multiple of 4: D and lse * log2(e), each [Lc][B][H][T_pad]

@@ -23,7 +23,8 @@ import torch
 __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd",
            "keyset_debug", "poll_device_error", "status_string", "lib", "library_path",
            "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
-           "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac"]
+           "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac", "bwd_frac",
+           "bwd_frac_workspace_size", "FibFracAttention"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
@@ -106,6 +107,11 @@ def lib():
                                            ctypes.POINTER(f32), i32, ctypes.POINTER(i32)]
         L.fibattn_fwd_frac.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                        i64, ctypes.POINTER(f32), i32, vp]
+        L.fibattn_bwd_frac_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i64,
+                                                      ctypes.POINTER(f32), i32, ctypes.POINTER(u64)]
+        L.fibattn_bwd_frac.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32,
+                                       i32, i32, i32, i32, f32, i32, i64, ctypes.POINTER(f32), i32,
+                                       vp]
         L.fibattn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, sp, i32, i32,
                                                  ctypes.POINTER(u64)]
         L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32, i32,
@@ -129,7 +135,8 @@ def lib():
         for name in ("fibattn_offsets", "fibattn_offsets_device", "fibattn_fwd", "fibattn_bwd",
                      "fibattn_bwd_workspace_size",
                      "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error",
-                     "fibattn_frac_offsets", "fibattn_fwd_frac"):
+                     "fibattn_frac_offsets", "fibattn_fwd_frac", "fibattn_bwd_frac",
+                     "fibattn_bwd_frac_workspace_size"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -238,18 +245,64 @@ def fwd_frac(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, alphas: 
     """Forward with fractional offsets (learned alphas, one float per call-layer, linear
     interpolation between key/value rows); returns (o, lse)."""
     Lc, B, H, T, d = _shape(q)
-    if len(alphas) != Lc:
-        raise ValueError("need one alpha per layer of the call")
+    a = _alphas_c(alphas, Lc)
     o = torch.empty_like(q) if out is None else out
     _check_tensors(q, k, v, o)
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-    a = (ctypes.c_float * Lc)(*[float(x) for x in alphas])
     st = lib().fibattn_fwd_frac(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, d,
                                 _DTYPES[q.dtype], W, float(scale or 0.0), _BASES[base],
                                 int(base_max), a, Lc, _stream(q))
     _check(st, "fibattn_fwd_frac")
     return o, lse
+
+
+def _alphas_c(alphas, Lc):
+    if len(alphas) != Lc:
+        raise ValueError("need one alpha per layer of the call")
+    return (ctypes.c_float * Lc)(*[float(x) for x in alphas])
+
+
+def bwd_frac_workspace_size(q: torch.Tensor, W: int, alphas: Sequence[float], base: str = "fib",
+                            base_max: int = 0) -> int:
+    """Bytes of device workspace bwd_frac() needs for q's shape and dtype."""
+    Lc, B, H, T, d = _shape(q)
+    if q.dtype not in _DTYPES:
+        raise ValueError("dtype must be float32 or bfloat16")
+    n = ctypes.c_uint64(0)
+    _check(lib().fibattn_bwd_frac_workspace_size(B, H, T, d, _DTYPES[q.dtype], W, _BASES[base],
+                                                 int(base_max), _alphas_c(alphas, Lc), Lc,
+                                                 ctypes.byref(n)),
+           "fibattn_bwd_frac_workspace_size")
+    return int(n.value)
+
+
+def bwd_frac(q, k, v, o, lse, dO, W: int, alphas: Sequence[float], base: str = "fib",
+             base_max: int = 0, scale: Optional[float] = None, dq=None, dk=None, dv=None,
+             dalpha=None, workspace=None):
+    """Backward of fwd_frac; returns (dq, dk, dv, dalpha) with dalpha a float32 [Lc] tensor
+    on q's device (the gradient of each layer's alpha)."""
+    Lc, B, H, T, d = _shape(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _check_tensors(q, k, v, o, dO, dq, dk, dv)
+    if dalpha is None:
+        dalpha = torch.empty(Lc, dtype=torch.float32, device=q.device)
+    if dalpha.device != q.device or dalpha.dtype != torch.float32 or dalpha.numel() != Lc:
+        raise ValueError("dalpha must be a float32 [Lc] tensor on q's device")
+    need = bwd_frac_workspace_size(q, W, alphas, base, base_max)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on q's device")
+    st = lib().fibattn_bwd_frac(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), B, H, T, d,
+                                _DTYPES[q.dtype], W, float(scale or 0.0), _BASES[base],
+                                int(base_max), _alphas_c(alphas, Lc), Lc, _stream(q))
+    _check(st, "fibattn_bwd_frac")
+    return dq, dk, dv, dalpha
 
 
 def bwd_workspace_size(q: torch.Tensor, W: int, sched: Schedule, layer0: int = 0) -> int:
@@ -345,3 +398,26 @@ class FibSparseAttention(torch.autograd.Function):
         W, sched, layer0, scale = ctx.cfg
         dq, dk, dv = bwd(q, k, v, o, lse, dO.contiguous(), W, sched, layer0, scale)
         return dq, dk, dv, None, None, None, None
+
+
+class FibFracAttention(torch.autograd.Function):
+    """autograd wrapper of the fractional-offset (learned-alpha) attention: alpha is a
+    float32 tensor [Lc] (on any device; read on the host at every call) and receives its
+    gradient from the library's backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, alpha, W: int, base: str = "fib", base_max: int = 0, scale=None):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        alphas = [float(x) for x in alpha.detach().to("cpu", torch.float32).reshape(-1)]
+        o, lse = fwd_frac(q, k, v, W, alphas, base, base_max, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.cfg = (W, alphas, base, base_max, scale, alpha.shape, alpha.device, alpha.dtype)
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, o, lse = ctx.saved_tensors
+        W, alphas, base, base_max, scale, ashape, adev, adtype = ctx.cfg
+        dq, dk, dv, da = bwd_frac(q, k, v, o, lse, dO.contiguous(), W, alphas, base, base_max,
+                                  scale)
+        return dq, dk, dv, da.to(adev, adtype).reshape(ashape), None, None, None, None

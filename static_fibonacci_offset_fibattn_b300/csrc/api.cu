@@ -44,26 +44,43 @@ size_t elt_size(int32_t dtype) { return dtype == FIBATTN_F32 ? 4 : 2; }
 // T_pad = T rounded up to 4 (16-byte rows for bulk copies): D [rows_pad], lse*log2(e)
 // [rows_pad], then the (P, dS) pairs [slices][n_max][T_pad]; each array starts 256-aligned.
 struct BwdWorkspace {
-    uint64_t lse2_offset;  // bytes
-    uint64_t pds_offset;   // bytes
-    uint64_t total;        // bytes
-    int32_t n_max;         // table entries per layer slot of the pairs array
+    uint64_t lse2_offset;    // bytes
+    uint64_t pds_offset;     // bytes
+    uint64_t galpha_offset;  // bytes (fractional backward only)
+    uint64_t total;          // bytes
+    int32_t n_max;           // table entries per layer slot of the pairs array
     int32_t T_pad;
 };
 
 uint64_t align256(uint64_t x) { return (x + 255) & ~(uint64_t)255; }
 
-// Callers have validated the arguments (check_common), so every table builds.
-BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t dtype, int32_t W,
-                           const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
+// The layout for a given n_max; `frac` appends the per-query dalpha partials [rows].
+BwdWorkspace workspace_layout(int32_t B, int32_t H, int32_t T, int32_t dtype, int32_t n_layers_call,
+                              int32_t n_max, bool frac) {
     BwdWorkspace ws;
+    const uint64_t rows = (uint64_t)n_layers_call * B * H * T;
     if (dtype != FIBATTN_BF16) {
         ws.lse2_offset = ws.pds_offset = 0;
-        ws.total = (uint64_t)n_layers_call * B * H * T * 4;
+        ws.galpha_offset = align256(rows * 4);
+        ws.total = frac ? ws.galpha_offset + rows * 4 : rows * 4;
         ws.n_max = 0;
         ws.T_pad = T;
         return ws;
     }
+    ws.T_pad = (T + 3) & ~3;
+    const uint64_t rows_pad = (uint64_t)n_layers_call * B * H * ws.T_pad;
+    ws.n_max = n_max;
+    ws.lse2_offset = align256(rows_pad * 4);
+    ws.pds_offset = ws.lse2_offset + align256(rows_pad * 4);
+    ws.galpha_offset = align256(ws.pds_offset + rows_pad * (uint64_t)n_max * 4);
+    ws.total = frac ? ws.galpha_offset + rows * 4 : ws.pds_offset + rows_pad * (uint64_t)n_max * 4;
+    return ws;
+}
+
+// Callers have validated the arguments (check_common), so every table builds.
+BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t dtype, int32_t W,
+                           const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
+    if (dtype != FIBATTN_BF16) return workspace_layout(B, H, T, dtype, n_layers_call, 0, false);
     int32_t n_max = 0;
     for (int32_t c = 0; c < n_layers_call; ++c) {
         Alpha a;
@@ -72,13 +89,32 @@ BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t dtype, int32
             build_table(sched, a, W, T, nullptr, 0, &n) != FIBATTN_ERR_INVALID_ARG)
             n_max = n > n_max ? n : n_max;
     }
-    ws.T_pad = (T + 3) & ~3;
-    const uint64_t rows_pad = (uint64_t)n_layers_call * B * H * ws.T_pad;
-    ws.n_max = n_max;
-    ws.lse2_offset = align256(rows_pad * 4);
-    ws.pds_offset = ws.lse2_offset + align256(rows_pad * 4);
-    ws.total = ws.pds_offset + rows_pad * (uint64_t)n_max * 4;
-    return ws;
+    return workspace_layout(B, H, T, dtype, n_layers_call, n_max, false);
+}
+
+// Checks shared by the fractional-offset entry points (every layer's table validated).
+fibattn_status check_frac(int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                          int32_t base, int64_t base_max, const float* alphas,
+                          int32_t n_layers_call, int32_t* n_max) {
+    if (!alphas) return FIBATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 1 || W < 1 || n_layers_call < 1 || n_layers_call > FIBATTN_LAYERS_MAX)
+        return FIBATTN_ERR_INVALID_ARG;
+    if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
+    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    const int64_t per_layer = (int64_t)B * H * T;
+    if (per_layer > ((int64_t)1 << 34) || per_layer * n_layers_call > ((int64_t)1 << 40))
+        return FIBATTN_ERR_INVALID_ARG;
+    int32_t m = 0;
+    for (int32_t c = 0; c < n_layers_call; ++c) {
+        int32_t n = 0;
+        fibattn_status st =
+            build_frac_table(base, base_max, alphas[c], W, T, nullptr, nullptr, nullptr, 0, &n);
+        if (st == FIBATTN_ERR_INVALID_ARG) return st;
+        if (n > kMaxOffsets) return FIBATTN_ERR_CAPACITY;
+        m = n > m ? n : m;
+    }
+    if (n_max) *n_max = m;
+    return FIBATTN_OK;
 }
 
 }  // namespace
@@ -177,7 +213,7 @@ fibattn_status fibattn_frac_offsets(float alpha, int32_t base, int64_t base_max,
                                     int32_t T, int32_t* ceil_out, float* w_out, int32_t cap,
                                     int32_t* n_out) {
     if (!n_out || cap < 0 || (cap > 0 && (!ceil_out || !w_out))) return FIBATTN_ERR_INVALID_ARG;
-    return build_frac_table(base, base_max, alpha, W, T, ceil_out, w_out, cap, n_out);
+    return build_frac_table(base, base_max, alpha, W, T, ceil_out, w_out, nullptr, cap, n_out);
 }
 
 fibattn_status fibattn_fwd_frac(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -187,20 +223,10 @@ fibattn_status fibattn_fwd_frac(const void* q, const void* k, const void* v, voi
     if (!q || !k || !v || !o || !lse || !alphas) return FIBATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FIBATTN_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || T < 1 || W < 1 || n_layers_call < 1 || n_layers_call > FIBATTN_LAYERS_MAX)
-        return FIBATTN_ERR_INVALID_ARG;
-    if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
-    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
-    const int64_t per_layer = (int64_t)B * H * T;
-    if (per_layer > ((int64_t)1 << 34) || per_layer * n_layers_call > ((int64_t)1 << 40))
-        return FIBATTN_ERR_INVALID_ARG;
     // every layer's table is validated before anything is launched
-    for (int32_t c = 0; c < n_layers_call; ++c) {
-        int32_t n = 0;
-        fibattn_status st = build_frac_table(base, base_max, alphas[c], W, T, nullptr, nullptr, 0, &n);
-        if (st == FIBATTN_ERR_INVALID_ARG) return st;
-        if (n > kMaxOffsets) return FIBATTN_ERR_CAPACITY;
-    }
+    fibattn_status st0 = check_frac(B, H, T, d, dtype, W, base, base_max, alphas, n_layers_call, nullptr);
+    if (st0 != FIBATTN_OK) return st0;
+    const int64_t per_layer = (int64_t)B * H * T;
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
     const size_t es = elt_size(dtype);
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
@@ -284,6 +310,80 @@ fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const vo
                                     pds + poff * ws.n_max, ws.n_max, sh, t,
                                     as_stream(cuda_stream));
         }
+        if (st != FIBATTN_OK) return st;
+    }
+    return FIBATTN_OK;
+}
+
+fibattn_status fibattn_bwd_frac_workspace_size(int32_t B, int32_t H, int32_t T, int32_t d,
+                                               int32_t dtype, int32_t W, int32_t base,
+                                               int64_t base_max, const float* alphas,
+                                               int32_t n_layers_call, uint64_t* bytes) {
+    if (!bytes) return FIBATTN_ERR_INVALID_ARG;
+    int32_t n_max = 0;
+    fibattn_status st = check_frac(B, H, T, d, dtype, W, base, base_max, alphas, n_layers_call, &n_max);
+    if (st != FIBATTN_OK) return st;
+    *bytes = workspace_layout(B, H, T, dtype, n_layers_call, n_max, true).total;
+    return FIBATTN_OK;
+}
+
+fibattn_status fibattn_bwd_frac(const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                float* dalpha, void* workspace, uint64_t workspace_bytes,
+                                int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype,
+                                int32_t W, float scale, int32_t base, int64_t base_max,
+                                const float* alphas, int32_t n_layers_call, void* cuda_stream) {
+    const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return FIBATTN_ERR_INVALID_ARG;
+    if (!dalpha || (reinterpret_cast<uintptr_t>(dalpha) & 3u) != 0) return FIBATTN_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FIBATTN_ERR_INVALID_ARG;
+    int32_t n_max = 0;
+    fibattn_status st = check_frac(B, H, T, d, dtype, W, base, base_max, alphas, n_layers_call, &n_max);
+    if (st != FIBATTN_OK) return st;
+    const BwdWorkspace ws = workspace_layout(B, H, T, dtype, n_layers_call, n_max, true);
+    if (workspace_bytes < ws.total) return FIBATTN_ERR_INVALID_ARG;
+    char* wsb = static_cast<char*>(workspace);
+    float* delta = reinterpret_cast<float*>(wsb);
+    float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2_offset);
+    uint32_t* pds = reinterpret_cast<uint32_t*>(wsb + ws.pds_offset);
+    float* galpha = reinterpret_cast<float*>(wsb + ws.galpha_offset);
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    const int64_t per_layer = (int64_t)B * H * T;
+    const int64_t per_layer_pad = (int64_t)B * H * ws.T_pad;
+    // dalpha partials per layer: one per query (f32) or one per 128-query tile (bf16)
+    const int64_t parts = dtype == FIBATTN_F32 ? per_layer : (int64_t)B * H * ((T + 127) / 128);
+    const size_t es = elt_size(dtype);
+    cudaStream_t s = as_stream(cuda_stream);
+    for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
+        const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
+        FracTables t;
+        st = build_frac_launch_tables(base, base_max, alphas + c, n, W, T, &t);
+        if (st != FIBATTN_OK) return st;
+        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        const size_t off = (size_t)c * per_layer * d * es;
+        const size_t loff = (size_t)c * per_layer;
+        if (dtype == FIBATTN_F32) {
+            st = launch_bwd_frac_simt_f32((const float*)((const char*)q + off),
+                                          (const float*)((const char*)k + off),
+                                          (const float*)((const char*)v + off),
+                                          (const float*)((const char*)o + off), lse + loff,
+                                          (const float*)((const char*)dO + off),
+                                          (float*)((char*)dq + off), (float*)((char*)dk + off),
+                                          (float*)((char*)dv + off), delta + loff,
+                                          galpha + (size_t)c * parts, sh, t, s);
+        } else {
+            const size_t poff = (size_t)c * per_layer_pad;
+            st = launch_bwd_frac_tc_bf16((const char*)q + off, (const char*)k + off,
+                                         (const char*)v + off, (const char*)o + off, lse + loff,
+                                         (const char*)dO + off, (char*)dq + off, (char*)dk + off,
+                                         (char*)dv + off, delta + poff, lse2 + poff,
+                                         pds + poff * ws.n_max, ws.n_max, galpha + (size_t)c * parts,
+                                         sh, t, s);
+        }
+        if (st != FIBATTN_OK) return st;
+        st = launch_dalpha_reduce(galpha + (size_t)c * parts, dalpha + c, n, parts, s);
         if (st != FIBATTN_OK) return st;
     }
     return FIBATTN_OK;

@@ -38,6 +38,17 @@
 //   kernel stored, so no dot product is recomputed; each pass is added into TMEM.
 //   Epilogue: dk = scale dK, dv = dV, bf16, TMA stores.
 //
+// Fractional offsets (the learned-alpha variant; Metodologia / Arquitetura, "Implementacao":
+// keys and values linearly interpolated between rows so that the gradient reaches alpha),
+// kFrac: a real distance d is held as c = ceil(d) and the weight w = c - d of the row after
+// i - c. The query owner reads both rows of each shifted item (the item carries the 8 rows
+// after its tile), forms s~ = lerp(q.k_lo, q.k_lo+1), dp~ likewise, dq += dS k~ with k~ the
+// interpolated row, stores (P, dS) under the key row lo = i - c, and adds the query's share
+// of dL/dalpha, g_i = sum_k f_k [dS scale q.(k_lo - k_lo+1) + P dO.(v_lo - v_lo+1)], to a
+// per-row array that a reduction kernel sums per layer. The key owner takes, per distance,
+// the pair of query j + c (key j as row lo, weight 1 - w) and that of query j + c - 1 (key j
+// as row lo + 1, weight w); its shifted Q/dO items carry the 8 rows before their tile.
+//
 // Every mbarrier wait is bounded (tc::mbar_wait); a wait that runs out latches the device
 // error word, later waits return at once, and the CTA still releases its TMEM.
 #include <cuda.h>
@@ -80,7 +91,20 @@ struct BwdParams {
     int32_t n_max;                        // offsets per layer slot in pds
     float scale;
     float scale_log2;                     // scale * log2(e)
-    OffsetTables tabs;
+    OffsetTables tabs;                    // fractional mode: ceil(d) of each real distance d
+};
+
+template <bool kFrac>
+struct BwdArgs : BwdParams {};
+
+template <>
+struct BwdArgs<true> : BwdParams {
+    CUtensorMap tm_k8, tm_v8;   // 8-row boxes: the rows after a shifted K/V tile (query owner)
+    CUtensorMap tm_q8, tm_do8;  // 8-row boxes: the rows before a shifted Q/dO tile (key owner)
+    float* galpha;              // [slices][tiles]: sum over the tile's queries of
+                                // g_i = sum_k f_k dL/dd_k (fixed order)
+    float w[kMaxLayersPerLaunch][kMaxOffsets];  // weight ceil(d) - d of the later row
+    float f[kMaxLayersPerLaunch][kMaxOffsets];  // base value F of the distance (dd/dalpha)
 };
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t sbase, uint32_t off, int idx) {
@@ -107,14 +131,23 @@ constexpr uint32_t kOffDO = kOffQ + kTileBytes;
 constexpr uint32_t kOffK = kOffDO + kTileBytes;      // 2 stages x 8 KB
 constexpr uint32_t kOffV = kOffK + 2 * kChunkBytes;  // 2 stages x 8 KB
 constexpr uint32_t kOffRing = kOffV + 2 * kChunkBytes;
-constexpr uint32_t kOffBar = kOffRing + 2 * kTileBytes;
 // barriers: 0 q+dO, 1-2 band K/V full, 3 S/dP ready, 4 dS written (128), 5 dQ MMA done,
 // 6-7 ring full, 8-9 ring empty (128)
 constexpr int kNumBars = 10;
-constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemAlloc = kOffTmemSlot + 16 + 1024;
+// the two ring slots: a tile, plus (fractional mode) the 8 rows after it
+template <bool kFrac>
+struct Layout {
+    static constexpr uint32_t kSlot = kTileBytes + (kFrac ? 1024u : 0u);
+    static constexpr uint32_t kOffBar = kOffRing + 2 * kSlot;
+    static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffRed = kOffTmemSlot + 16;  // 4 floats: per-warp dalpha sums
+    static constexpr uint32_t kSmemAlloc = kOffRed + 16 + 1024;
+};
 
-__global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
+template <bool kFrac>
+__global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_constant__ BwdArgs<kFrac> p) {
+    using L = Layout<kFrac>;
+    constexpr uint32_t kOffBar = L::kOffBar, kOffTmemSlot = L::kOffTmemSlot, kSlot = L::kSlot;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
@@ -215,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
         // ring items: the O tile (for D), then K_o and V_o per active offset
         if (lane == 0) {
             prefetch_tmap(&p.tm_o);
+            if constexpr (kFrac) {
+                prefetch_tmap(&p.tm_k8);
+                prefetch_tmap(&p.tm_v8);
+            }
             mbar_arrive_expect_tx(B_FULL(0), kTileBytes);
             tma_load_3d(sbase + kOffRing, &p.tm_o, B_FULL(0), 0, i0, z);
             tma_load_3d(sbase + kOffRing + kChunkBytes, &p.tm_o, B_FULL(0), 0, i0 + kChunk, z);
@@ -224,11 +261,16 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                 for (int h = 0; h < 2; ++h, ++seq) {
                     const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
                     const int s = seq & 1;
+                    const uint32_t dst = sbase + kOffRing + s * kSlot;
                     mbar_wait(B_EMPTY(s), ((seq >> 1) & 1) ^ 1, aborted, p.err);
-                    mbar_arrive_expect_tx(B_FULL(s), kTileBytes);
-                    tma_load_3d(sbase + kOffRing + s * kTileBytes, map, B_FULL(s), 0, y, z);
-                    tma_load_3d(sbase + kOffRing + s * kTileBytes + kChunkBytes, map, B_FULL(s), 0,
-                                y + kChunk, z);
+                    // fractional mode: every item also carries the 8 rows after its tile (the
+                    // derivative in d needs row lo + 1 even where w = 0)
+                    mbar_arrive_expect_tx(B_FULL(s), kSlot);
+                    tma_load_3d(dst, map, B_FULL(s), 0, y, z);
+                    tma_load_3d(dst + kChunkBytes, map, B_FULL(s), 0, y + kChunk, z);
+                    if constexpr (kFrac)
+                        tma_load_3d(dst + kTileBytes, h == 0 ? &p.tm_k8 : &p.tm_v8, B_FULL(s), 0,
+                                    y + kRows, z);
                 }
             }
             for (uint32_t q = seq > 2 ? seq - 2 : 0; q < seq; ++q)
@@ -314,13 +356,75 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
         for (int c = 0; c < 64; ++c) dq[c] = 0.f;
         uint32_t seq = 1;  // ring item 0 was the O tile
         const int64_t pds_row = (int64_t)z * p.n_max * p.T_pad + i;
+        float ga = 0.f;  // fractional mode: this query's share of dL/dalpha
 #pragma unroll 1
         for (int k = 0; k < n_act; ++k) {
             const bool valid = row_ok && i - offs[k] >= 0;
+            if constexpr (kFrac) {
+                // k~ = k_lo + w (k_lo+1 - k_lo) into registers (bf16), the two row dots exact
+                const float wk = p.w[layer][k];
+                int s = seq & 1;
+                mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
+                const uint8_t* krow = smem + kOffRing + s * kSlot;
+                const uint8_t* qrow = smem + kOffQ;
+                uint32_t kt[32];
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
+                    const uint4 y = *reinterpret_cast<const uint4*>(krow + sw128_off(r + 1, c));
+                    const uint4 qq = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
+                    fma2_bf16(qq.x, x.x, a0, a1);
+                    fma2_bf16(qq.y, x.y, a2, a3);
+                    fma2_bf16(qq.z, x.z, a0, a1);
+                    fma2_bf16(qq.w, x.w, a2, a3);
+                    fma2_bf16(qq.x, y.x, b0, b1);
+                    fma2_bf16(qq.y, y.y, b2, b3);
+                    fma2_bf16(qq.z, y.z, b0, b1);
+                    fma2_bf16(qq.w, y.w, b2, b3);
+                    kt[4 * c + 0] = lerp_bf16x2(x.x, y.x, wk);
+                    kt[4 * c + 1] = lerp_bf16x2(x.y, y.y, wk);
+                    kt[4 * c + 2] = lerp_bf16x2(x.z, y.z, wk);
+                    kt[4 * c + 3] = lerp_bf16x2(x.w, y.w, wk);
+                }
+                mbar_arrive(B_EMPTY(s));
+                ++seq;
+                const float slo = (a0 + a1) + (a2 + a3), shi = (b0 + b1) + (b2 + b3);
+                s = seq & 1;
+                mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
+                const uint8_t* vrow = smem + kOffRing + s * kSlot;
+                a0 = a1 = a2 = a3 = b0 = b1 = b2 = b3 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(vrow + sw128_off(r, c));
+                    const uint4 y = *reinterpret_cast<const uint4*>(vrow + sw128_off(r + 1, c));
+                    fma2_bf16(gw[4 * c + 0], x.x, a0, a1);
+                    fma2_bf16(gw[4 * c + 1], x.y, a2, a3);
+                    fma2_bf16(gw[4 * c + 2], x.z, a0, a1);
+                    fma2_bf16(gw[4 * c + 3], x.w, a2, a3);
+                    fma2_bf16(gw[4 * c + 0], y.x, b0, b1);
+                    fma2_bf16(gw[4 * c + 1], y.y, b2, b3);
+                    fma2_bf16(gw[4 * c + 2], y.z, b0, b1);
+                    fma2_bf16(gw[4 * c + 3], y.w, b2, b3);
+                }
+                mbar_arrive(B_EMPTY(s));
+                ++seq;
+                const float dlo = (a0 + a1) + (a2 + a3), dhi = (b0 + b1) + (b2 + b3);
+                const float sdot = fmaf(wk, shi - slo, slo), dpd = fmaf(wk, dhi - dlo, dlo);
+                const float pr = valid ? ex2(sdot * sl2 - lse2) : 0.f;
+                const float ds = pr * (dpd - D);
+                const uint32_t pair = pack_bf16x2(pr, ds);  // lo = P, hi = dS
+                if (valid) p.pds[pds_row + (int64_t)k * p.T_pad - offs[k]] = pair;  // key row lo
+                ga += p.f[layer][k] * (ds * p.scale * (slo - shi) + pr * (dlo - dhi));
+                const uint32_t dsb = pair >> 16;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) axpy2_bf16(dsb, kt[c], dq[2 * c], dq[2 * c + 1]);
+                continue;
+            }
             int s = seq & 1;
             mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
             uint32_t kw[32];
-            load_row_sw(smem + kOffRing + s * kTileBytes, r, kw);
+            load_row_sw(smem + kOffRing + s * kSlot, r, kw);
             mbar_arrive(B_EMPTY(s));
             ++seq;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -340,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
             mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
             float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
             {
-                const uint8_t* vrow = smem + kOffRing + s * kTileBytes;
+                const uint8_t* vrow = smem + kOffRing + s * kSlot;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 x = *reinterpret_cast<const uint4*>(vrow + sw128_off(r, c));
@@ -360,6 +464,15 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
             const uint32_t dsb = pair >> 16;  // dS as bf16 in the low half
 #pragma unroll
             for (int c = 0; c < 32; ++c) axpy2_bf16(dsb, kw[c], dq[2 * c], dq[2 * c + 1]);
+        }
+
+        if constexpr (kFrac) {
+            // the tile's share of dL/dalpha: warp sums, then thread 0 adds the four in order
+            // after the epilogue's barrier
+            float g = ga;  // 0 on rows past T
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) g += __shfl_xor_sync(0xffffffffu, g, m);
+            if (lane == 0) reinterpret_cast<float*>(smem + L::kOffRed)[warp] = g;
         }
 
         // ---- epilogue: dq = scale (dQ_band + dq_off), staged in the Q tile, TMA store
@@ -388,6 +501,12 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
         fence_proxy_async_smem();
         tc_fence_before();
         asm volatile("bar.sync 1, 128;" ::: "memory");
+        if constexpr (kFrac) {
+            if (tid == 0) {
+                const float* red = reinterpret_cast<const float*>(smem + L::kOffRed);
+                p.galpha[zl * p.tiles_per_slice + tile] = ((red[0] + red[1]) + red[2]) + red[3];
+            }
+        }
         if (tid == 0 && !aborted) {
             tma_store_3d(&p.tm_dq, sbase + kOffQ, 0, i0, z);
             if (i0 + kChunk < T) tma_store_3d(&p.tm_dq, sbase + kOffQ + kChunkBytes, 0, i0 + kChunk, z);
@@ -417,15 +536,24 @@ constexpr uint32_t kSlots = 6;
 constexpr int kMaxGroupChunks = 4;    // band chunks per K/V copy: 2 + 4 ring items
 constexpr uint32_t kFullArrivals = 1;  // the producer's arrival with the byte count
 
-constexpr uint32_t kOffRing = 0;
-constexpr uint32_t kOffSide = kOffRing + kSlots * ring::kSlotBytes;  // [slot][128] 4-byte words
-constexpr uint32_t kOffBar = kOffSide + kSlots * 128 * 4;
 // barriers: FULL[kSlots], EMPTY[kSlots], S^T/dP^T ready, P^T/dS^T written (8 warps),
 // dK/dV MMAs done, TMEM free (8 warps)
 constexpr uint32_t kBarS = 2 * kSlots, kBarP = kBarS + 1, kBarM = kBarS + 2, kBarT = kBarS + 3;
 constexpr uint32_t kNumBars = kBarT + 1;
-constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemAlloc = kOffTmemSlot + 16 + 1024;
+// Shared memory: the ring slots, then per slot its side words, then the barriers. In the
+// fractional mode a shifted Q/dO item puts the 8 rows before its tile at the slot's start
+// and the tile 1 KB further (kPre), and its side data holds the pairs of key rows j0-4 ..
+// j0+127 (132 words).
+template <bool kFrac>
+struct Layout {
+    static constexpr uint32_t kPre = kFrac ? 1024u : 0u;
+    static constexpr uint32_t kSlot = ring::kSlotBytes + kPre;
+    static constexpr uint32_t kSide = kFrac ? 640u : 512u;  // bytes of side data per slot
+    static constexpr uint32_t kOffSide = kSlots * kSlot;
+    static constexpr uint32_t kOffBar = kOffSide + kSlots * kSide;
+    static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kSmemAlloc = kOffTmemSlot + 16 + 1024;
+};
 
 // Band queries [j0, min(T-1, j0+127+W-1)] in 64-query chunks, grouped by kMaxGroupChunks
 // (each group re-reads the K and V tiles, so no ring item waits on a later one); active
@@ -453,19 +581,22 @@ __device__ __forceinline__ Plan make_plan(const BwdParams& p, int layer, int32_t
     return pl;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
+template <bool kFrac>
+__global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs<kFrac> p) {
+    using L = Layout<kFrac>;
+    constexpr uint32_t kOffBar = L::kOffBar, kOffTmemSlot = L::kOffTmemSlot, kPre = L::kPre;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t T = p.T, W = p.W;
-    const ring::Ring rg{sbase + kOffRing, sbase + kOffBar, kSlots, kRowWarps};
+    const ring::Ring rg{sbase, sbase + kOffBar, kSlots, kRowWarps, L::kSlot};
     auto bar = [&](uint32_t idx) { return sbase + kOffBar + 8u * idx; };
     const uint32_t B_S = bar(kBarS), B_P = bar(kBarP), B_M = bar(kBarM), B_T = bar(kBarT);
-    auto side_addr = [&](uint32_t seq) { return sbase + kOffSide + rg.slot(seq) * 512u; };
+    auto side_addr = [&](uint32_t seq) { return sbase + L::kOffSide + rg.slot(seq) * L::kSide; };
     auto side_ptr = [&](uint32_t seq) {
-        return reinterpret_cast<const float*>(smem + kOffSide + rg.slot(seq) * 512u);
+        return reinterpret_cast<const float*>(smem + L::kOffSide + rg.slot(seq) * L::kSide);
     };
     auto slot_ptr = [&](uint32_t seq) { return smem + (rg.addr(seq) - sbase); };
 
@@ -496,6 +627,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             prefetch_tmap(&p.tm_v);
             prefetch_tmap(&p.tm_dk);
             prefetch_tmap(&p.tm_dv);
+            if constexpr (kFrac) {
+                prefetch_tmap(&p.tm_q8);
+                prefetch_tmap(&p.tm_do8);
+            }
             uint32_t seq = 0;
             const int32_t Tp = p.T_pad;
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
@@ -526,18 +661,30 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                     }
                 }
                 // Q_o of every offset, then dO_o of every offset; both carry the (P, dS) pairs of
-                // the tile's key rows as side data
+                // the tile's key rows as side data. Fractional mode: pairs from key row j0 - 4
+                // (from row 0 at j0 = 0, leaving words 0-3 unread) and, where w != 0, the 8 rows
+                // before the tile.
                 const int32_t* offs = p.tabs.off[tl.layer];
-                const uint32_t pair_bytes = 4u * (uint32_t)min(kRows, Tp - pl.j0);
+                const int32_t pfirst = kFrac ? max(pl.j0 - 4, 0) : pl.j0;
+                const uint32_t pskip = kFrac ? 4u * (uint32_t)(pfirst - (pl.j0 - 4)) : 0u;
+                const uint32_t pair_bytes =
+                    4u * (uint32_t)min(kRows + (int32_t)(kFrac ? 4 : 0) - (int32_t)(pskip / 4u), Tp - pfirst);
                 for (int h = 0; h < 2; ++h) {
                     for (int k = 0; k < pl.n_act; ++k, ++seq) {
                         if (!rg.acquire(seq, aborted, p.err)) continue;
                         const int32_t y = pl.j0 + offs[k];
                         const CUtensorMap* map = h == 0 ? &p.tm_q : &p.tm_do;
-                        mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + pair_bytes);
-                        tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, z);
-                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, z);
-                        bulk_load(side_addr(seq), p.pds + ((int64_t)z * p.n_max + k) * Tp + pl.j0,
+                        bool pre = false;
+                        if constexpr (kFrac) pre = p.w[tl.layer][k] != 0.f;
+                        mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + (pre ? 1024u : 0u) + pair_bytes);
+                        tma_load_3d(rg.addr(seq) + kPre, map, rg.full(seq), 0, y, z);
+                        tma_load_3d(rg.addr(seq) + kPre + kChunkBytes, map, rg.full(seq), 0, y + kChunk, z);
+                        if constexpr (kFrac) {
+                            if (pre)
+                                tma_load_3d(rg.addr(seq), h == 0 ? &p.tm_q8 : &p.tm_do8, rg.full(seq), 0,
+                                            y - 8, z);
+                        }
+                        bulk_load(side_addr(seq) + pskip, p.pds + ((int64_t)z * p.n_max + k) * Tp + pfirst,
                                   pair_bytes, rg.full(seq));
                     }
                 }
@@ -687,6 +834,42 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
 #pragma unroll 1
                 for (int k = 0; k < pl.n_act; ++k) {
                     rg.wait_full(seq, aborted, p.err);
+                    if constexpr (kFrac) {
+                        // key j is row lo of query j + c (weight 1 - w: pair of key row j) and
+                        // row lo + 1 of query j + c - 1 (weight w: pair of key row j - 1); the
+                        // tile's row r is virtual row r + 8 of the slot, the row before it r + 7
+                        const float wk = p.w[tl.layer][k];
+                        const uint32_t* pw = reinterpret_cast<const uint32_t*>(side_ptr(seq));
+                        const uint32_t plo = (row_ok && j + offs[k] < T) ? pw[r + 4] : 0u;
+                        const uint32_t phi =
+                            (wk != 0.f && row_ok && j >= 1 && j + offs[k] - 1 < T) ? pw[r + 3] : 0u;
+                        const float xlo = pass == 0 ? bf16hi(plo) : bf16lo(plo);  // dS or P
+                        const float xhi = pass == 0 ? bf16hi(phi) : bf16lo(phi);
+                        const uint32_t clo = pack_bf16x2((1.f - wk) * xlo, 0.f);
+                        const uint32_t chi = pack_bf16x2(wk * xhi, 0.f);
+                        const uint8_t* row = slot_ptr(seq);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 x = *reinterpret_cast<const uint4*>(row + sw128_off(r + 8, 4 * h + c));
+                            axpy2_bf16(clo, x.x, acc[8 * c + 0], acc[8 * c + 1]);
+                            axpy2_bf16(clo, x.y, acc[8 * c + 2], acc[8 * c + 3]);
+                            axpy2_bf16(clo, x.z, acc[8 * c + 4], acc[8 * c + 5]);
+                            axpy2_bf16(clo, x.w, acc[8 * c + 6], acc[8 * c + 7]);
+                        }
+                        if (wk != 0.f) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint4 x = *reinterpret_cast<const uint4*>(row + sw128_off(r + 7, 4 * h + c));
+                                axpy2_bf16(chi, x.x, acc[8 * c + 0], acc[8 * c + 1]);
+                                axpy2_bf16(chi, x.y, acc[8 * c + 2], acc[8 * c + 3]);
+                                axpy2_bf16(chi, x.z, acc[8 * c + 4], acc[8 * c + 5]);
+                                axpy2_bf16(chi, x.w, acc[8 * c + 6], acc[8 * c + 7]);
+                            }
+                        }
+                        rg.release_warp(seq, lane);
+                        ++seq;
+                        continue;
+                    }
                     const uint32_t pair = (row_ok && j + offs[k] < T)
                                               ? reinterpret_cast<const uint32_t*>(side_ptr(seq))[r] : 0u;
                     const uint32_t sc = pass == 0 ? pair >> 16 : pair & 0xFFFFu;  // dS or P (bf16)
@@ -801,16 +984,20 @@ fibattn_status set_smem(const void* fn, uint32_t bytes, bool (&done)[64]) {
 
 }  // namespace
 
-fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, const void* o,
-                                  const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                                  float* delta, float* lse2, uint32_t* pds, int32_t n_max,
-                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
+namespace {
+
+template <bool kFrac>
+fibattn_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          float* delta, float* lse2, uint32_t* pds, int32_t n_max,
+                          const AttnShape& sh, const OffsetTables& t, const FracTables* ft,
+                          float* galpha, cudaStream_t st) {
     const int64_t slices = sh.slices_per_layer * sh.n_layers;
     if (slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     const int32_t tiles = (sh.T + kRows - 1) / kRows;
     const int64_t gx = (int64_t)tiles * sh.slices_per_layer;
     if (gx > 0x7fffffff || (int64_t)tiles * slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
-    BwdParams P;
+    BwdArgs<kFrac> P;
     // the error-word lookup is a runtime call: it binds the device's primary context to this
     // thread (a fresh thread, e.g. autograd's, may have none), which the encoding needs
     P.err = device_error_word();
@@ -820,6 +1007,20 @@ fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, c
     for (int m = 0; m < 8; ++m) {
         const int r = make_bf16_rows_map(maps[m], bases[m], slices, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (bwd)");
+    }
+    if constexpr (kFrac) {
+        const void* b8[4] = {k, v, q, dO};
+        CUtensorMap* m8[4] = {&P.tm_k8, &P.tm_v8, &P.tm_q8, &P.tm_do8};
+        for (int m = 0; m < 4; ++m) {
+            const int r = make_bf16_rows8_map(m8[m], b8[m], slices, sh.T);
+            if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (bwd, 8-row box)");
+        }
+        P.galpha = galpha;
+        for (int l = 0; l < kMaxLayersPerLaunch; ++l)
+            for (int e = 0; e < kMaxOffsets; ++e) {
+                P.w[l][e] = ft->w[l][e];
+                P.f[l][e] = ft->f[l][e];
+            }
     }
     P.lse = lse;
     P.delta = delta;
@@ -838,9 +1039,11 @@ fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, c
     P.tabs = t;
     static bool dq_set[64] = {}, dkdv_set[64] = {};
     static int n_sm[64] = {};
-    fibattn_status s0 = set_smem((const void*)dq::bwd_dq_tc_kernel, dq::kSmemAlloc, dq_set);
+    fibattn_status s0 = set_smem((const void*)dq::bwd_dq_tc_kernel<kFrac>,
+                                 dq::Layout<kFrac>::kSmemAlloc, dq_set);
     if (s0 != FIBATTN_OK) return s0;
-    s0 = set_smem((const void*)dkdv::bwd_dkdv_tc_kernel, dkdv::kSmemAlloc, dkdv_set);
+    s0 = set_smem((const void*)dkdv::bwd_dkdv_tc_kernel<kFrac>, dkdv::Layout<kFrac>::kSmemAlloc,
+                  dkdv_set);
     if (s0 != FIBATTN_OK) return s0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -852,17 +1055,39 @@ fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, c
     }
     const int64_t pgrid = (int64_t)P.total_tiles < 2LL * n_sm[dev] ? (int64_t)P.total_tiles : 2LL * n_sm[dev];
     dim3 grid((unsigned)gx, sh.n_layers);
+    const char* n_dq = kFrac ? "bwd_dq_frac_tc" : "bwd_dq_tc";
+    const char* n_kv = kFrac ? "bwd_dkdv_frac_tc" : "bwd_dkdv_tc";
     {
-        KernelScope ks("bwd_dq_tc", st);
-        dq::bwd_dq_tc_kernel<<<grid, dq::kThreads, dq::kSmemAlloc, st>>>(P);
+        KernelScope ks(n_dq, st);
+        dq::bwd_dq_tc_kernel<kFrac><<<grid, dq::kThreads, dq::Layout<kFrac>::kSmemAlloc, st>>>(P);
     }
-    s0 = launch_status("launch bwd_dq_tc");
+    s0 = launch_status(n_dq);
     if (s0 != FIBATTN_OK) return s0;
     {
-        KernelScope ks("bwd_dkdv_tc", st);
-        dkdv::bwd_dkdv_tc_kernel<<<(unsigned)pgrid, dkdv::kThreads, dkdv::kSmemAlloc, st>>>(P);
+        KernelScope ks(n_kv, st);
+        dkdv::bwd_dkdv_tc_kernel<kFrac>
+            <<<(unsigned)pgrid, dkdv::kThreads, dkdv::Layout<kFrac>::kSmemAlloc, st>>>(P);
     }
-    return launch_status("launch bwd_dkdv_tc");
+    return launch_status(n_kv);
+}
+
+}  // namespace
+
+fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                  float* delta, float* lse2, uint32_t* pds, int32_t n_max,
+                                  const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
+    return launch_bwd<false>(q, k, v, o, lse, dO, dq, dk, dv, delta, lse2, pds, n_max, sh, t,
+                             nullptr, nullptr, st);
+}
+
+fibattn_status launch_bwd_frac_tc_bf16(const void* q, const void* k, const void* v, const void* o,
+                                       const float* lse, const void* dO, void* dq, void* dk,
+                                       void* dv, float* delta, float* lse2, uint32_t* pds,
+                                       int32_t n_max, float* galpha, const AttnShape& sh,
+                                       const FracTables& t, cudaStream_t st) {
+    return launch_bwd<true>(q, k, v, o, lse, dO, dq, dk, dv, delta, lse2, pds, n_max, sh, t.c,
+                            &t, galpha, st);
 }
 
 }  // namespace fibattn

@@ -21,11 +21,13 @@ struct OffsetTables {
 };
 
 // Fractional-offset tables of one launch (the learned-alpha variant): for every real distance
-// d = alpha * F kept by the table rule, `c.off` holds ceil(d) (ascending, possibly repeated)
-// and `w` the interpolation weight ceil(d) - d in [0, 1) of the row after i - ceil(d).
+// d = alpha * F kept by the table rule, `c.off` holds ceil(d) (ascending, possibly repeated),
+// `w` the interpolation weight ceil(d) - d in [0, 1) of the row after i - ceil(d), and `f`
+// the base value F (dd/dalpha, for the gradient of alpha).
 struct FracTables {
     OffsetTables c;
     float w[kMaxLayersPerLaunch][kMaxOffsets];
+    float f[kMaxLayersPerLaunch][kMaxOffsets];
 };
 
 // An exact alpha = num / den of one layer (num, den > 0, already reduced).
@@ -42,7 +44,8 @@ fibattn_status build_table(const fibattn_schedule* s, Alpha a, int32_t W, int32_
 
 // Fractional-offset table of one real alpha (see fibattn_frac_offsets).
 fibattn_status build_frac_table(int32_t base, int64_t base_max, float alpha, int32_t W, int32_t T,
-                                int32_t* c_out, float* w_out, int32_t cap, int32_t* n_out);
+                                int32_t* c_out, float* w_out, float* f_out, int32_t cap,
+                                int32_t* n_out);
 
 // Builds FracTables for n launch layers with alphas[0..n).
 fibattn_status build_frac_launch_tables(int32_t base, int64_t base_max, const float* alphas,
@@ -111,6 +114,26 @@ fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* 
                                    const float* lse, const float* dO, float* dq, float* dk,
                                    float* dv, float* delta, const AttnShape& sh,
                                    const OffsetTables& t, cudaStream_t st);
+
+// Fractional-offset backwards: dq/dk/dv as the static ones with interpolated rows, plus the
+// partials of dL/dalpha (g_i = sum_k f_k dL/dd_k of query i) into galpha: per query,
+// [slices][T], on the SIMT path; per 128-query tile, [slices][tiles], on the tensor-core
+// path (reduced per layer by launch_dalpha_reduce). Workspace as the static bf16 backward
+// (n_max from the frac tables).
+fibattn_status launch_bwd_frac_simt_f32(const float* q, const float* k, const float* v,
+                                        const float* o, const float* lse, const float* dO,
+                                        float* dq, float* dk, float* dv, float* delta,
+                                        float* galpha, const AttnShape& sh, const FracTables& t,
+                                        cudaStream_t st);
+fibattn_status launch_bwd_frac_tc_bf16(const void* q, const void* k, const void* v, const void* o,
+                                       const float* lse, const void* dO, void* dq, void* dk,
+                                       void* dv, float* delta, float* lse2, uint32_t* pds,
+                                       int32_t n_max, float* galpha, const AttnShape& sh,
+                                       const FracTables& t, cudaStream_t st);
+// dalpha[l] = sum of galpha over the rows_per_layer rows of launch layer l, for n layers
+// (fixed summation order, fp64 accumulation: deterministic).
+fibattn_status launch_dalpha_reduce(const float* galpha, float* dalpha, int32_t n,
+                                    int64_t rows_per_layer, cudaStream_t st);
 
 // Tensor-core backward (bf16 path). Workspace rows are padded to T_pad = T rounded up to 4:
 // delta and lse2 [slices][T_pad] fp32, pds [slices][n_max][T_pad] (P, dS) bf16 pairs indexed

@@ -113,19 +113,21 @@ fibattn_status build_table(const fibattn_schedule* s, Alpha a, int32_t W, int32_
 }
 
 fibattn_status build_frac_table(int32_t base, int64_t base_max, float alpha, int32_t W, int32_t T,
-                                int32_t* c_out, float* w_out, int32_t cap, int32_t* n_out) {
+                                int32_t* c_out, float* w_out, float* f_out, int32_t cap,
+                                int32_t* n_out) {
     if (W < 1 || T < 1 || cap < 0 || base_max < 0) return FIBATTN_ERR_INVALID_ARG;
     if (base != FIBATTN_BASE_FIB && base != FIBATTN_BASE_POW2) return FIBATTN_ERR_INVALID_ARG;
     if (!(alpha > 0.f) || !(alpha <= (float)FIBATTN_RATIO_MAX)) return FIBATTN_ERR_INVALID_ARG;
     const bool fib = base == FIBATTN_BASE_FIB;
     const double a = (double)alpha;
     int32_t n = 0;
-    auto keep = [&](double d) {
+    auto keep = [&](double d, int64_t f) {
         if (d < (double)W || d > (double)T - 1) return;
         if (n < cap) {
             const double c = ceil(d);
             c_out[n] = (int32_t)c;
             w_out[n] = (float)(c - d);
+            if (f_out) f_out[n] = (float)f;
         }
         ++n;
     };
@@ -133,14 +135,14 @@ fibattn_status build_frac_table(int32_t base, int64_t base_max, float alpha, int
         const int64_t fmax = base_max > 0 ? base_max : 987;
         for (int64_t f = 1, g = 2; f <= fmax;) {
             if (a * (double)f > (double)T - 1) break;  // d grows with F: nothing further fits
-            keep(a * (double)f);
+            keep(a * (double)f, f);
             const int64_t h = f + g;
             f = g;
             g = h;
         }
     } else {
         for (int64_t f = 1; a * (double)f <= (double)T - 1 && (base_max <= 0 || f <= base_max);) {
-            keep(a * (double)f);
+            keep(a * (double)f, f);
             if (f > INT64_MAX / 2) break;
             f *= 2;
         }
@@ -157,12 +159,13 @@ fibattn_status build_frac_launch_tables(int32_t base, int64_t base_max, const fl
         for (int e = 0; e < kMaxOffsets; ++e) {
             t->c.off[c][e] = -1;
             t->w[c][e] = 0.f;
+            t->f[c][e] = 0.f;
         }
     }
     for (int c = 0; c < n; ++c) {
         int32_t cnt = 0;
         fibattn_status st = build_frac_table(base, base_max, alphas[c], W, T, t->c.off[c], t->w[c],
-                                             kMaxOffsets, &cnt);
+                                             t->f[c], kMaxOffsets, &cnt);
         if (st != FIBATTN_OK) return st;
         t->c.count[c] = cnt;
     }

@@ -246,7 +246,176 @@ bwd_dkdv_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
     Io<E>::st(dv + rj, av);
 }
 
+// ---------------------------------------------------------------- fractional backward
+// The rows interpolated at i - d (c = ceil(d), w = c - d, rows lo = i - c and lo + 1):
+//   k~ = (1 - w) k_lo + w k_lo+1, v~ likewise; s = scale q.k~, P = exp(s - lse), dS = P (dO.v~ - D)
+//   dq_i += scale dS k~;  dk_lo += (1 - w) scale dS q_i, dk_lo+1 += w scale dS q_i;
+//   dv_lo += (1 - w) P dO_i, dv_lo+1 += w P dO_i;
+//   dL/dd = dS scale q.(k_lo - k_lo+1) + P dO.(v_lo - v_lo+1)  (the segment [lo, lo+1] even
+//   at w = 0), and the query's share of dL/dalpha is g_i = sum_k f_k dL/dd_k.
+
+// Query owner: dq and g_i (into galpha).
+template <typename E>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+bwd_dq_frac_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
+                   const float* __restrict__ lse, const E* __restrict__ dO,
+                   const float* __restrict__ delta, E* __restrict__ dq, float* __restrict__ galpha,
+                   AttnShape sh, const __grid_constant__ FracTables tab) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int layer = blockIdx.y;
+    if (row >= rows) return;
+    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int32_t i = (int32_t)(row % sh.T);
+    const int64_t base = slice * sh.T * kD;
+    auto row_of = [&](const E* x, int32_t j) { return Io<E>::ld(x + base + (int64_t)j * kD + 2 * lane); };
+    const float2 qv = row_of(q, i);
+    const float2 gv = row_of(dO, i);
+    const float Li = lse[slice * sh.T + i];
+    const float Di = delta[slice * sh.T + i];
+    // the static kernel's order (distances descending, then the window), so that an integer
+    // alpha gives its results bit for bit
+    float2 acc = make_float2(0.f, 0.f);
+    float ga = 0.f;
+    for (int e = tab.c.count[layer] - 1; e >= 0; --e) {
+        const int32_t lo = i - tab.c.off[layer][e];
+        if (lo < 0) continue;
+        const float w = tab.w[layer][e];
+        const float2 k0 = row_of(k, lo), k1 = row_of(k, lo + 1);  // lo + 1 <= i
+        const float2 v0 = row_of(v, lo), v1 = row_of(v, lo + 1);
+        const float2 kt = make_float2((1.f - w) * k0.x + w * k1.x, (1.f - w) * k0.y + w * k1.y);
+        const float2 vt = make_float2((1.f - w) * v0.x + w * v1.x, (1.f - w) * v0.y + w * v1.y);
+        const float s = warp_sum(qv.x * kt.x + qv.y * kt.y);
+        const float dp = warp_sum(gv.x * vt.x + gv.y * vt.y);
+        const float sdiff = warp_sum(qv.x * (k0.x - k1.x) + qv.y * (k0.y - k1.y));
+        const float vdiff = warp_sum(gv.x * (v0.x - v1.x) + gv.y * (v0.y - v1.y));
+        const float p = expf(s * sh.scale - Li);
+        const float ds = p * (dp - Di);
+        acc.x += ds * kt.x;
+        acc.y += ds * kt.y;
+        ga += tab.f[layer][e] * (ds * sh.scale * sdiff + p * vdiff);
+    }
+    const int32_t j0 = i - sh.W + 1 > 0 ? i - sh.W + 1 : 0;
+    for (int32_t j = j0; j <= i; ++j) {
+        const float2 kv = row_of(k, j), vv = row_of(v, j);
+        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
+        const float dp = warp_sum(gv.x * vv.x + gv.y * vv.y);
+        const float p = expf(s * sh.scale - Li);
+        const float ds = p * (dp - Di);
+        acc.x += ds * kv.x;
+        acc.y += ds * kv.y;
+    }
+    Io<E>::st(dq + base + (int64_t)i * kD + 2 * lane, make_float2(acc.x * sh.scale, acc.y * sh.scale));
+    if (lane == 0) galpha[slice * sh.T + i] = ga;
+}
+
+// Key owner: key j is row lo of the query i = j + c (weight 1 - w) and row lo + 1 of the
+// query i = j + c - 1 (weight w), for every distance; plus its window queries j .. j+W-1.
+template <typename E>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+bwd_dkdv_frac_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
+                     const float* __restrict__ lse, const E* __restrict__ dO,
+                     const float* __restrict__ delta, E* __restrict__ dk, E* __restrict__ dv,
+                     AttnShape sh, const __grid_constant__ FracTables tab) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int layer = blockIdx.y;
+    if (row >= rows) return;
+    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int32_t j = (int32_t)(row % sh.T);
+    const int64_t base = slice * sh.T * kD;
+    auto row_of = [&](const E* x, int32_t r) { return Io<E>::ld(x + base + (int64_t)r * kD + 2 * lane); };
+    const float2 kv = row_of(k, j);
+    const float2 vv = row_of(v, j);
+    float2 ak = make_float2(0.f, 0.f), av = make_float2(0.f, 0.f);
+    // query i sees key and value rows (kx, vx); this key's share of them is wt
+    auto visit = [&](int32_t i, float2 kx, float2 vx, float wt) {
+        const float2 qv = row_of(q, i);
+        const float2 gv = row_of(dO, i);
+        const float s = warp_sum(qv.x * kx.x + qv.y * kx.y);
+        const float dp = warp_sum(gv.x * vx.x + gv.y * vx.y);
+        const float p = expf(s * sh.scale - lse[slice * sh.T + i]);
+        const float ds = p * (dp - delta[slice * sh.T + i]);
+        av.x += wt * p * gv.x;
+        av.y += wt * p * gv.y;
+        ak.x += wt * ds * qv.x;
+        ak.y += wt * ds * qv.y;
+    };
+    const int32_t i1 = j + sh.W - 1 < sh.T - 1 ? j + sh.W - 1 : sh.T - 1;
+    for (int32_t i = j; i <= i1; ++i) visit(i, kv, vv, 1.f);
+    for (int e = 0; e < tab.c.count[layer]; ++e) {
+        const int64_t c = tab.c.off[layer][e];
+        const float w = tab.w[layer][e];
+        if ((int64_t)j + c < sh.T) {  // row lo of query j + c: the other row is j + 1 <= j + c
+            const float2 k1 = row_of(k, j + 1), v1 = row_of(v, j + 1);
+            visit((int32_t)(j + c), make_float2((1.f - w) * kv.x + w * k1.x, (1.f - w) * kv.y + w * k1.y),
+                  make_float2((1.f - w) * vv.x + w * v1.x, (1.f - w) * vv.y + w * v1.y), 1.f - w);
+        }
+        if (w != 0.f && j >= 1 && (int64_t)j + c - 1 < sh.T) {  // row lo + 1 of query j + c - 1
+            const float2 k0 = row_of(k, j - 1), v0 = row_of(v, j - 1);
+            visit((int32_t)(j + c - 1), make_float2((1.f - w) * k0.x + w * kv.x, (1.f - w) * k0.y + w * kv.y),
+                  make_float2((1.f - w) * v0.x + w * vv.x, (1.f - w) * v0.y + w * vv.y), w);
+        }
+    }
+    Io<E>::st(dk + base + (int64_t)j * kD + 2 * lane, make_float2(ak.x * sh.scale, ak.y * sh.scale));
+    Io<E>::st(dv + base + (int64_t)j * kD + 2 * lane, av);
+}
+
+// One block per layer: a fixed-order sum (strided fp64 partials, then a tree) of its rows.
+constexpr int kReduceThreads = 1024;
+__global__ void __launch_bounds__(kReduceThreads)
+dalpha_reduce_kernel(const float* __restrict__ galpha, float* __restrict__ dalpha, int64_t rows) {
+    __shared__ double part[kReduceThreads];
+    const float* g = galpha + (int64_t)blockIdx.x * rows;
+    double a = 0.0;
+    for (int64_t r = threadIdx.x; r < rows; r += kReduceThreads) a += (double)g[r];
+    part[threadIdx.x] = a;
+    __syncthreads();
+    for (int s = kReduceThreads / 2; s > 0; s >>= 1) {
+        if ((int)threadIdx.x < s) part[threadIdx.x] += part[threadIdx.x + s];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) dalpha[blockIdx.x] = (float)part[0];
+}
+
 }  // namespace
+
+fibattn_status launch_dalpha_reduce(const float* galpha, float* dalpha, int32_t n,
+                                    int64_t rows_per_layer, cudaStream_t st) {
+    KernelScope ks("dalpha_reduce", st);
+    dalpha_reduce_kernel<<<n, kReduceThreads, 0, st>>>(galpha, dalpha, rows_per_layer);
+    return launch_status("launch dalpha_reduce");
+}
+
+fibattn_status launch_bwd_frac_simt_f32(const float* q, const float* k, const float* v,
+                                        const float* o, const float* lse, const float* dO,
+                                        float* dq, float* dk, float* dv, float* delta,
+                                        float* galpha, const AttnShape& sh, const FracTables& t,
+                                        cudaStream_t st) {
+    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t all_rows = rows * sh.n_layers;
+    const int64_t dblocks = (all_rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffff || dblocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    {
+        KernelScope ks("bwd_delta_simt", st);
+        bwd_delta_kernel<float><<<(unsigned)dblocks, kWarpsPerBlock * 32, 0, st>>>(o, dO, delta, all_rows);
+    }
+    dim3 grid((unsigned)blocks, sh.n_layers);
+    {
+        KernelScope ks("bwd_dq_frac_simt", st);
+        bwd_dq_frac_kernel<float><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dq,
+                                                                         galpha, sh, t);
+    }
+    {
+        KernelScope ks("bwd_dkdv_frac_simt", st);
+        bwd_dkdv_frac_kernel<float><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta,
+                                                                           dk, dv, sh, t);
+    }
+    return launch_status("launch SIMT kernel");
+}
 
 fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o,
                                    float* lse, const AttnShape& sh, const OffsetTables& t,

@@ -331,6 +331,13 @@ __device__ __forceinline__ void axpy2_bf16(uint32_t p, uint32_t v, float& c0, fl
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Elementwise x + w (y - x) of two bf16 pairs, in fp32, rounded to a bf16 pair.
+__device__ __forceinline__ uint32_t lerp_bf16x2(uint32_t x, uint32_t y, float w) {
+    const float lo = fmaf(w, bf16lo(y) - bf16lo(x), bf16lo(x));
+    const float hi = fmaf(w, bf16hi(y) - bf16hi(x), bf16hi(x));
+    return pack_bf16x2(lo, hi);
+}
+
 // Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile (rows of 128 B,
 // 1024-byte aligned): chunk index XOR (row mod 8).
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {

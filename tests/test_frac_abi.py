@@ -90,3 +90,50 @@ def test_binding_refuses_cpu_tensors():
         fa.fwd_frac(q, q, q, 4, [1.0])
     with pytest.raises(ValueError):
         fa.fwd_frac(q, q, q, 4, [1.0, 2.0])
+
+
+def _bwd_frac_raw(ptrs=None, dalpha=256, ws=256, ws_bytes=1 << 40, d=64, dtype=1, alphas=(1.3,),
+                  base=0):
+    L = fa.lib()
+    P = ctypes.c_void_p
+    ptrs = [256] * 9 if ptrs is None else ptrs
+    a = (ctypes.c_float * len(alphas))(*alphas)
+    return L.fibattn_bwd_frac(*[P(x) for x in ptrs], P(dalpha), P(ws), ctypes.c_uint64(ws_bytes),
+                              1, 1, 8, d, dtype, 4, 0.0, base, 0, a, len(alphas), None)
+
+
+def test_bwd_frac_validates_before_launch():
+    for bad in range(9):
+        ptrs = [256] * 9
+        ptrs[bad] = 0
+        assert _bwd_frac_raw(ptrs) == fa.INVALID_ARG
+        ptrs[bad] = 264
+        assert _bwd_frac_raw(ptrs) == fa.INVALID_ARG
+    assert _bwd_frac_raw(dalpha=0) == fa.INVALID_ARG
+    assert _bwd_frac_raw(dalpha=258) == fa.INVALID_ARG
+    assert _bwd_frac_raw(ws=0) == fa.INVALID_ARG
+    assert _bwd_frac_raw(ws=256 + 16) == fa.INVALID_ARG
+    assert _bwd_frac_raw(ws_bytes=16) == fa.INVALID_ARG
+    assert _bwd_frac_raw(d=32) == fa.UNSUPPORTED
+    assert _bwd_frac_raw(alphas=(1.0, -2.0)) == fa.INVALID_ARG
+    assert _bwd_frac_raw(base=5) == fa.INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("shape", [(1, 2, 256, 16), (8, 8, 1024, 64), (3, 1, 777, 6)])
+def test_bwd_frac_workspace_size_layout(dtype, shape):
+    B, H, T, W = shape
+    alphas = [0.8, 1.37, 1.9]
+    L = fa.lib()
+    n = ctypes.c_uint64(0)
+    a = (ctypes.c_float * 3)(*alphas)
+    assert L.fibattn_bwd_frac_workspace_size(B, H, T, 64, dtype, W, 0, 0, a, 3, ctypes.byref(n)) == fa.OK
+    rows = 3 * B * H * T
+    a256 = lambda x: (x + 255) // 256 * 256
+    if dtype == 0:
+        want = a256(rows * 4) + rows * 4
+    else:
+        n_max = max(len(oracle.frac_distances(f, S.FIB, W, T)) for f in [float(np.float32(x)) for x in alphas])
+        rows_pad = 3 * B * H * ((T + 3) // 4 * 4)
+        want = a256(2 * a256(rows_pad * 4) + rows_pad * n_max * 4) + rows * 4
+    assert n.value == want

@@ -128,3 +128,137 @@ def test_fwd_frac_deterministic():
     a = fa.fwd_frac(inp["q"], inp["k"], inp["v"], 64, alphas)
     b = fa.fwd_frac(inp["q"], inp["k"], inp["v"], 64, alphas)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------ backward
+
+DALPHA_TOL = {"f32": 1e-4, "bf16": 2e-2}  # relative to sum_t F_t |dL/dd_t| over the layer
+
+
+def _frac_bwd_run(inp, W, alphas, base="fib"):
+    dev = to_dev(inp)
+    o, lse = fa.fwd_frac(dev["q"], dev["k"], dev["v"], W, alphas, base)
+    dq, dk, dv, da = fa.bwd_frac(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], W, alphas, base)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    return o, dq, dk, dv, da
+
+
+def _check_frac_bwd(inp, W, alphas, base, dtype, layers_full=None, picks=None):
+    """Compare dq/dk/dv on picked slices and dalpha of fully recomputed layers."""
+    o, dq, dk, dv, da = _frac_bwd_run(inp, W, alphas, base)
+    Lc, B, H, T, _ = inp["q"].shape
+    if picks is None:
+        picks = [(l, b, h) for l in range(Lc) for b in range(B) for h in range(H)]
+    if layers_full is None:
+        layers_full = range(Lc)
+    need = sorted(set(picks) | {(l, b, h) for l in layers_full for b in range(B) for h in range(H)})
+    by_layer = {}
+    for (l, b, h) in need:
+        by_layer.setdefault(l, []).append((b, h))
+    worst = dict(dq=0.0, dk=0.0, dv=0.0, o=0.0)
+    for l, bhs in by_layer.items():
+        a = f32(alphas[l])
+        dists = oracle.frac_distances(a, base, W, T)
+        fb = np.array(oracle.frac_bases(a, base, W, T), dtype=np.float64)
+        g = lambda n: np.stack([f64(inp[n][l, b, h]) for b, h in bhs])
+        rq, rk, rv, ro, rl, rdd = oracle.bwd_frac(g("q"), g("k"), g("v"), g("dO"), W, dists)
+        for n, (b, h) in enumerate(bhs):
+            if (l, b, h) in picks:
+                worst["dq"] = max(worst["dq"], max_abs(f64(dq[l, b, h]), rq[n]))
+                worst["dk"] = max(worst["dk"], max_abs(f64(dk[l, b, h]), rk[n]))
+                worst["dv"] = max(worst["dv"], max_abs(f64(dv[l, b, h]), rv[n]))
+                worst["o"] = max(worst["o"], max_abs(f64(o[l, b, h]), ro[n]))
+        if l in layers_full and len(fb):
+            ref = float((rdd[:, : len(fb)] * fb).sum())
+            mag = float((np.abs(rdd[:, : len(fb)]) * fb).sum())
+            err = abs(float(da[l]) - ref)
+            assert err <= DALPHA_TOL[dtype] * max(mag, 1e-6), (l, float(da[l]), ref, mag)
+    for key, val in worst.items():
+        assert val <= TOL[dtype], (key, val)
+
+
+FRAC_BWD_EDGE = [
+    # (B, H, T, W, alpha, base)
+    (1, 1, 1, 4, 1.37, "fib"),
+    (1, 2, 2, 1, 0.61, "fib"),
+    (2, 1, 63, 6, 1.37, "fib"),
+    (1, 3, 127, 8, 0.77, "fib"),
+    (1, 1, 129, 12, 2.3, "fib"),
+    (2, 2, 1000, 10, 1.618, "fib"),
+    (1, 2, 300, 64, 1.1, "pow2"),
+    (1, 1, 700, 700, 1.3, "fib"),
+    (1, 1, 1024, 1, 0.6, "fib"),
+    (1, 2, 2049, 64, 3.7, "pow2"),
+    (1, 1, 640, 16, 0.9999999, "fib"),
+    (1, 1, 640, 16, 1.0000001, "fib"),
+    (1, 1, 640, 16, 2.0, "fib"),          # integer alpha: the one-sided derivative
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", FRAC_BWD_EDGE)
+def test_bwd_frac_edge_cases(dtype, case):
+    B, H, T, W, alpha, base = case
+    inp = fi.draw((1, B, H, T, 64), seed=61 + T, scale=0.5, dtype=dtype, names=("q", "k", "v", "dO"))
+    _check_frac_bwd(inp, W, [alpha], base, dtype)
+
+
+def test_bwd_frac_training_step_sampled():
+    # the fractional workload's shape, forward + backward; dalpha of two layers in full
+    spec = fi.WORKLOADS["c3f"]
+    alphas = fi.frac_alphas(spec)
+    inp = fi.workload_inputs("c3f", names=("q", "k", "v", "dO"))
+    picks = [(l, b, h) for l in range(spec["Lc"]) for (b, h) in sample_slices(spec["B"], spec["H"], 2)]
+    _check_frac_bwd(inp, spec["W"], alphas, spec["base"], "bf16", layers_full=[0, 15], picks=picks)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bwd_frac_integer_alpha_equals_static_bitwise(dtype):
+    inp = to_dev(fi.draw((2, 2, 2, 700, 64), seed=71, scale=0.5, dtype=dtype,
+                         names=("q", "k", "v", "dO")))
+    o, lse = fa.fwd_frac(inp["q"], inp["k"], inp["v"], 16, [1.0, 3.0])
+    dq, dk, dv, _ = fa.bwd_frac(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], 16, [1.0, 3.0])
+    for c, a in enumerate((1, 3)):
+        sc = fa.Schedule("fixed", "fib", alpha=(a, 1))
+        g = fa.bwd(inp["q"][c], inp["k"][c], inp["v"][c], o[c], lse[c], inp["dO"][c], 16, sc)
+        assert torch.equal(dq[c], g[0]) and torch.equal(dk[c], g[1]) and torch.equal(dv[c], g[2]), a
+
+
+def test_bwd_frac_more_layers_than_one_launch_equals_per_layer_calls():
+    n = 18
+    alphas = [0.55 + 0.083 * l for l in range(n)]
+    inp = to_dev(fi.draw((n, 1, 2, 300, 64), seed=81, scale=0.5, dtype="bf16",
+                         names=("q", "k", "v", "dO")))
+    o, lse = fa.fwd_frac(inp["q"], inp["k"], inp["v"], 8, alphas)
+    dq, dk, dv, da = fa.bwd_frac(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], 8, alphas)
+    for c in range(n):
+        g = fa.bwd_frac(inp["q"][c], inp["k"][c], inp["v"][c], o[c], lse[c], inp["dO"][c], 8,
+                        [alphas[c]])
+        assert torch.equal(dq[c], g[0]) and torch.equal(dk[c], g[1]) and torch.equal(dv[c], g[2])
+        assert torch.equal(da[c:c + 1], g[3]), c
+
+
+def test_bwd_frac_deterministic():
+    spec = fi.WORKLOADS["c3f"]
+    inp = to_dev(fi.workload_inputs("c3f", layers=range(3), B=2, names=("q", "k", "v", "dO")))
+    alphas = fi.frac_alphas(spec)[:3]
+    o, lse = fa.fwd_frac(inp["q"], inp["k"], inp["v"], 64, alphas)
+    a = fa.bwd_frac(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], 64, alphas)
+    b = fa.bwd_frac(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], 64, alphas)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_frac_autograd_wrapper_gives_alpha_gradient():
+    inp = to_dev(fi.draw((2, 1, 2, 400, 64), seed=91, scale=0.5, dtype="bf16",
+                         names=("q", "k", "v", "dO")))
+    alpha = torch.tensor([0.9, 1.45], dtype=torch.float32, requires_grad=True)
+    q, k, v = (inp[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+    o = fa.FibFracAttention.apply(q, k, v, alpha, 16)
+    o.backward(inp["dO"])
+    o2, lse = fa.fwd_frac(inp["q"], inp["k"], inp["v"], 16, [0.9, 1.45])
+    dq, dk, dv, da = fa.bwd_frac(inp["q"], inp["k"], inp["v"], o2, lse, inp["dO"], 16, [0.9, 1.45])
+    assert torch.equal(o.detach(), o2)
+    assert torch.equal(q.grad, dq) and torch.equal(k.grad, dk) and torch.equal(v.grad, dv)
+    assert torch.equal(alpha.grad, da.cpu())
