@@ -143,6 +143,38 @@ def fwd(q, k, v, W: int, tables, scale: float | None = None, n_threads: int = 0)
     return out.reshape(shape), lse.reshape(shape[:-1])
 
 
+def _repeat_kv(x, G: int):
+    """Grouped-query layout: [..., H_kv, T, d] -> [..., H_kv * G, T, d], query head h reading
+    kv head h // G (consecutive query heads share one kv head)."""
+    return np.repeat(np.asarray(x, dtype=np.float64), G, axis=-3)
+
+
+def fwd_gqa(q, k, v, W: int, tables, scale: float | None = None, n_threads: int = 0):
+    """Forward with grouped K/V heads: q [..., H, T, d], k and v [..., H_kv, T, d] with
+    H = G * H_kv. By the definition of sharing, every query head attends its kv head's rows:
+    the multi-head forward over the repeated K/V."""
+    G = _group(q, k)
+    return fwd(q, _repeat_kv(k, G), _repeat_kv(v, G), W, tables, scale, n_threads)
+
+
+def bwd_gqa(q, k, v, dout, W: int, tables, scale: float | None = None, n_threads: int = 0):
+    """Backward with grouped K/V heads: a shared kv row's gradient is the sum of the gradients
+    of its G copies. Returns (dq, dk, dv, out, lse) with dk, dv shaped like k, v."""
+    G = _group(q, k)
+    dq, dk, dv, out, lse = bwd(q, _repeat_kv(k, G), _repeat_kv(v, G), dout, W, tables, scale,
+                               n_threads)
+    shp = np.shape(k)
+    red = lambda a: a.reshape(shp[:-3] + (shp[-3], G) + shp[-2:]).sum(axis=-3)
+    return dq, red(dk), red(dv), out, lse
+
+
+def _group(q, k):
+    H, Hkv = np.shape(q)[-3], np.shape(k)[-3]
+    if Hkv < 1 or H % Hkv or np.shape(q)[:-3] != np.shape(k)[:-3]:
+        raise ValueError("q heads must be a multiple of the kv heads, other dims equal")
+    return H // Hkv
+
+
 def _frac_tables(dist_tables, shape, n_slices):
     per_layer = len(dist_tables) > 0 and isinstance(dist_tables[0], (list, tuple, np.ndarray))
     tabs = [list(map(float, t)) for t in dist_tables] if per_layer else [list(map(float, dist_tables))]
@@ -235,4 +267,5 @@ def bwd(q, k, v, dout, W: int, tables, scale: float | None = None, n_threads: in
 __all__ = ["schedule", "FIB", "POW2", "FIXED", "LINEAR", "COPRIME", "alpha_for_layer",
            "fibonacci_base", "frac_distances", "key_set", "key_set_c", "layer_table",
            "offset_table", "round_half_up", "fwd", "fwd_frac", "bwd", "bwd_frac", "frac_bases",
+           "fwd_gqa", "bwd_gqa",
            "threads", "lib"]
