@@ -6,7 +6,7 @@ backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
 (B=8, H=8, T=1024, d=64), W=64, coprime reassignment (l -> 5l mod 16) of the linear
 stagger alpha 0.5 -> 2.0, bf16, forward + backward.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f|c5f]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f|c5f|c5g]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
@@ -16,7 +16,7 @@ data path); value = all ranks' query tokens / max-over-ranks time.
 c3f / c5f are the fractional-offset (learned-alpha) forward / training step (with the
 gradient of every layer's alpha) on the c3 / c5 shapes; their lines add
 "static_counterpart", the static c3 / c5 step (same shape and alpha range) timed in the
-same process, and the latency ratio.
+same process, and the latency ratio. c5g is the c5 step with 8 query heads sharing 2 kv heads.
 """
 from __future__ import annotations
 
@@ -61,6 +61,9 @@ ALGO_BYTES = {
     "bwd_dkdv_frac_simt": 4 * 256 + 8 + 2 * 256,
     "dalpha_reduce": 4,                         # the dalpha partials in
 }
+# Rows per query token of each kernel that are k/v-shaped (k, v in; dk, dv out).
+KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_simt_bf16": 2, "bwd_dq_tc": 2,
+           "bwd_dkdv_tc": 4, "bwd_dq_simt": 2, "bwd_dkdv_simt": 4}
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
@@ -72,13 +75,24 @@ KERNEL_SRC = {
 }
 
 
+def algo_bytes(kernel, spec):
+    """ALGO_BYTES per query token, with the k/v rows (and dk/dv) of a grouped-query workload
+    shared by H / Hkv query heads."""
+    b = ALGO_BYTES.get(kernel, 0)
+    G = spec["H"] // spec.get("Hkv", spec["H"])
+    if G > 1 and kernel in KV_ROWS:
+        row = 256 if "f32" in kernel or kernel.endswith("_simt") else 128
+        b -= KV_ROWS[kernel] * row * (1 - 1 / G)
+    return b
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c5",
-                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f"])
+                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f", "c5g"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -225,7 +239,8 @@ def run_ours(a, spec, world, rank, local):
     o = torch.empty_like(d_in["q"])
     lse = torch.empty(d_in["q"].shape[:-1], dtype=torch.float32, device=dev)
     if train:
-        dq, dk, dv = (torch.empty_like(d_in["q"]) for _ in range(3))
+        dq = torch.empty_like(d_in["q"])
+        dk, dv = torch.empty_like(d_in["k"]), torch.empty_like(d_in["v"])
         need = (fa.bwd_frac_workspace_size(d_in["q"], W, alphas, spec["base"]) if frac
                 else fa.bwd_workspace_size(d_in["q"], W, sched))
         ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
@@ -302,7 +317,7 @@ def run_ours(a, spec, world, rank, local):
     if dom:
         ms, n = per_kernel[dom]
         per_launch_tokens = tokens(spec) / max(1, math.ceil(spec["Lc"] / 16))
-        algo = ALGO_BYTES.get(dom, 0) * per_launch_tokens
+        algo = algo_bytes(dom, spec) * per_launch_tokens
         avg_s = ms / n / 1e3
         achieved = algo / avg_s / 1e9
         traffic_pt = committed_traffic(dom, a.workload)
@@ -390,7 +405,7 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None):
     outs_host = {}
     shapes = {"o": inp["q"].shape, "lse": inp["q"].shape[:-1]}
     if train:
-        shapes.update(dq=inp["q"].shape, dk=inp["q"].shape, dv=inp["q"].shape)
+        shapes.update(dq=inp["q"].shape, dk=inp["k"].shape, dv=inp["v"].shape)
         if alphas is not None:
             shapes["dalpha"] = (spec["Lc"],)
     for n, shp in shapes.items():
@@ -469,7 +484,11 @@ def oracle_sample(spec, n_slices, n_threads=0):
         picks = per_layer[l]
         if not picks:
             continue
-        g = lambda n: np.stack([f64(inp[n][li, b, h]) for b, h in picks])
+        # grouped-query workloads: query head h reads kv head h // G (the oracle's grouped
+        # form runs the multi-head oracle on the repeated kv rows, as here)
+        G = spec["H"] // spec.get("Hkv", spec["H"])
+        g = lambda n: np.stack([f64(inp[n][li, b, h // G if n in ("k", "v") else h])
+                                for b, h in picks])
         if alphas is not None:
             dists = oracle.frac_distances(alphas[l], spec["base"], W, T)
             if "bwd" in spec["passes"]:

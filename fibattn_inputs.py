@@ -18,12 +18,13 @@ import torch
 DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
-def draw(shape, seed: int, scale: float, dtype: str = "bf16", names=("q", "k", "v")):
-    """Return a dict name -> CPU tensor of `shape`, drawn in `names` order."""
+def draw(shape, seed: int, scale: float, dtype: str = "bf16", names=("q", "k", "v"), shapes=None):
+    """Return a dict name -> CPU tensor of `shape` (or shapes[name]), drawn in `names` order."""
     g = torch.Generator("cpu").manual_seed(int(seed))
     out = {}
     for name in names:
-        x = torch.randn(tuple(shape), generator=g, dtype=torch.float32) * float(scale)
+        shp = (shapes or {}).get(name, shape)
+        x = torch.randn(tuple(shp), generator=g, dtype=torch.float32) * float(scale)
         out[name] = x.to(DTYPES[dtype]).contiguous()
     return out
 
@@ -79,6 +80,12 @@ WORKLOADS = {
                W=64, seed=4, scale=0.125, names=("q", "k", "v", "dO"), passes=("fwd", "bwd"),
                sched=dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
                           n_layers=16, coprime_c=5)),
+    "c5g": dict(desc="training step fwd+bwd, 16 layers, grouped-query (8 query heads sharing 2 "
+                     "kv heads), coprime (5l mod 16) of the linear stagger 0.5->2.0, bf16",
+                dtype="bf16", Lc=16, B=8, H=8, Hkv=2, T=1024, d=64, W=64, seed=4, scale=0.125,
+                names=("q", "k", "v", "dO"), passes=("fwd", "bwd"),
+                sched=dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
+                           n_layers=16, coprime_c=5)),
     "c3f": dict(desc="16-layer stack, fractional (learned-style) alphas in [0.5, 2.0], bf16",
                 dtype="bf16", Lc=16, B=8, H=8, T=1024, d=64, W=64, seed="per_layer:2",
                 scale=0.125, names=("q", "k", "v"), passes=("fwd",), base="fib",
@@ -112,13 +119,15 @@ def workload_inputs(name: str, layers=None, **override):
     """CPU tensors [Lc, B, H, T, d] of a named workload (optionally only `layers`)."""
     spec = dict(WORKLOADS[name], **override)
     shape = (spec["B"], spec["H"], spec["T"], spec["d"])
+    # grouped-query workloads: k and v have Hkv heads
+    kv = {n: (spec["B"], spec["Hkv"], spec["T"], spec["d"]) for n in ("k", "v")} if "Hkv" in spec else None
     seed = seed_of(spec)
     Lc = spec["Lc"]
     if layers is None:
         layers = list(range(Lc))
     if callable(seed):
-        per = [draw(shape, seed(l), spec["scale"], spec["dtype"], spec["names"]) for l in layers]
+        per = [draw(shape, seed(l), spec["scale"], spec["dtype"], spec["names"], kv) for l in layers]
     else:
-        one = draw(shape, seed, spec["scale"], spec["dtype"], spec["names"])
+        one = draw(shape, seed, spec["scale"], spec["dtype"], spec["names"], kv)
         per = [{n: t.clone() for n, t in one.items()} for _ in layers]
     return {n: torch.stack([p[n] for p in per]).contiguous() for n in spec["names"]}

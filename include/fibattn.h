@@ -129,6 +129,32 @@ FIBATTN_API fibattn_status fibattn_fwd(const void* q, const void* k, const void*
                            int32_t n_layers_call, void* cuda_stream);
 
 /*
+ * Grouped-query forms of fibattn_fwd / fibattn_bwd (GQA; MQA at H_kv = 1): H query heads
+ * share H_kv key/value heads, H a multiple of H_kv, query head h of batch b reading kv head
+ * h / (H / H_kv) of batch b. q, o, dO, dq, lse are [Lc][B][H][T](d) as above; k, v, dk, dv
+ * are [Lc][B][H_kv][T][d]. dk, dv of a kv row sum the contributions of every query head that
+ * reads it (computed by the one thread block that owns the row: no atomics). The workspace is
+ * fibattn_bwd_workspace_size(B, H, ...) (it is indexed by query rows). H_kv = H is exactly
+ * fibattn_fwd / fibattn_bwd. Errors as those, plus INVALID_ARG when H_kv < 1 or H % H_kv != 0.
+ * (This shape is not on the pages, which study 8 heads of 64; it is the head sharing of larger
+ * models.)
+ */
+FIBATTN_API fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void* o,
+                                           float* lse, int32_t B, int32_t H, int32_t H_kv,
+                                           int32_t T, int32_t d, int32_t dtype, int32_t W,
+                                           float scale, const fibattn_schedule* sched,
+                                           int32_t layer0, int32_t n_layers_call,
+                                           void* cuda_stream);
+FIBATTN_API fibattn_status fibattn_bwd_gqa(const void* q, const void* k, const void* v,
+                                           const void* o, const float* lse, const void* dO,
+                                           void* dq, void* dk, void* dv, void* workspace,
+                                           uint64_t workspace_bytes, int32_t B, int32_t H,
+                                           int32_t H_kv, int32_t T, int32_t d, int32_t dtype,
+                                           int32_t W, float scale, const fibattn_schedule* sched,
+                                           int32_t layer0, int32_t n_layers_call,
+                                           void* cuda_stream);
+
+/*
  * Fractional-offset table of one real alpha: the learned-alpha variant of the pages
  * (Metodologia / Arquitetura, "Implementacao": keys and values are linearly interpolated
  * between rows so that the gradient reaches alpha when alpha * F is not an integer).

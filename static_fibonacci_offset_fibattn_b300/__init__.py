@@ -101,6 +101,8 @@ def lib():
         L.fibattn_offsets_device.argtypes = [sp, i32, i32, i32, i32, vp, vp, vp]
         L.fibattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, sp, i32,
                                   i32, vp]
+        L.fibattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                      sp, i32, i32, vp]
         u64 = ctypes.c_uint64
         i64 = ctypes.c_int64
         L.fibattn_frac_offsets.argtypes = [f32, i32, i64, i32, i32, ctypes.POINTER(i32),
@@ -116,6 +118,8 @@ def lib():
                                                  ctypes.POINTER(u64)]
         L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32, i32,
                                   i32, i32, f32, sp, i32, i32, vp]
+        L.fibattn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
+                                      i32, i32, i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_keyset_debug.argtypes = [sp, i32, i32, i32, vp, vp]
@@ -136,6 +140,7 @@ def lib():
                      "fibattn_bwd_workspace_size",
                      "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error",
                      "fibattn_frac_offsets", "fibattn_fwd_frac", "fibattn_bwd_frac",
+                     "fibattn_fwd_gqa", "fibattn_bwd_gqa",
                      "fibattn_bwd_frac_workspace_size"):
             getattr(L, name).restype = i32
         _lib = L
@@ -198,11 +203,26 @@ def _shape(q: torch.Tensor):
     return Lc, B, H, T, d
 
 
+def _kv_heads(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
+    """H_kv of a grouped-query call: k and v share a shape that differs from q's only in the
+    head dim (-3), which divides q's."""
+    if k.shape != v.shape or k.dim() != q.dim() or k.dim() < 4:
+        raise ValueError("k and v must share a shape with q's rank")
+    if k.shape[:-3] != q.shape[:-3] or k.shape[-2:] != q.shape[-2:]:
+        raise ValueError("k/v may differ from q only in the head dim")
+    H, Hkv = q.shape[-3], k.shape[-3]
+    if Hkv < 1 or H % Hkv:
+        raise ValueError("q heads must be a multiple of the kv heads")
+    return Hkv
+
+
 def _check_tensors(ref: torch.Tensor, *ts):
     if not ref.is_cuda:
         raise ValueError("tensors must be on a CUDA device (there is no CPU path)")
     if ref.dtype not in _DTYPES:
         raise ValueError("dtype must be float32 or bfloat16")
+    if not ref.is_contiguous():
+        raise ValueError("tensors must be contiguous")
     for t in ts:
         if t.device != ref.device or t.dtype != ref.dtype or t.shape != ref.shape:
             raise ValueError("q/k/v/o/dO/dq/dk/dv must share device, dtype and shape")
@@ -213,17 +233,22 @@ def _check_tensors(ref: torch.Tensor, *ts):
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, sched: Schedule,
         layer0: int = 0, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
         lse: Optional[torch.Tensor] = None):
-    """Sparse attention forward; returns (o, lse). q/k/v: [Lc,B,H,T,64] or [B,H,T,64]."""
+    """Sparse attention forward; returns (o, lse). q/k/v: [Lc,B,H,T,64] or [B,H,T,64]; k and
+    v may have fewer heads than q (grouped-query: query head h reads kv head h // (H/H_kv))."""
     Lc, B, H, T, d = _shape(q)
+    Hkv = _kv_heads(q, k, v)
     o = torch.empty_like(q) if out is None else out
-    _check_tensors(q, k, v, o)
+    _check_tensors(q, o)
+    _check_tensors(k, v)
+    if k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("q/k/v must share device and dtype")
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     s = sched.to_c()
-    st = lib().fibattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, d,
-                           _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0, Lc,
-                           _stream(q))
-    _check(st, "fibattn_fwd")
+    st = lib().fibattn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, T, d,
+                               _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0,
+                               Lc, _stream(q))
+    _check(st, "fibattn_fwd_gqa")
     return o, lse
 
 
@@ -320,25 +345,30 @@ def bwd_workspace_size(q: torch.Tensor, W: int, sched: Schedule, layer0: int = 0
 
 def bwd(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
         scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None):
-    """Sparse attention backward from the saved forward; returns (dq, dk, dv).
+    """Sparse attention backward from the saved forward; returns (dq, dk, dv) (dk, dv shaped
+    like k, v: grouped-query calls sum each kv row over the heads that read it).
     workspace: optional uint8 device tensor of at least bwd_workspace_size() bytes."""
     Lc, B, H, T, d = _shape(q)
+    Hkv = _kv_heads(q, k, v)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    _check_tensors(q, k, v, o, dO, dq, dk, dv)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    _check_tensors(q, o, dO, dq)
+    _check_tensors(k, v, dk, dv)
+    if k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("q/k/v must share device and dtype")
     need = bwd_workspace_size(q, W, sched, layer0)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if workspace.device != q.device or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on q's device")
     s = sched.to_c()
-    st = lib().fibattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
-                           _ptr(dk), _ptr(dv), _ptr(workspace),
-                           workspace.numel() * workspace.element_size(), B, H, T, d,
-                           _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0, Lc,
-                           _stream(q))
-    _check(st, "fibattn_bwd")
+    st = lib().fibattn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                               _ptr(dk), _ptr(dv), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), B, H, Hkv, T, d,
+                               _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0,
+                               Lc, _stream(q))
+    _check(st, "fibattn_bwd_gqa")
     return dq, dk, dv
 
 

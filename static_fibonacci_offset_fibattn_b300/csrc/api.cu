@@ -175,28 +175,31 @@ fibattn_status fibattn_keyset_debug(const fibattn_schedule* sched, int32_t layer
     return launch_keyset(t, W, T, d_mask, as_stream(cuda_stream));
 }
 
-fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                           int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
-                           float scale, const fibattn_schedule* sched, int32_t layer0,
-                           int32_t n_layers_call, void* cuda_stream) {
+fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int32_t B, int32_t H, int32_t H_kv, int32_t T, int32_t d,
+                               int32_t dtype, int32_t W, float scale, const fibattn_schedule* sched,
+                               int32_t layer0, int32_t n_layers_call, void* cuda_stream) {
     if (!q || !k || !v || !o || !lse) return FIBATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FIBATTN_ERR_INVALID_ARG;
+    if (H_kv < 1 || H < 1 || H % H_kv != 0) return FIBATTN_ERR_INVALID_ARG;
     fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (st != FIBATTN_OK) return st;
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
     const int64_t per_layer = (int64_t)B * H * T;
+    const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv};
         const size_t off = (size_t)c * per_layer * d * es;
+        const size_t koff = (size_t)c * per_layer_kv * d * es;
         const char* qc = (const char*)q + off;
-        const char* kc = (const char*)k + off;
-        const char* vc = (const char*)v + off;
+        const char* kc = (const char*)k + koff;
+        const char* vc = (const char*)v + koff;
         char* oc = (char*)o + off;
         float* lc = lse + (size_t)c * per_layer;
         if (dtype == FIBATTN_F32)
@@ -207,6 +210,14 @@ fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o,
         if (st != FIBATTN_OK) return st;
     }
     return FIBATTN_OK;
+}
+
+fibattn_status fibattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                           float scale, const fibattn_schedule* sched, int32_t layer0,
+                           int32_t n_layers_call, void* cuda_stream) {
+    return fibattn_fwd_gqa(q, k, v, o, lse, B, H, H, T, d, dtype, W, scale, sched, layer0,
+                           n_layers_call, cuda_stream);
 }
 
 fibattn_status fibattn_frac_offsets(float alpha, int32_t base, int64_t base_max, int32_t W,
@@ -262,17 +273,18 @@ fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int32_t T, int32
     return FIBATTN_OK;
 }
 
-fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
-                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                           void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
-                           int32_t T, int32_t d, int32_t dtype, int32_t W, float scale,
-                           const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call,
-                           void* cuda_stream) {
+fibattn_status fibattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
+                               int32_t H_kv, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                               float scale, const fibattn_schedule* sched, int32_t layer0,
+                               int32_t n_layers_call, void* cuda_stream) {
     const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return FIBATTN_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return FIBATTN_ERR_INVALID_ARG;
+    if (H_kv < 1 || H < 1 || H % H_kv != 0) return FIBATTN_ERR_INVALID_ARG;
     fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (st != FIBATTN_OK) return st;
     const BwdWorkspace ws = bwd_workspace(B, H, T, dtype, W, sched, layer0, n_layers_call);
@@ -283,30 +295,32 @@ fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const vo
     const int64_t per_layer_pad = (int64_t)B * H * ws.T_pad;
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
     const int64_t per_layer = (int64_t)B * H * T;
+    const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv};
         const size_t off = (size_t)c * per_layer * d * es;
+        const size_t koff = (size_t)c * per_layer_kv * d * es;
         const size_t loff = (size_t)c * per_layer;
         if (dtype == FIBATTN_F32) {
             st = launch_bwd_simt_f32((const float*)((const char*)q + off),
-                                     (const float*)((const char*)k + off),
-                                     (const float*)((const char*)v + off),
+                                     (const float*)((const char*)k + koff),
+                                     (const float*)((const char*)v + koff),
                                      (const float*)((const char*)o + off), lse + loff,
                                      (const float*)((const char*)dO + off),
-                                     (float*)((char*)dq + off), (float*)((char*)dk + off),
-                                     (float*)((char*)dv + off), delta + loff, sh, t,
+                                     (float*)((char*)dq + off), (float*)((char*)dk + koff),
+                                     (float*)((char*)dv + koff), delta + loff, sh, t,
                                      as_stream(cuda_stream));
         } else {
             const size_t poff = (size_t)c * per_layer_pad;
-            st = launch_bwd_tc_bf16((const char*)q + off, (const char*)k + off,
-                                    (const char*)v + off, (const char*)o + off, lse + loff,
-                                    (const char*)dO + off, (char*)dq + off, (char*)dk + off,
-                                    (char*)dv + off, delta + poff, lse2 + poff,
+            st = launch_bwd_tc_bf16((const char*)q + off, (const char*)k + koff,
+                                    (const char*)v + koff, (const char*)o + off, lse + loff,
+                                    (const char*)dO + off, (char*)dq + off, (char*)dk + koff,
+                                    (char*)dv + koff, delta + poff, lse2 + poff,
                                     pds + poff * ws.n_max, ws.n_max, sh, t,
                                     as_stream(cuda_stream));
         }
@@ -315,6 +329,15 @@ fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const vo
     return FIBATTN_OK;
 }
 
+fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
+                           int32_t T, int32_t d, int32_t dtype, int32_t W, float scale,
+                           const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call,
+                           void* cuda_stream) {
+    return fibattn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, H, H,
+                           T, d, dtype, W, scale, sched, layer0, n_layers_call, cuda_stream);
+}
 fibattn_status fibattn_bwd_frac_workspace_size(int32_t B, int32_t H, int32_t T, int32_t d,
                                                int32_t dtype, int32_t W, int32_t base,
                                                int64_t base_max, const float* alphas,

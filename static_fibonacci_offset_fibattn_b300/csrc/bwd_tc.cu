@@ -74,7 +74,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // inputs, 3D {64, T, slices}, box {64, 64, 1}
-    CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs
+    CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs (K, V, dK, dV over the kv slices)
     CUtensorMap tm_o;                     // forward output (for D)
     const float* lse;                     // [slices][T]
     float* delta;                         // workspace: D [slices][T_pad]
@@ -82,8 +82,10 @@ struct BwdParams {
     uint32_t* pds;                        // workspace: (P, dS) bf16 pairs [slices][n_max][T_pad],
                                           // entry k of key row j = the pair (j + o_k, j)
     int32_t* err;
-    int64_t slices_per_layer;
-    uint32_t slices_per_layer32;          // the same, for the persistent tile walk
+    int64_t slices_per_layer;             // query slices per layer (B * H)
+    uint32_t group;                       // query heads per kv head
+    uint32_t slices_per_layer_kv32;       // kv slices per layer (B * H / group), for the
+                                          // key owner's persistent tile walk
     uint32_t total_tiles;                 // tiles of the launch (<= INT32_MAX)
     int32_t T, W;
     int32_t T_pad;                        // T rounded up to 4: rows of the workspace arrays
@@ -157,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
     const int tile = blockIdx.x % p.tiles_per_slice;
     const int64_t zl = (int64_t)layer * p.slices_per_layer + blockIdx.x / p.tiles_per_slice;
     const int32_t z = (int32_t)zl;
+    // the kv slice: query head h of batch b reads kv head h / group
+    const int32_t zk = (int32_t)((int64_t)layer * p.slices_per_layer_kv32 +
+                                 (uint32_t)(blockIdx.x / p.tiles_per_slice) / p.group);
     const int32_t T = p.T, W = p.W;
     const int32_t i0 = tile * kRows;
 
@@ -206,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                 const int s = c & 1;
                 const int32_t y = (c_lo + c) * kChunk;
                 mbar_arrive_expect_tx(B_KV(s), 2 * kChunkBytes);
-                tma_load_3d(sbase + kOffK + s * kChunkBytes, &p.tm_k, B_KV(s), 0, y, z);
-                tma_load_3d(sbase + kOffV + s * kChunkBytes, &p.tm_v, B_KV(s), 0, y, z);
+                tma_load_3d(sbase + kOffK + s * kChunkBytes, &p.tm_k, B_KV(s), 0, y, zk);
+                tma_load_3d(sbase + kOffV + s * kChunkBytes, &p.tm_v, B_KV(s), 0, y, zk);
             };
             load_chunk(0);
             if (n_chunks > 1) load_chunk(1);
@@ -266,11 +271,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                     // fractional mode: every item also carries the 8 rows after its tile (the
                     // derivative in d needs row lo + 1 even where w = 0)
                     mbar_arrive_expect_tx(B_FULL(s), kSlot);
-                    tma_load_3d(dst, map, B_FULL(s), 0, y, z);
-                    tma_load_3d(dst + kChunkBytes, map, B_FULL(s), 0, y + kChunk, z);
+                    tma_load_3d(dst, map, B_FULL(s), 0, y, zk);
+                    tma_load_3d(dst + kChunkBytes, map, B_FULL(s), 0, y + kChunk, zk);
                     if constexpr (kFrac)
                         tma_load_3d(dst + kTileBytes, h == 0 ? &p.tm_k8 : &p.tm_v8, B_FULL(s), 0,
-                                    y + kRows, z);
+                                    y + kRows, zk);
                 }
             }
             for (uint32_t q = seq > 2 ? seq - 2 : 0; q < seq; ++q)
@@ -565,6 +570,11 @@ struct Plan {
     }
 };
 
+// Launch query slice of query head hq (of the `group` heads that read the tile's kv head).
+__device__ __forceinline__ int64_t query_slice(const BwdParams& p, const ring::Tile& tl, int hq) {
+    return (int64_t)tl.layer * p.slices_per_layer + (int64_t)tl.s * p.group + hq;
+}
+
 __device__ __forceinline__ Plan make_plan(const BwdParams& p, int layer, int32_t j0) {
     Plan pl;
     pl.j0 = j0;
@@ -634,12 +644,16 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             uint32_t seq = 0;
             const int32_t Tp = p.T_pad;
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
-                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer32);
+                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer_kv32);
                 const Plan pl = make_plan(p, tl.layer, tl.row0);
-                const int32_t z = (int32_t)tl.zl;
-                const float* l2_row = p.lse2 + tl.zl * Tp;
-                const float* d_row = p.delta + tl.zl * Tp;
+                const int32_t z = (int32_t)tl.zl;  // the kv slice of the tile
+                for (int hq = 0; hq < (int)p.group; ++hq)
                 for (int g = 0; g < pl.n_groups; ++g) {
+                    // the query slice: head hq of the heads that read this kv head
+                    const int64_t zq64 = query_slice(p, tl, hq);
+                    const int32_t zq = (int32_t)zq64;
+                    const float* l2_row = p.lse2 + zq64 * Tp;
+                    const float* d_row = p.delta + zq64 * Tp;
                     // K and V tiles
                     for (int h = 0; h < 2; ++h, ++seq) {
                         if (!rg.acquire(seq, aborted, p.err)) continue;
@@ -654,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                         const int32_t qb = (pl.q_lo + g * kMaxGroupChunks + c) * kChunk;
                         const uint32_t side_bytes = 4u * (uint32_t)min(kChunk, Tp - qb);
                         mbar_arrive_expect_tx(rg.full(seq), 2 * kChunkBytes + 2 * side_bytes);
-                        tma_load_3d(rg.addr(seq), &p.tm_q, rg.full(seq), 0, qb, z);
-                        tma_load_3d(rg.addr(seq) + kChunkBytes, &p.tm_do, rg.full(seq), 0, qb, z);
+                        tma_load_3d(rg.addr(seq), &p.tm_q, rg.full(seq), 0, qb, zq);
+                        tma_load_3d(rg.addr(seq) + kChunkBytes, &p.tm_do, rg.full(seq), 0, qb, zq);
                         bulk_load(side_addr(seq), l2_row + qb, side_bytes, rg.full(seq));
                         bulk_load(side_addr(seq) + 256, d_row + qb, side_bytes, rg.full(seq));
                     }
@@ -669,7 +683,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                 const uint32_t pskip = kFrac ? 4u * (uint32_t)(pfirst - (pl.j0 - 4)) : 0u;
                 const uint32_t pair_bytes =
                     4u * (uint32_t)min(kRows + (int32_t)(kFrac ? 4 : 0) - (int32_t)(pskip / 4u), Tp - pfirst);
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < 2; ++h)
+                for (int hq = 0; hq < (int)p.group; ++hq) {
+                    const int32_t zq = (int32_t)query_slice(p, tl, hq);
                     for (int k = 0; k < pl.n_act; ++k, ++seq) {
                         if (!rg.acquire(seq, aborted, p.err)) continue;
                         const int32_t y = pl.j0 + offs[k];
@@ -677,14 +693,14 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                         bool pre = false;
                         if constexpr (kFrac) pre = p.w[tl.layer][k] != 0.f;
                         mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + (pre ? 1024u : 0u) + pair_bytes);
-                        tma_load_3d(rg.addr(seq) + kPre, map, rg.full(seq), 0, y, z);
-                        tma_load_3d(rg.addr(seq) + kPre + kChunkBytes, map, rg.full(seq), 0, y + kChunk, z);
+                        tma_load_3d(rg.addr(seq) + kPre, map, rg.full(seq), 0, y, zq);
+                        tma_load_3d(rg.addr(seq) + kPre + kChunkBytes, map, rg.full(seq), 0, y + kChunk, zq);
                         if constexpr (kFrac) {
                             if (pre)
                                 tma_load_3d(rg.addr(seq), h == 0 ? &p.tm_q8 : &p.tm_do8, rg.full(seq), 0,
-                                            y - 8, z);
+                                            y - 8, zq);
                         }
-                        bulk_load(side_addr(seq) + pskip, p.pds + ((int64_t)z * p.n_max + k) * Tp + pfirst,
+                        bulk_load(side_addr(seq) + pskip, p.pds + ((int64_t)zq * p.n_max + k) * Tp + pfirst,
                                   pair_bytes, rg.full(seq));
                     }
                 }
@@ -708,10 +724,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             // descriptors of shared address sbase; an operand at sbase + x adds x >> 4
             const uint64_t dkm = sdesc_sw128(sbase, 16, 1024), dmn = sdesc_sw128(sbase, 0, 1024);
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x, ++tcount) {
-                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer32);
+                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer_kv32);
                 const Plan pl = make_plan(p, tl.layer, tl.row0);
                 if (tcount > 0) mbar_wait(B_T, (tcount - 1) & 1, aborted, p.err);
-                int cg = 0;  // chunk index within the tile
+                int cg = 0;  // chunk index within the tile (over every query head)
+                for (int hq = 0; hq < (int)p.group; ++hq)
                 for (int g = 0; g < pl.n_groups; ++g) {
                     const int nch = pl.nch(g);
                     const uint32_t kseq = seq, vseq = seq + 1, bseq = seq + 2;
@@ -754,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                         rg.release_mma(bseq + c);
                     }
                 }
-                seq += 2 * pl.n_act + 2;
+                seq += 2 * p.group * pl.n_act + 2;
             }
             if (mcount > 0) mbar_wait(B_M, (mcount - 1) & 1, aborted, p.err);
         }
@@ -766,14 +783,16 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
         const float sl2 = p.scale_log2;
         uint32_t seq = 0, mcount = 0;
         for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
-            const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer32);
+            const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer_kv32);
             const Plan pl = make_plan(p, tl.layer, tl.row0);
             const int32_t j0 = pl.j0;
             const int32_t j = j0 + r;
             const bool row_ok = j < T;
             const int32_t* offs = p.tabs.off[tl.layer];
 
-            // ---- band: P^T and dS^T of this thread's 32 query columns, 16 at a time
+            // ---- band: P^T and dS^T of this thread's 32 query columns, 16 at a time (for every
+            // query head reading this kv head)
+            for (int hq = 0; hq < (int)p.group; ++hq)
             for (int g = 0; g < pl.n_groups; ++g) {
                 const int nch = pl.nch(g);
                 const uint32_t bseq = seq + 2;
@@ -832,7 +851,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
 #pragma unroll
                 for (int c = 0; c < 32; ++c) acc[c] = 0.f;
 #pragma unroll 1
-                for (int k = 0; k < pl.n_act; ++k) {
+                for (int e = 0; e < (int)p.group * pl.n_act; ++e) {
+                    const int k = e % pl.n_act;  // the offset (the query head is e / n_act)
                     rg.wait_full(seq, aborted, p.err);
                     if constexpr (kFrac) {
                         // key j is row lo of query j + c (weight 1 - w: pair of key row j) and
@@ -994,6 +1014,7 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
                           float* galpha, cudaStream_t st) {
     const int64_t slices = sh.slices_per_layer * sh.n_layers;
     if (slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    const int64_t slices_kv = slices / sh.group;
     const int32_t tiles = (sh.T + kRows - 1) / kRows;
     const int64_t gx = (int64_t)tiles * sh.slices_per_layer;
     if (gx > 0x7fffffff || (int64_t)tiles * slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
@@ -1005,14 +1026,16 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
     const void* bases[8] = {q, k, v, dO, dq, dk, dv, o};
     CUtensorMap* maps[8] = {&P.tm_q, &P.tm_k, &P.tm_v, &P.tm_do, &P.tm_dq, &P.tm_dk, &P.tm_dv, &P.tm_o};
     for (int m = 0; m < 8; ++m) {
-        const int r = make_bf16_rows_map(maps[m], bases[m], slices, sh.T);
+        // k, v, dk, dv (maps 1, 2, 5, 6) over the kv slices
+        const bool kvmap = m == 1 || m == 2 || m == 5 || m == 6;
+        const int r = make_bf16_rows_map(maps[m], bases[m], kvmap ? slices_kv : slices, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (bwd)");
     }
     if constexpr (kFrac) {
         const void* b8[4] = {k, v, q, dO};
         CUtensorMap* m8[4] = {&P.tm_k8, &P.tm_v8, &P.tm_q8, &P.tm_do8};
         for (int m = 0; m < 4; ++m) {
-            const int r = make_bf16_rows8_map(m8[m], b8[m], slices, sh.T);
+            const int r = make_bf16_rows8_map(m8[m], b8[m], m < 2 ? slices_kv : slices, sh.T);
             if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (bwd, 8-row box)");
         }
         P.galpha = galpha;
@@ -1027,8 +1050,9 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
     P.lse2 = lse2;
     P.pds = pds;
     P.slices_per_layer = sh.slices_per_layer;
-    P.slices_per_layer32 = (uint32_t)sh.slices_per_layer;
-    P.total_tiles = (uint32_t)((int64_t)tiles * slices);
+    P.group = (uint32_t)sh.group;
+    P.slices_per_layer_kv32 = (uint32_t)(sh.slices_per_layer / sh.group);
+    P.total_tiles = (uint32_t)((int64_t)tiles * slices_kv);  // the key owner walks kv tiles
     P.T = sh.T;
     P.W = sh.W;
     P.T_pad = (sh.T + 3) & ~3;

@@ -83,9 +83,12 @@ __host__ __device__ constexpr uint32_t smem_alloc() { return tmem_slot_off<kFrac
 
 struct FwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3D {64, T, slices}, box {64, 64, 1}, 128B swizzle
+                                         // (tm_k, tm_v over the kv slices)
     float* lse;
     int32_t* err;
     uint32_t slices_per_layer;
+    uint32_t group;             // query heads per kv head (1: one kv head per query head)
+    uint32_t slices_per_layer_kv;  // slices_per_layer / group
     uint32_t total_tiles;       // <= INT32_MAX
     int32_t T, W;
     int32_t tiles_per_slice;
@@ -190,6 +193,9 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                 const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer);
                 const Plan pl = make_plan(p, tl.layer, tl.row0);
                 const int32_t z = (int32_t)tl.zl;
+                // the kv slice: query head h of batch b reads kv head h / group
+                const int32_t zk = (int32_t)((int64_t)tl.layer * p.slices_per_layer_kv +
+                                             (uint32_t)tl.s / p.group);
                 // band: per group a copy of Q, its K chunks, then its V chunks (two per slot)
                 for (int g = 0; g < pl.n_groups; ++g) {
                     if (rg.acquire(seq, aborted, p.err)) {
@@ -206,9 +212,9 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                             const int32_t y = (pl.c_lo + g * kMaxGroupChunks + c) * kChunk;
                             if (!rg.acquire(seq, aborted, p.err)) continue;
                             mbar_arrive_expect_tx(rg.full(seq), n2 * kChunkBytes);
-                            tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, z);
+                            tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, zk);
                             if (n2 == 2)
-                                tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, z);
+                                tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, zk);
                         }
                     }
                 }
@@ -222,12 +228,12 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                         const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
                         if (!rg.acquire(seq, aborted, p.err)) continue;
                         mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + (side ? 1024u : 0u));
-                        tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, z);
-                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, z);
+                        tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, zk);
+                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, zk);
                         if constexpr (kFrac) {
                             if (side)
                                 tma_load_3d(rg.addr(seq) + ring::kSlotBytes, h == 0 ? &p.tm_k8 : &p.tm_v8,
-                                            rg.full(seq), 0, y + kRows, z);
+                                            rg.full(seq), 0, y + kRows, zk);
                         }
                     }
                 }
@@ -554,21 +560,24 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
     // thread (a fresh thread may have none), which the tensor-map encoding below needs
     P.err = device_error_word();
     if (!P.err) return cuda_fail(-1, "cudaGetSymbolAddress (error word)");
+    const int64_t slices_kv = slices / sh.group;
     const void* bases[4] = {q, k, v, o};
     CUtensorMap* maps[4] = {&P.tm_q, &P.tm_k, &P.tm_v, &P.tm_o};
     for (int m = 0; m < 4; ++m) {
-        const int r = make_bf16_rows_map(maps[m], bases[m], slices, sh.T);
+        const int r = make_bf16_rows_map(maps[m], bases[m], (m == 1 || m == 2) ? slices_kv : slices, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (fwd)");
     }
     if constexpr (kFrac) {
-        int r = make_bf16_rows8_map(&P.tm_k8, k, slices, sh.T);
-        if (r == 0) r = make_bf16_rows8_map(&P.tm_v8, v, slices, sh.T);
+        int r = make_bf16_rows8_map(&P.tm_k8, k, slices_kv, sh.T);
+        if (r == 0) r = make_bf16_rows8_map(&P.tm_v8, v, slices_kv, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (fwd, 8-row box)");
         for (int l = 0; l < kMaxLayersPerLaunch; ++l)
             for (int e = 0; e < kMaxOffsets; ++e) P.w[l][e] = w[l][e];
     }
     P.lse = lse;
     P.slices_per_layer = (uint32_t)sh.slices_per_layer;
+    P.group = (uint32_t)sh.group;
+    P.slices_per_layer_kv = (uint32_t)(sh.slices_per_layer / sh.group);
     P.total_tiles = (uint32_t)((int64_t)tiles * slices);
     P.T = sh.T;
     P.W = sh.W;

@@ -87,11 +87,14 @@ fibattn_status launch_keyset(const OffsetTables& t, int32_t W, int32_t T, uint32
                              cudaStream_t st);
 
 struct AttnShape {
-    int64_t slices_per_layer;  // B * H
+    int64_t slices_per_layer;  // B * H (query heads)
     int32_t T;
     int32_t W;
     float scale;
     int32_t n_layers;          // layers in this launch
+    int32_t group = 1;         // query heads per kv head: K/V (and dK/dV) have
+                               // slices_per_layer / group slices per layer, query head h of
+                               // batch b reading kv head h / group of batch b
 };
 
 fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o,

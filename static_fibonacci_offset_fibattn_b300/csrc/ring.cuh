@@ -26,7 +26,8 @@ constexpr uint32_t kSlotBytes = 16384;  // 128 rows x 128 bytes (64 bf16)
 
 struct Tile {
     int32_t layer;   // launch layer
-    int64_t zl;      // launch slice (layer * slices_per_layer + slice)
+    int64_t zl;      // launch slice (layer * slices_per_layer + s)
+    int32_t s;       // slice within the layer (b * heads + h)
     int32_t row0;    // first row of the tile in its slice
 };
 
@@ -38,6 +39,7 @@ __device__ __forceinline__ Tile tile_of(uint32_t idx, uint32_t tiles_per_slice, 
     const uint32_t rem = idx - (uint32_t)t.layer * per_layer;
     const uint32_t s = rem / tiles_per_slice;
     t.zl = (int64_t)t.layer * slices_per_layer + s;
+    t.s = (int32_t)s;
     t.row0 = (int32_t)(rem - s * tiles_per_slice) * 128;
     return t;
 }

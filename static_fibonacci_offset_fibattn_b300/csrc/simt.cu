@@ -44,6 +44,12 @@ struct Io<__nv_bfloat16> {
     }
 };
 
+// Element offset of the kv slice read by query slice `s` of launch layer `layer` (query head h
+// of batch b reads kv head h / group of batch b; K/V hold slices_per_layer / group slices).
+__device__ __forceinline__ int64_t kv_base(const AttnShape& sh, int layer, int64_t s) {
+    return ((int64_t)layer * (sh.slices_per_layer / sh.group) + s / sh.group) * sh.T * 64;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
@@ -65,14 +71,15 @@ fwd_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
     const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
     const int32_t i = (int32_t)(row % sh.T);
     const int64_t base = slice * sh.T * kD;
+    const int64_t kbase = kv_base(sh, layer, row / sh.T);
     const float2 qv = Io<E>::ld(q + base + (int64_t)i * kD + 2 * lane);
 
     float m = -INFINITY, l = 0.f;
     float2 acc = make_float2(0.f, 0.f);
     auto visit = [&](int32_t j) {
-        const float2 kv = Io<E>::ld(k + base + (int64_t)j * kD + 2 * lane);
+        const float2 kv = Io<E>::ld(k + kbase + (int64_t)j * kD + 2 * lane);
         const float s = warp_sum(qv.x * kv.x + qv.y * kv.y) * sh.scale;
-        const float2 vv = Io<E>::ld(v + base + (int64_t)j * kD + 2 * lane);
+        const float2 vv = Io<E>::ld(v + kbase + (int64_t)j * kD + 2 * lane);
         const float mn = fmaxf(m, s);
         const float corr = expf(m - mn);  // m = -inf on the first key: corr = 0
         const float p = expf(s - mn);
@@ -124,7 +131,8 @@ fwd_frac_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* 
         acc.y = acc.y * corr + p * vv.y;
         m = mn;
     };
-    auto row_of = [&](const E* x, int32_t j) { return Io<E>::ld(x + base + (int64_t)j * kD + 2 * lane); };
+    const int64_t kbase = kv_base(sh, layer, row / sh.T);
+    auto row_of = [&](const E* x, int32_t j) { return Io<E>::ld(x + kbase + (int64_t)j * kD + 2 * lane); };
     const int n_off = tab.c.count[layer];
     for (int e = n_off - 1; e >= 0; --e) {
         const int32_t j = i - tab.c.off[layer][e];
@@ -181,9 +189,10 @@ bwd_dq_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restr
     const float2 gv = Io<E>::ld(dO + ri);
     const float Li = lse[slice * sh.T + i];
     const float Di = delta[slice * sh.T + i];
+    const int64_t kbase = kv_base(sh, layer, row / sh.T);
     float2 acc = make_float2(0.f, 0.f);
     auto visit = [&](int32_t j) {
-        const int64_t rj = base + (int64_t)j * kD + 2 * lane;
+        const int64_t rj = kbase + (int64_t)j * kD + 2 * lane;
         const float2 kv = Io<E>::ld(k + rj);
         const float2 vv = Io<E>::ld(v + rj);
         const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
@@ -204,7 +213,8 @@ bwd_dq_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restr
 
 // dK_j = scale * sum_{i : j in S_i} dS_ij q_i,  dV_j = sum_{i : j in S_i} P_ij dO_i  (key owner)
 // The queries that see key j: i = j + t for 0 <= t < W, and i = j + o for table offsets o,
-// each only while i < T. No atomics: this warp is the only writer of row j.
+// each only while i < T, in each of the `group` query heads that read this kv head. One warp
+// per kv row; no atomics: this warp is the only writer of row j.
 template <typename E>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 bwd_dkdv_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
@@ -212,35 +222,39 @@ bwd_dkdv_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
                 const float* __restrict__ delta, E* __restrict__ dk, E* __restrict__ dv,
                 AttnShape sh, const __grid_constant__ OffsetTables tab) {
     const int lane = threadIdx.x & 31;
-    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t spl_kv = sh.slices_per_layer / sh.group;
+    const int64_t rows = spl_kv * sh.T;
     const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int layer = blockIdx.y;
     if (row >= rows) return;
-    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int64_t skv = row / sh.T;  // kv slice within the layer
     const int32_t j = (int32_t)(row % sh.T);
-    const int64_t base = slice * sh.T * kD;
-    const int64_t rj = base + (int64_t)j * kD + 2 * lane;
+    const int64_t rj = ((int64_t)layer * spl_kv + skv) * sh.T * kD + (int64_t)j * kD + 2 * lane;
     const float2 kv = Io<E>::ld(k + rj);
     const float2 vv = Io<E>::ld(v + rj);
     float2 ak = make_float2(0.f, 0.f), av = make_float2(0.f, 0.f);
-    auto visit = [&](int32_t i) {
-        const int64_t ri = base + (int64_t)i * kD + 2 * lane;
-        const float2 qv = Io<E>::ld(q + ri);
-        const float2 gv = Io<E>::ld(dO + ri);
-        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
-        const float dp = warp_sum(gv.x * vv.x + gv.y * vv.y);
-        const float p = expf(s * sh.scale - lse[slice * sh.T + i]);
-        const float ds = p * (dp - delta[slice * sh.T + i]);
-        av.x += p * gv.x;
-        av.y += p * gv.y;
-        ak.x += ds * qv.x;
-        ak.y += ds * qv.y;
-    };
-    const int32_t i1 = j + sh.W - 1 < sh.T - 1 ? j + sh.W - 1 : sh.T - 1;
-    for (int32_t i = j; i <= i1; ++i) visit(i);
-    for (int e = 0; e < tab.count[layer]; ++e) {
-        const int64_t i = (int64_t)j + tab.off[layer][e];
-        if (i < sh.T) visit((int32_t)i);
+    for (int g = 0; g < sh.group; ++g) {
+        const int64_t slice = (int64_t)layer * sh.slices_per_layer + skv * sh.group + g;
+        const int64_t base = slice * sh.T * kD;
+        auto visit = [&](int32_t i) {
+            const int64_t ri = base + (int64_t)i * kD + 2 * lane;
+            const float2 qv = Io<E>::ld(q + ri);
+            const float2 gv = Io<E>::ld(dO + ri);
+            const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
+            const float dp = warp_sum(gv.x * vv.x + gv.y * vv.y);
+            const float p = expf(s * sh.scale - lse[slice * sh.T + i]);
+            const float ds = p * (dp - delta[slice * sh.T + i]);
+            av.x += p * gv.x;
+            av.y += p * gv.y;
+            ak.x += ds * qv.x;
+            ak.y += ds * qv.y;
+        };
+        const int32_t i1 = j + sh.W - 1 < sh.T - 1 ? j + sh.W - 1 : sh.T - 1;
+        for (int32_t i = j; i <= i1; ++i) visit(i);
+        for (int e = 0; e < tab.count[layer]; ++e) {
+            const int64_t i = (int64_t)j + tab.off[layer][e];
+            if (i < sh.T) visit((int32_t)i);
+        }
     }
     Io<E>::st(dk + rj, make_float2(ak.x * sh.scale, ak.y * sh.scale));
     Io<E>::st(dv + rj, av);
@@ -269,9 +283,10 @@ bwd_dq_frac_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __
     const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
     const int32_t i = (int32_t)(row % sh.T);
     const int64_t base = slice * sh.T * kD;
-    auto row_of = [&](const E* x, int32_t j) { return Io<E>::ld(x + base + (int64_t)j * kD + 2 * lane); };
-    const float2 qv = row_of(q, i);
-    const float2 gv = row_of(dO, i);
+    const int64_t kbase = kv_base(sh, layer, row / sh.T);
+    auto row_of = [&](const E* x, int32_t j) { return Io<E>::ld(x + kbase + (int64_t)j * kD + 2 * lane); };
+    const float2 qv = Io<E>::ld(q + base + (int64_t)i * kD + 2 * lane);
+    const float2 gv = Io<E>::ld(dO + base + (int64_t)i * kD + 2 * lane);
     const float Li = lse[slice * sh.T + i];
     const float Di = delta[slice * sh.T + i];
     // the static kernel's order (distances descending, then the window), so that an integer
@@ -319,48 +334,53 @@ bwd_dkdv_frac_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* 
                      const float* __restrict__ delta, E* __restrict__ dk, E* __restrict__ dv,
                      AttnShape sh, const __grid_constant__ FracTables tab) {
     const int lane = threadIdx.x & 31;
-    const int64_t rows = sh.slices_per_layer * sh.T;
+    const int64_t spl_kv = sh.slices_per_layer / sh.group;
+    const int64_t rows = spl_kv * sh.T;
     const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int layer = blockIdx.y;
     if (row >= rows) return;
-    const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
+    const int64_t skv = row / sh.T;  // kv slice within the layer
     const int32_t j = (int32_t)(row % sh.T);
-    const int64_t base = slice * sh.T * kD;
-    auto row_of = [&](const E* x, int32_t r) { return Io<E>::ld(x + base + (int64_t)r * kD + 2 * lane); };
-    const float2 kv = row_of(k, j);
-    const float2 vv = row_of(v, j);
+    const int64_t kb = ((int64_t)layer * spl_kv + skv) * sh.T * kD;
+    auto kv_row = [&](const E* x, int32_t r) { return Io<E>::ld(x + kb + (int64_t)r * kD + 2 * lane); };
+    const float2 kv = kv_row(k, j);
+    const float2 vv = kv_row(v, j);
     float2 ak = make_float2(0.f, 0.f), av = make_float2(0.f, 0.f);
-    // query i sees key and value rows (kx, vx); this key's share of them is wt
-    auto visit = [&](int32_t i, float2 kx, float2 vx, float wt) {
-        const float2 qv = row_of(q, i);
-        const float2 gv = row_of(dO, i);
-        const float s = warp_sum(qv.x * kx.x + qv.y * kx.y);
-        const float dp = warp_sum(gv.x * vx.x + gv.y * vx.y);
-        const float p = expf(s * sh.scale - lse[slice * sh.T + i]);
-        const float ds = p * (dp - delta[slice * sh.T + i]);
-        av.x += wt * p * gv.x;
-        av.y += wt * p * gv.y;
-        ak.x += wt * ds * qv.x;
-        ak.y += wt * ds * qv.y;
-    };
-    const int32_t i1 = j + sh.W - 1 < sh.T - 1 ? j + sh.W - 1 : sh.T - 1;
-    for (int32_t i = j; i <= i1; ++i) visit(i, kv, vv, 1.f);
-    for (int e = 0; e < tab.c.count[layer]; ++e) {
-        const int64_t c = tab.c.off[layer][e];
-        const float w = tab.w[layer][e];
-        if ((int64_t)j + c < sh.T) {  // row lo of query j + c: the other row is j + 1 <= j + c
-            const float2 k1 = row_of(k, j + 1), v1 = row_of(v, j + 1);
-            visit((int32_t)(j + c), make_float2((1.f - w) * kv.x + w * k1.x, (1.f - w) * kv.y + w * k1.y),
-                  make_float2((1.f - w) * vv.x + w * v1.x, (1.f - w) * vv.y + w * v1.y), 1.f - w);
-        }
-        if (w != 0.f && j >= 1 && (int64_t)j + c - 1 < sh.T) {  // row lo + 1 of query j + c - 1
-            const float2 k0 = row_of(k, j - 1), v0 = row_of(v, j - 1);
-            visit((int32_t)(j + c - 1), make_float2((1.f - w) * k0.x + w * kv.x, (1.f - w) * k0.y + w * kv.y),
-                  make_float2((1.f - w) * v0.x + w * vv.x, (1.f - w) * v0.y + w * vv.y), w);
+    for (int g = 0; g < sh.group; ++g) {
+        const int64_t slice = (int64_t)layer * sh.slices_per_layer + skv * sh.group + g;
+        const int64_t base = slice * sh.T * kD;
+        // query i sees key and value rows (kx, vx); this key's share of them is wt
+        auto visit = [&](int32_t i, float2 kx, float2 vx, float wt) {
+            const float2 qv = Io<E>::ld(q + base + (int64_t)i * kD + 2 * lane);
+            const float2 gv = Io<E>::ld(dO + base + (int64_t)i * kD + 2 * lane);
+            const float s = warp_sum(qv.x * kx.x + qv.y * kx.y);
+            const float dp = warp_sum(gv.x * vx.x + gv.y * vx.y);
+            const float p = expf(s * sh.scale - lse[slice * sh.T + i]);
+            const float ds = p * (dp - delta[slice * sh.T + i]);
+            av.x += wt * p * gv.x;
+            av.y += wt * p * gv.y;
+            ak.x += wt * ds * qv.x;
+            ak.y += wt * ds * qv.y;
+        };
+        const int32_t i1 = j + sh.W - 1 < sh.T - 1 ? j + sh.W - 1 : sh.T - 1;
+        for (int32_t i = j; i <= i1; ++i) visit(i, kv, vv, 1.f);
+        for (int e = 0; e < tab.c.count[layer]; ++e) {
+            const int64_t c = tab.c.off[layer][e];
+            const float w = tab.w[layer][e];
+            if ((int64_t)j + c < sh.T) {  // row lo of query j + c: the other row is j + 1 <= j + c
+                const float2 k1 = kv_row(k, j + 1), v1 = kv_row(v, j + 1);
+                visit((int32_t)(j + c), make_float2((1.f - w) * kv.x + w * k1.x, (1.f - w) * kv.y + w * k1.y),
+                      make_float2((1.f - w) * vv.x + w * v1.x, (1.f - w) * vv.y + w * v1.y), 1.f - w);
+            }
+            if (w != 0.f && j >= 1 && (int64_t)j + c - 1 < sh.T) {  // row lo + 1 of query j + c - 1
+                const float2 k0 = kv_row(k, j - 1), v0 = kv_row(v, j - 1);
+                visit((int32_t)(j + c - 1), make_float2((1.f - w) * k0.x + w * kv.x, (1.f - w) * k0.y + w * kv.y),
+                      make_float2((1.f - w) * v0.x + w * vv.x, (1.f - w) * v0.y + w * vv.y), w);
+            }
         }
     }
-    Io<E>::st(dk + base + (int64_t)j * kD + 2 * lane, make_float2(ak.x * sh.scale, ak.y * sh.scale));
-    Io<E>::st(dv + base + (int64_t)j * kD + 2 * lane, av);
+    Io<E>::st(dk + kb + (int64_t)j * kD + 2 * lane, make_float2(ak.x * sh.scale, ak.y * sh.scale));
+    Io<E>::st(dv + kb + (int64_t)j * kD + 2 * lane, av);
 }
 
 // One block per layer: a fixed-order sum (strided fp64 partials, then a tree) of its rows.
@@ -410,9 +430,12 @@ fibattn_status launch_bwd_frac_simt_f32(const float* q, const float* k, const fl
                                                                          galpha, sh, t);
     }
     {
+        // one warp per kv row
+        const int64_t kv_rows = sh.slices_per_layer / sh.group * sh.T;
+        dim3 kgrid((unsigned)((kv_rows + kWarpsPerBlock - 1) / kWarpsPerBlock), sh.n_layers);
         KernelScope ks("bwd_dkdv_frac_simt", st);
-        bwd_dkdv_frac_kernel<float><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta,
-                                                                           dk, dv, sh, t);
+        bwd_dkdv_frac_kernel<float><<<kgrid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta,
+                                                                            dk, dv, sh, t);
     }
     return launch_status("launch SIMT kernel");
 }
@@ -474,8 +497,11 @@ static fibattn_status bwd_typed(const E* q, const E* k, const E* v, const E* o, 
         bwd_dq_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dq, sh, t);
     }
     {
+        // one warp per kv row
+        const int64_t kv_rows = sh.slices_per_layer / sh.group * sh.T;
+        dim3 kgrid((unsigned)((kv_rows + kWarpsPerBlock - 1) / kWarpsPerBlock), sh.n_layers);
         KernelScope ks("bwd_dkdv_simt", st);
-        bwd_dkdv_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dk, dv, sh, t);
+        bwd_dkdv_kernel<E><<<kgrid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dk, dv, sh, t);
     }
     return launch_status("launch SIMT kernel");
 }

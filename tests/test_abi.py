@@ -215,3 +215,27 @@ def test_bwd_noalloc_rejects_oversize_on_the_host():
     assert L.fibattn_bwd_workspace_size(8, 8, 1024, 64, 1, 64, ctypes.byref(sc), 0, 16,
                                         ctypes.byref(n)) == fa.OK
     assert n.value <= fa.NOALLOC_SCRATCH_BYTES
+
+
+def test_gqa_entry_points_validate_before_launch():
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    ok = ctypes.c_void_p(256)
+    big = ctypes.c_uint64(1 << 40)
+    for H, Hkv in ((6, 4), (4, 0), (4, -1), (0, 1)):
+        assert L.fibattn_fwd_gqa(ok, ok, ok, ok, ok, 1, H, Hkv, 8, 64, 1, 4, 0.0, ctypes.byref(sc),
+                                 0, 1, None) == fa.INVALID_ARG
+        assert L.fibattn_bwd_gqa(*([ok] * 10), big, 1, H, Hkv, 8, 64, 1, 4, 0.0, ctypes.byref(sc),
+                                 0, 1, None) == fa.INVALID_ARG
+    assert L.fibattn_fwd_gqa(ok, ok, ok, ok, ok, 1, 4, 2, 8, 32, 1, 4, 0.0, ctypes.byref(sc), 0, 1,
+                             None) == fa.UNSUPPORTED
+
+
+def test_binding_checks_kv_head_shapes():
+    q = torch.zeros(1, 6, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd(q, torch.zeros(1, 4, 8, 64, dtype=torch.bfloat16),
+               torch.zeros(1, 4, 8, 64, dtype=torch.bfloat16), 4, fa.Schedule())
+    with pytest.raises(ValueError):
+        fa.fwd(q, torch.zeros(1, 3, 8, 64, dtype=torch.bfloat16),
+               torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16), 4, fa.Schedule())
