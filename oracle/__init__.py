@@ -175,6 +175,42 @@ def _group(q, k):
     return H // Hkv
 
 
+def rope(x, base: float = 10000.0, inverse: bool = False):
+    """Vanilla rotary position embedding in fp64 (pt Significancia: the models use RoPE
+    without scaling; Metodologia / Arquitetura, "Implementacao": RoPE is applied before the
+    gather). Row i of every [..., T, d] slice has each pair (2p, 2p+1) rotated by the angle
+    i * theta_p, theta_p = base^(-2p/d); `inverse` rotates by the opposite angle (the
+    transpose, which carries gradients back through the rotation)."""
+    x = np.asarray(x, dtype=np.float64)
+    T, d = x.shape[-2], x.shape[-1]
+    if d % 2:
+        raise ValueError("d must be even")
+    theta = float(base) ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)
+    ang = np.arange(T, dtype=np.float64)[:, None] * theta[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    if inverse:
+        s = -s
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2] = x0 * c - x1 * s
+    y[..., 1::2] = x0 * s + x1 * c
+    return y
+
+
+def fwd_rope(q, k, v, W: int, tables, base: float = 10000.0, scale: float | None = None,
+             n_threads: int = 0):
+    """Forward with RoPE applied to q and k before the attention (kv heads may be grouped)."""
+    return fwd_gqa(rope(q, base), rope(k, base), v, W, tables, scale, n_threads)
+
+
+def bwd_rope(q, k, v, dout, W: int, tables, base: float = 10000.0, scale: float | None = None,
+             n_threads: int = 0):
+    """Backward through RoPE: the attention gradients of the rotated q and k, rotated back."""
+    dq, dk, dv, out, lse = bwd_gqa(rope(q, base), rope(k, base), v, dout, W, tables, scale,
+                                   n_threads)
+    return rope(dq, base, inverse=True), rope(dk, base, inverse=True), dv, out, lse
+
+
 def _frac_tables(dist_tables, shape, n_slices):
     per_layer = len(dist_tables) > 0 and isinstance(dist_tables[0], (list, tuple, np.ndarray))
     tabs = [list(map(float, t)) for t in dist_tables] if per_layer else [list(map(float, dist_tables))]
@@ -267,5 +303,5 @@ def bwd(q, k, v, dout, W: int, tables, scale: float | None = None, n_threads: in
 __all__ = ["schedule", "FIB", "POW2", "FIXED", "LINEAR", "COPRIME", "alpha_for_layer",
            "fibonacci_base", "frac_distances", "key_set", "key_set_c", "layer_table",
            "offset_table", "round_half_up", "fwd", "fwd_frac", "bwd", "bwd_frac", "frac_bases",
-           "fwd_gqa", "bwd_gqa",
+           "fwd_gqa", "bwd_gqa", "rope", "fwd_rope", "bwd_rope",
            "threads", "lib"]
