@@ -6,7 +6,7 @@ backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
 (B=8, H=8, T=1024, d=64), W=64, coprime reassignment (l -> 5l mod 16) of the linear
 stagger alpha 0.5 -> 2.0, bf16, forward + backward.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f|c5f|c5g]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f|c5f|c5g|c5r]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
@@ -16,7 +16,9 @@ data path); value = all ranks' query tokens / max-over-ranks time.
 c3f / c5f are the fractional-offset (learned-alpha) forward / training step (with the
 gradient of every layer's alpha) on the c3 / c5 shapes; their lines add
 "static_counterpart", the static c3 / c5 step (same shape and alpha range) timed in the
-same process, and the latency ratio. c5g is the c5 step with 8 query heads sharing 2 kv heads.
+same process, and the latency ratio. c5g is the c5 step with 8 query heads sharing 2 kv heads;
+c5r the c5 step with RoPE on q and k before the gather (the cos/sin table is built once,
+outside the timed region), with the static c5 step as its counterpart.
 """
 from __future__ import annotations
 
@@ -60,6 +62,8 @@ ALGO_BYTES = {
     "bwd_dq_frac_simt": 4 * 256 + 8 + 256 + 4,
     "bwd_dkdv_frac_simt": 4 * 256 + 8 + 2 * 256,
     "dalpha_reduce": 4,                         # the dalpha partials in
+    "rope_bf16": 2 * 128,                       # one row in, one row out (per rotated row)
+    "rope_f32": 2 * 256,
 }
 # Rows per query token of each kernel that are k/v-shaped (k, v in; dk, dv out).
 KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_simt_bf16": 2, "bwd_dq_tc": 2,
@@ -70,6 +74,7 @@ KERNEL_SRC = {
     "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu",
     "bwd_dq_frac_tc": "bwd_tc.cu", "bwd_dkdv_frac_tc": "bwd_tc.cu",
     "bwd_dq_frac_simt": "simt.cu", "bwd_dkdv_frac_simt": "simt.cu", "dalpha_reduce": "simt.cu",
+    "rope_bf16": "rope.cu", "rope_f32": "rope.cu",
     "bwd_delta_simt": "simt.cu", "bwd_dq_simt": "simt.cu", "bwd_dkdv_simt": "simt.cu",
     "bwd_dq_tc": "bwd_tc.cu", "bwd_dkdv_tc": "bwd_tc.cu",
 }
@@ -92,7 +97,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c5",
-                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f", "c5g"])
+                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f", "c5g", "c5r"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -230,6 +235,7 @@ def run_ours(a, spec, world, rank, local):
     torch.cuda.set_device(dev)
     L = fa.lib()
     frac = "alphas" in spec
+    use_rope = "rope_base" in spec
     sched = None if frac else fa.Schedule(**spec["sched"])
     alphas = fi.frac_alphas(spec) if frac else None
     inp = fi.workload_inputs(a.workload)
@@ -245,6 +251,9 @@ def run_ours(a, spec, world, rank, local):
                 else fa.bwd_workspace_size(d_in["q"], W, sched))
         ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
         dalpha = torch.empty(spec["Lc"], dtype=torch.float32, device=dev)
+    if use_rope:  # built once per (T, base), like a framework's cos/sin cache
+        table = fa.rope_table(spec["T"], spec["rope_base"], dev)
+        rotated = (torch.empty_like(d_in["q"]), torch.empty_like(d_in["k"]))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -255,6 +264,12 @@ def run_ours(a, spec, world, rank, local):
             if train:
                 fa.bwd_frac(x["q"], x["k"], x["v"], o, lse, x["dO"], W, alphas, spec["base"],
                             dq=dq, dk=dk, dv=dv, dalpha=dalpha, workspace=ws)
+            return
+        if use_rope:
+            fa.fwd_rope(x["q"], x["k"], x["v"], W, sched, table, out=o, lse=lse, rotated=rotated)
+            if train:
+                fa.bwd_rope(rotated[0], rotated[1], x["v"], o, lse, x["dO"], W, sched, table,
+                            dq=dq, dk=dk, dv=dv, workspace=ws)
             return
         fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
         if train:
@@ -334,11 +349,12 @@ def run_ours(a, spec, world, rank, local):
     # ---- end to end through the public API, host buffers, copies inside the timed region
     e2e = None
     if not a.no_e2e:
-        e2e = run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas)
+        e2e = run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas,
+                      table if use_rope else None)
 
     # ---- fractional workload: the static step of the same shape, timed the same way
     counterpart = None
-    if frac:
+    if frac or use_rope:
         cname = "c5" if train else "c3"
         cspec = fi.WORKLOADS[cname]
         csched = fa.Schedule(**cspec["sched"])
@@ -398,7 +414,7 @@ def clock_index(local):
     return local
 
 
-def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None):
+def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None, table=None):
     pinned = {n: t.pin_memory() for n, t in inp.items()}
     W = spec["W"]
     train = "bwd" in spec["passes"]
@@ -416,8 +432,11 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None):
 
     def step():
         x = {n: t.to(dev, non_blocking=True) for n, t in pinned.items()}
+        rot = None
         if alphas is not None:
             o, lse = fa.fwd_frac(x["q"], x["k"], x["v"], W, alphas, spec["base"])
+        elif table is not None:
+            o, lse, rot = fa.fwd_rope(x["q"], x["k"], x["v"], W, sched, table)
         else:
             o, lse = fa.fwd(x["q"], x["k"], x["v"], W, sched)
         res = {"o": o, "lse": lse}
@@ -425,6 +444,9 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None):
             dq, dk, dv, da = fa.bwd_frac(x["q"], x["k"], x["v"], o, lse, x["dO"], W, alphas,
                                          spec["base"])
             res.update(dq=dq, dk=dk, dv=dv, dalpha=da)
+        elif train and rot is not None:
+            dq, dk, dv = fa.bwd_rope(rot[0], rot[1], x["v"], o, lse, x["dO"], W, sched, table)
+            res.update(dq=dq, dk=dk, dv=dv)
         elif train:
             dq, dk, dv = fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched)
             res.update(dq=dq, dk=dk, dv=dv)
@@ -499,6 +521,14 @@ def oracle_sample(spec, n_slices, n_threads=0):
             continue
         tab = oracle.layer_table(sc["base"], sc["kind"], l, sc["n_layers"], W, T,
                                  sc.get("base_max", 0), **kw_of())
+        if "rope_base" in spec:
+            if "bwd" in spec["passes"]:
+                oracle.bwd_rope(g("q"), g("k"), g("v"), g("dO"), W, tab, spec["rope_base"], None,
+                                n_threads)
+            else:
+                oracle.fwd_rope(g("q"), g("k"), g("v"), W, tab, spec["rope_base"], None, n_threads)
+            done += len(picks) * T
+            continue
         if "bwd" in spec["passes"]:
             oracle.bwd(g("q"), g("k"), g("v"), g("dO"), W, tab, None, n_threads)
         else:

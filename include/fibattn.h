@@ -301,6 +301,50 @@ FIBATTN_API fibattn_status fibattn_keyset_debug(const fibattn_schedule* sched, i
                                     int32_t T, uint32_t* d_mask, void* cuda_stream);
 
 /*
+ * Rotary position embedding, applied to q and k before the attention (Metodologia /
+ * Arquitetura, "Implementacao": RoPE is applied before the gather; Significancia: vanilla
+ * RoPE without scaling). Row i, pair (2p, 2p+1) is rotated by the angle i * theta_p,
+ * theta_p = base^(-2p/d).
+ * fibattn_rope_table: writes table, float32 device [T][d/2][2] (cos, sin of i * theta_p,
+ *   computed in fp64 and rounded once), 16-byte aligned, caller-owned; build it once per
+ *   (T, base) and pass it to every fibattn_rope call. base > 1 (10000 is the usual value).
+ * fibattn_rope: y = x rotated, x and y [slices][T][d] of dtype `dtype` (row r of a slice at
+ *   position r); inverse != 0 rotates by the opposite angles (R^T: it carries dq and dk back
+ *   through the rotation, and undoes it). x == y (in place) is allowed; a partial overlap is
+ *   INVALID_ARG. table_rows (>= T) is the number of rows the table was built with.
+ * fibattn_fwd_rope: the forward with RoPE before the gather, in one call: q and k rotated into
+ *   the caller's q_rot ([Lc][B][H][T][d]) and k_rot ([Lc][B][H_kv][T][d]) by fibattn_rope,
+ *   then fibattn_fwd_gqa on them. Keep q_rot and k_rot for the backward.
+ * fibattn_bwd_rope: the backward through RoPE from the forward's q_rot and k_rot: the
+ *   attention backward of fibattn_bwd_gqa, then dq and dk rotated back in place (R^T,
+ *   fibattn_rope), so they are the gradients of the unrotated q and k. Workspace as
+ *   fibattn_bwd_workspace_size.
+ * Errors: INVALID_ARG (null or misaligned pointers, sizes, base, a table shorter than T),
+ * UNSUPPORTED (d != 64, dtype), and those of the attention calls; CUDA.
+ */
+FIBATTN_API fibattn_status fibattn_rope_table(float* table, int32_t T, int32_t d, double base,
+                                              void* cuda_stream);
+FIBATTN_API fibattn_status fibattn_rope(const void* x, void* y, int64_t slices, int32_t T,
+                                        int32_t d, int32_t dtype, const float* table,
+                                        int32_t table_rows, int32_t inverse, void* cuda_stream);
+FIBATTN_API fibattn_status fibattn_fwd_rope(const void* q, const void* k, const void* v,
+                                            void* q_rot, void* k_rot, void* o, float* lse,
+                                            int32_t B, int32_t H, int32_t H_kv, int32_t T,
+                                            int32_t d, int32_t dtype, int32_t W, float scale,
+                                            const fibattn_schedule* sched, int32_t layer0,
+                                            int32_t n_layers_call, const float* rope_table,
+                                            int32_t table_rows, void* cuda_stream);
+FIBATTN_API fibattn_status fibattn_bwd_rope(const void* q_rot, const void* k_rot, const void* v,
+                                            const void* o, const float* lse, const void* dO,
+                                            void* dq, void* dk, void* dv, void* workspace,
+                                            uint64_t workspace_bytes, int32_t B, int32_t H,
+                                            int32_t H_kv, int32_t T, int32_t d, int32_t dtype,
+                                            int32_t W, float scale, const fibattn_schedule* sched,
+                                            int32_t layer0, int32_t n_layers_call,
+                                            const float* rope_table, int32_t table_rows,
+                                            void* cuda_stream);
+
+/*
  * Synchronises `cuda_stream`, then reads and clears the device error word.
  * Returns OK, TIMEOUT (a kernel gave up a bounded wait and returned early; its
  * outputs are undefined) or CUDA (a CUDA error is pending on the context).

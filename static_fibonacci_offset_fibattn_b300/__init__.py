@@ -24,7 +24,8 @@ __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd"
            "keyset_debug", "poll_device_error", "status_string", "lib", "library_path",
            "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
            "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac", "bwd_frac",
-           "bwd_frac_workspace_size", "FibFracAttention"]
+           "bwd_frac_workspace_size", "FibFracAttention", "rope_table", "rope", "fwd_rope",
+           "bwd_rope"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
@@ -118,6 +119,12 @@ def lib():
                                                  ctypes.POINTER(u64)]
         L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32, i32,
                                   i32, i32, f32, sp, i32, i32, vp]
+        L.fibattn_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
+        L.fibattn_rope.argtypes = [vp, vp, ctypes.c_int64, i32, i32, i32, vp, i32, i32, vp]
+        L.fibattn_fwd_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                       i32, f32, sp, i32, i32, vp, i32, vp]
+        L.fibattn_bwd_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
+                                       i32, i32, i32, i32, f32, sp, i32, i32, vp, i32, vp]
         L.fibattn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
                                       i32, i32, i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -140,7 +147,8 @@ def lib():
                      "fibattn_bwd_workspace_size",
                      "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error",
                      "fibattn_frac_offsets", "fibattn_fwd_frac", "fibattn_bwd_frac",
-                     "fibattn_fwd_gqa", "fibattn_bwd_gqa",
+                     "fibattn_fwd_gqa", "fibattn_bwd_gqa", "fibattn_rope_table", "fibattn_rope",
+                     "fibattn_fwd_rope", "fibattn_bwd_rope",
                      "fibattn_bwd_frac_workspace_size"):
             getattr(L, name).restype = i32
         _lib = L
@@ -451,3 +459,86 @@ class FibFracAttention(torch.autograd.Function):
         dq, dk, dv, da = bwd_frac(q, k, v, o, lse, dO.contiguous(), W, alphas, base, base_max,
                                   scale)
         return dq, dk, dv, da.to(adev, adtype).reshape(ashape), None, None, None, None
+
+
+def rope_table(T: int, base: float = 10000.0, device="cuda") -> torch.Tensor:
+    """cos/sin table of vanilla RoPE for positions 0..T-1 (fibattn_rope_table), a float32
+    [T, 32, 2] device tensor; build once per (T, base)."""
+    t = torch.empty((T, 32, 2), dtype=torch.float32, device=device)
+    _check(lib().fibattn_rope_table(_ptr(t), T, 64, float(base), _stream(t)), "fibattn_rope_table")
+    return t
+
+
+def rope(x: torch.Tensor, table: torch.Tensor, inverse: bool = False,
+         out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """x [..., T, 64] with RoPE applied (fibattn_rope); `out` may be x (in place)."""
+    if not x.is_cuda or x.dtype not in _DTYPES or not x.is_contiguous() or x.shape[-1] != 64:
+        raise ValueError("x must be a contiguous CUDA float32/bfloat16 tensor [..., T, 64]")
+    T = x.shape[-2]
+    if table.dtype != torch.float32 or table.device != x.device or table.shape[0] < T or \
+            not table.is_contiguous():
+        raise ValueError("table must be a contiguous float32 rope_table of >= T rows on x's device")
+    y = torch.empty_like(x) if out is None else out
+    if y.shape != x.shape or y.dtype != x.dtype or y.device != x.device or not y.is_contiguous():
+        raise ValueError("out must match x")
+    slices = x.numel() // (T * 64)
+    _check(lib().fibattn_rope(_ptr(x), _ptr(y), slices, T, 64, _DTYPES[x.dtype], _ptr(table),
+                              table.shape[0], int(bool(inverse)), _stream(x)), "fibattn_rope")
+    return y
+
+
+def _check_table(table: torch.Tensor, T: int, ref: torch.Tensor):
+    if table.dtype != torch.float32 or table.device != ref.device or table.shape[0] < T or \
+            not table.is_contiguous():
+        raise ValueError("table must be a contiguous float32 rope_table of >= T rows on q's device")
+
+
+def fwd_rope(q, k, v, W: int, sched: Schedule, table: torch.Tensor, layer0: int = 0,
+             scale: Optional[float] = None, out=None, lse=None, rotated=None):
+    """Forward with RoPE on q and k before the gather (fibattn_fwd_rope: q and k rotated, then
+    the attention). Returns (o, lse, (q_rot, k_rot)); keep q_rot and k_rot for bwd_rope.
+    `rotated` may pass preallocated (q_rot, k_rot) buffers."""
+    Lc, B, H, T, d = _shape(q)
+    Hkv = _kv_heads(q, k, v)
+    qr, kr = rotated if rotated is not None else (torch.empty_like(q), torch.empty_like(k))
+    o = torch.empty_like(q) if out is None else out
+    _check_tensors(q, o, qr)
+    _check_tensors(k, v, kr)
+    _check_table(table, T, q)
+    if k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("q/k/v must share device and dtype")
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    s = sched.to_c()
+    st = lib().fibattn_fwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(o), _ptr(lse),
+                                B, H, Hkv, T, d, _DTYPES[q.dtype], W, float(scale or 0.0),
+                                ctypes.byref(s), layer0, Lc, _ptr(table), table.shape[0],
+                                _stream(q))
+    _check(st, "fibattn_fwd_rope")
+    return o, lse, (qr, kr)
+
+
+def bwd_rope(q_rot, k_rot, v, o, lse, dO, W: int, sched: Schedule, table: torch.Tensor,
+             layer0: int = 0, scale: Optional[float] = None, dq=None, dk=None, dv=None,
+             workspace=None):
+    """Backward through RoPE from fwd_rope's rotated q and k (fibattn_bwd_rope: dq and dk come
+    out rotated back, as the gradients of the unrotated q and k). Returns (dq, dk, dv)."""
+    Lc, B, H, T, d = _shape(q_rot)
+    Hkv = _kv_heads(q_rot, k_rot, v)
+    dq = torch.empty_like(q_rot) if dq is None else dq
+    dk = torch.empty_like(k_rot) if dk is None else dk
+    dv = torch.empty_like(k_rot) if dv is None else dv
+    _check_tensors(q_rot, o, dO, dq)
+    _check_tensors(k_rot, v, dk, dv)
+    _check_table(table, T, q_rot)
+    need = bwd_workspace_size(q_rot, W, sched, layer0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_rot.device)
+    s = sched.to_c()
+    st = lib().fibattn_bwd_rope(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), B, H, Hkv, T, d,
+                                _DTYPES[q_rot.dtype], W, float(scale or 0.0), ctypes.byref(s),
+                                layer0, Lc, _ptr(table), table.shape[0], _stream(q_rot))
+    _check(st, "fibattn_bwd_rope")
+    return dq, dk, dv

@@ -273,12 +273,15 @@ fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int32_t T, int32
     return FIBATTN_OK;
 }
 
-fibattn_status fibattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
-                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                               void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
-                               int32_t H_kv, int32_t T, int32_t d, int32_t dtype, int32_t W,
-                               float scale, const fibattn_schedule* sched, int32_t layer0,
-                               int32_t n_layers_call, void* cuda_stream) {
+namespace {
+
+// The backward of fibattn_bwd_gqa / fibattn_bwd_rope (rope: the RoPE table or null).
+fibattn_status bwd_common(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
+                          int32_t H_kv, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                          float scale, const fibattn_schedule* sched, int32_t layer0,
+                          int32_t n_layers_call, void* cuda_stream) {
     const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return FIBATTN_ERR_INVALID_ARG;
@@ -327,6 +330,65 @@ fibattn_status fibattn_bwd_gqa(const void* q, const void* k, const void* v, cons
         if (st != FIBATTN_OK) return st;
     }
     return FIBATTN_OK;
+}
+
+}  // namespace
+
+fibattn_status fibattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
+                               int32_t H_kv, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                               float scale, const fibattn_schedule* sched, int32_t layer0,
+                               int32_t n_layers_call, void* cuda_stream) {
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, H, H_kv, T,
+                      d, dtype, W, scale, sched, layer0, n_layers_call, cuda_stream);
+}
+
+fibattn_status fibattn_bwd_rope(const void* q_rot, const void* k_rot, const void* v,
+                                const void* o, const float* lse, const void* dO, void* dq,
+                                void* dk, void* dv, void* workspace, uint64_t workspace_bytes,
+                                int32_t B, int32_t H, int32_t H_kv, int32_t T, int32_t d,
+                                int32_t dtype, int32_t W, float scale,
+                                const fibattn_schedule* sched, int32_t layer0,
+                                int32_t n_layers_call, const float* rope_table,
+                                int32_t table_rows, void* cuda_stream) {
+    if (!rope_table || !aligned16(rope_table) || table_rows < T) return FIBATTN_ERR_INVALID_ARG;
+    fibattn_status st = bwd_common(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace,
+                                   workspace_bytes, B, H, H_kv, T, d, dtype, W, scale, sched,
+                                   layer0, n_layers_call, cuda_stream);
+    if (st != FIBATTN_OK) return st;
+    // dq and dk of the rotated q and k, rotated back in place: the gradients of q and k
+    st = fibattn_rope(dq, dq, (int64_t)n_layers_call * B * H, T, d, dtype, rope_table, table_rows,
+                      1, cuda_stream);
+    if (st != FIBATTN_OK) return st;
+    return fibattn_rope(dk, dk, (int64_t)n_layers_call * B * H_kv, T, d, dtype, rope_table,
+                        table_rows, 1, cuda_stream);
+}
+
+fibattn_status fibattn_fwd_rope(const void* q, const void* k, const void* v, void* q_rot,
+                                void* k_rot, void* o, float* lse, int32_t B, int32_t H,
+                                int32_t H_kv, int32_t T, int32_t d, int32_t dtype, int32_t W,
+                                float scale, const fibattn_schedule* sched, int32_t layer0,
+                                int32_t n_layers_call, const float* rope_table,
+                                int32_t table_rows, void* cuda_stream) {
+    if (!rope_table || !aligned16(rope_table) || table_rows < T) return FIBATTN_ERR_INVALID_ARG;
+    if (!q || !k || !q_rot || !k_rot || !aligned16(q) || !aligned16(k) || !aligned16(q_rot) ||
+        !aligned16(k_rot))
+        return FIBATTN_ERR_INVALID_ARG;
+    if (H_kv < 1 || H < 1 || H % H_kv != 0) return FIBATTN_ERR_INVALID_ARG;
+    // every argument of the attention is checked before the first rotation is launched
+    fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
+    if (st != FIBATTN_OK) return st;
+    if (!v || !o || !lse || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FIBATTN_ERR_INVALID_ARG;
+    st = fibattn_rope(q, q_rot, (int64_t)n_layers_call * B * H, T, d, dtype, rope_table,
+                      table_rows, 0, cuda_stream);
+    if (st != FIBATTN_OK) return st;
+    st = fibattn_rope(k, k_rot, (int64_t)n_layers_call * B * H_kv, T, d, dtype, rope_table,
+                      table_rows, 0, cuda_stream);
+    if (st != FIBATTN_OK) return st;
+    return fibattn_fwd_gqa(q_rot, k_rot, v, o, lse, B, H, H_kv, T, d, dtype, W, scale, sched,
+                           layer0, n_layers_call, cuda_stream);
 }
 
 fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -410,6 +472,31 @@ fibattn_status fibattn_bwd_frac(const void* q, const void* k, const void* v, con
         if (st != FIBATTN_OK) return st;
     }
     return FIBATTN_OK;
+}
+
+fibattn_status fibattn_rope_table(float* table, int32_t T, int32_t d, double base,
+                                  void* cuda_stream) {
+    if (!table || (reinterpret_cast<uintptr_t>(table) & 15u) != 0 || T < 1) return FIBATTN_ERR_INVALID_ARG;
+    if (!(base > 1.0) || !(base < 1e300)) return FIBATTN_ERR_INVALID_ARG;
+    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    return launch_rope_table(table, T, base, as_stream(cuda_stream));
+}
+
+fibattn_status fibattn_rope(const void* x, void* y, int64_t slices, int32_t T, int32_t d,
+                            int32_t dtype, const float* table, int32_t table_rows,
+                            int32_t inverse, void* cuda_stream) {
+    if (!x || !y || !table || !aligned16(x) || !aligned16(y) || !aligned16(table))
+        return FIBATTN_ERR_INVALID_ARG;
+    if (table_rows < T) return FIBATTN_ERR_INVALID_ARG;
+    if (slices < 1 || T < 1 || slices * (int64_t)T > ((int64_t)1 << 40)) return FIBATTN_ERR_INVALID_ARG;
+    if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
+    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    const int64_t bytes = slices * (int64_t)T * d * (int64_t)elt_size(dtype);
+    const char* xb = static_cast<const char*>(x);
+    const char* yb = static_cast<const char*>(y);
+    if (xb != yb && xb < yb + bytes && yb < xb + bytes) return FIBATTN_ERR_INVALID_ARG;  // partial overlap
+    return launch_rope(x, y, slices * (int64_t)T, T, dtype, table, inverse != 0,
+                       as_stream(cuda_stream));
 }
 
 fibattn_status fibattn_poll_device_error(void* cuda_stream) {

@@ -138,6 +138,12 @@ fibattn_status launch_bwd_frac_tc_bf16(const void* q, const void* k, const void*
 fibattn_status launch_dalpha_reduce(const float* galpha, float* dalpha, int32_t n,
                                     int64_t rows_per_layer, cudaStream_t st);
 
+// Rotary position embedding (rope.cu): the cos/sin table [T][32] (float2, fp64-computed) and
+// the rotation of rows [rows][64] (row r at position r % T), y = R x or R^T x.
+fibattn_status launch_rope_table(float* table, int32_t T, double base, cudaStream_t st);
+fibattn_status launch_rope(const void* x, void* y, int64_t rows, int32_t T, int32_t dtype,
+                           const float* table, bool inverse, cudaStream_t st);
+
 // Tensor-core backward (bf16 path). Workspace rows are padded to T_pad = T rounded up to 4:
 // delta and lse2 [slices][T_pad] fp32, pds [slices][n_max][T_pad] (P, dS) bf16 pairs indexed
 // by key row, n_max >= every launch layer's table size.

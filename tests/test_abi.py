@@ -239,3 +239,23 @@ def test_binding_checks_kv_head_shapes():
     with pytest.raises(ValueError):
         fa.fwd(q, torch.zeros(1, 3, 8, 64, dtype=torch.bfloat16),
                torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16), 4, fa.Schedule())
+
+
+def test_rope_entry_points_validate_before_launch():
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    ok = ctypes.c_void_p(256)
+    assert L.fibattn_rope_table(ok, 8, 64, ctypes.c_double(1.0), None) == fa.INVALID_ARG
+    assert L.fibattn_rope_table(ok, 0, 64, ctypes.c_double(1e4), None) == fa.INVALID_ARG
+    assert L.fibattn_rope_table(ok, 8, 32, ctypes.c_double(1e4), None) == fa.UNSUPPORTED
+    # table shorter than T, partial overlap, misalignment
+    assert L.fibattn_rope(ok, ok, 1, 8, 64, 1, ok, 4, 0, None) == fa.INVALID_ARG
+    assert L.fibattn_rope(ok, ctypes.c_void_p(256 + 128), 1, 8, 64, 1, ok, 8, 0, None) == fa.INVALID_ARG
+    assert L.fibattn_rope(ctypes.c_void_p(264), ok, 1, 8, 64, 1, ok, 8, 0, None) == fa.INVALID_ARG
+    assert L.fibattn_rope(ok, ok, 1, 8, 64, 3, ok, 8, 0, None) == fa.UNSUPPORTED
+    assert L.fibattn_fwd_rope(*([ok] * 7), 1, 4, 2, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 7,
+                              None) == fa.INVALID_ARG
+    assert L.fibattn_fwd_rope(*([ok] * 7), 1, 4, 3, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 8,
+                              None) == fa.INVALID_ARG
+    assert L.fibattn_bwd_rope(*([ok] * 10), ctypes.c_uint64(1 << 40), 1, 4, 2, 8, 64, 1, 4, 0.0,
+                              ctypes.byref(sc), 0, 1, None, 8, None) == fa.INVALID_ARG

@@ -1,0 +1,100 @@
+"""GPU parity of the rotary position embedding kernels and of the attention through them.
+
+The table (fp64 cos/sin rounded once to float32) must agree with fp64 to one float ulp; the
+rotation within the output dtype's rounding; the attention through RoPE within the path's
+tolerances (max-abs 1e-5 fp32, 2e-2 bf16; lse 1e-5 / 1e-3).
+"""
+import numpy as np
+import pytest
+import torch
+
+import fibattn_inputs as fi
+import oracle
+import static_fibonacci_offset_fibattn_b300 as fa
+from gpu_common import LSE_TOL, TOL, f64, lib_schedule, max_abs, oracle_table, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,base", [(1, 10000.0), (1024, 10000.0), (4096, 10000.0), (300, 500.0)])
+def test_rope_table_matches_fp64(T, base):
+    t = fa.rope_table(T, base).cpu().numpy().astype(np.float64)
+    theta = base ** (-2.0 * np.arange(32) / 64)
+    ang = np.arange(T)[:, None] * theta[None, :]
+    ref = np.stack((np.cos(ang), np.sin(ang)), axis=-1)
+    assert np.all(np.abs(t - ref) <= 2.0 ** -24 * np.abs(ref) + 1e-30)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(3, 257, 64), (2, 2, 1024, 64), (1, 1, 64)])
+@pytest.mark.parametrize("inverse", [False, True])
+def test_rope_kernel_matches_oracle(dtype, shape, inverse):
+    x = fi.draw(shape, seed=5, scale=2.0, dtype=dtype, names=("x",))["x"]
+    T = shape[-2]
+    table = fa.rope_table(T)
+    y = fa.rope(x.cuda(), table, inverse=inverse)
+    ref = oracle.rope(f64(x), inverse=inverse)
+    if dtype == "f32":
+        assert max_abs(f64(y), ref) <= 2e-6
+    else:  # one bf16 rounding of the result
+        assert np.all(np.abs(f64(y) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+def test_rope_in_place_and_round_trip():
+    x = fi.draw((2, 3, 500, 64), seed=6, scale=1.0, dtype="f32", names=("x",))["x"].cuda()
+    table = fa.rope_table(500)
+    y = fa.rope(x, table)
+    z = x.clone()
+    fa.rope(z, table, out=z)
+    assert torch.equal(y, z)
+    back = fa.rope(y, table, inverse=True)
+    assert max_abs(f64(back), f64(x)) <= 2e-6
+    with pytest.raises(ValueError):
+        fa.rope(x, fa.rope_table(100))  # table shorter than T
+
+
+SCHED = dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", [(1, 2, 2, 300, 16), (2, 4, 1, 1030, 64), (1, 8, 2, 257, 8)])
+def test_attention_through_rope_matches_oracle(dtype, case):
+    Lc, H, Hkv, T, W = case
+    kv = {n: (Lc, 1, Hkv, T, 64) for n in ("k", "v")}
+    inp = fi.draw((Lc, 1, H, T, 64), seed=T, scale=0.5, dtype=dtype, names=("q", "k", "v", "dO"),
+                  shapes=kv)
+    dev = to_dev(inp)
+    sc = lib_schedule(SCHED)
+    table = fa.rope_table(T)
+    o, lse, (qr, kr) = fa.fwd_rope(dev["q"], dev["k"], dev["v"], W, sc, table, layer0=5)
+    dq, dk, dv = fa.bwd_rope(qr, kr, dev["v"], o, lse, dev["dO"], W, sc, table, layer0=5)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    tabs = [oracle_table(SCHED, 5 + l, W, T) for l in range(Lc)]
+    g = lambda n: f64(inp[n])
+    rq, rk, rv, ro, rl = oracle.bwd_rope(g("q"), g("k"), g("v"), g("dO"), W, tabs)
+    assert max_abs(f64(o), ro) <= TOL[dtype]
+    assert max_abs(f64(lse), rl) <= LSE_TOL[dtype]
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert max_abs(f64(got), ref) <= TOL[dtype]
+
+
+def test_rope_training_step_sampled():
+    spec = fi.WORKLOADS["c5r"]
+    inp = fi.workload_inputs("c5r")
+    dev = to_dev(inp)
+    sc = lib_schedule(spec["sched"])
+    W, T = spec["W"], spec["T"]
+    table = fa.rope_table(T, spec["rope_base"])
+    o, lse, (qr, kr) = fa.fwd_rope(dev["q"], dev["k"], dev["v"], W, sc, table)
+    dq, dk, dv = fa.bwd_rope(qr, kr, dev["v"], o, lse, dev["dO"], W, sc, table)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    for l in (0, 7, 15):
+        tab = oracle_table(spec["sched"], l, W, T)
+        b, h = l % spec["B"], (3 * l) % spec["H"]
+        g = lambda n: f64(inp[n][l, b, h])[None]
+        rq, rk, rv, ro, rl = oracle.bwd_rope(g("q"), g("k"), g("v"), g("dO"), W, tab,
+                                             spec["rope_base"])
+        for got, ref in ((o, ro), (dq, rq), (dk, rk), (dv, rv)):
+            assert max_abs(f64(got[l, b, h])[None], ref) <= TOL["bf16"], l
