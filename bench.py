@@ -6,7 +6,8 @@ backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
 (B=8, H=8, T=1024, d=64), W=64, coprime reassignment (l -> 5l mod 16) of the linear
 stagger alpha 0.5 -> 2.0, bf16, forward + backward.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c2|c3|c3p|c3f|c5f|c5g|c5r]
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+                  [--workload c5|c4|c2|c3|c3p|c3f|c5f|c5g|c5r|c3w|c5w]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
@@ -18,7 +19,8 @@ gradient of every layer's alpha) on the c3 / c5 shapes; their lines add
 "static_counterpart", the static c3 / c5 step (same shape and alpha range) timed in the
 same process, and the latency ratio. c5g is the c5 step with 8 query heads sharing 2 kv heads;
 c5r the c5 step with RoPE on q and k before the gather (the cos/sin table is built once,
-outside the timed region), with the static c5 step as its counterpart.
+outside the timed region), with the static c5 step as its counterpart; c3w / c5w the c3
+forward / c5 step at head size 128 (4 heads of 128).
 """
 from __future__ import annotations
 
@@ -49,6 +51,7 @@ UNIT = "query-tokens/s"
 ALGO_BYTES = {
     "fwd_tc_bf16": 3 * 128 + 128 + 4,          # q, k, v in; o, lse out
     "fwd_frac_tc_bf16": 3 * 128 + 128 + 4,     # the same for fractional offsets
+    "fwd_tc128_bf16": 3 * 256 + 256 + 4,       # head size 128: rows of 256 B
     "fwd_frac_simt_f32": 3 * 256 + 256 + 4,
     "fwd_simt_bf16": 3 * 128 + 128 + 4,
     "fwd_simt_f32": 3 * 256 + 256 + 4,
@@ -66,12 +69,12 @@ ALGO_BYTES = {
     "rope_f32": 2 * 256,
 }
 # Rows per query token of each kernel that are k/v-shaped (k, v in; dk, dv out).
-KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_simt_bf16": 2, "bwd_dq_tc": 2,
+KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_simt_bf16": 2, "fwd_tc128_bf16": 2, "bwd_dq_tc": 2,
            "bwd_dkdv_tc": 4, "bwd_dq_simt": 2, "bwd_dkdv_simt": 4}
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
-    "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu",
+    "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu", "fwd_tc128_bf16": "fwd_tc.cu",
     "bwd_dq_frac_tc": "bwd_tc.cu", "bwd_dkdv_frac_tc": "bwd_tc.cu",
     "bwd_dq_frac_simt": "simt.cu", "bwd_dkdv_frac_simt": "simt.cu", "dalpha_reduce": "simt.cu",
     "rope_bf16": "rope.cu", "rope_f32": "rope.cu",
@@ -86,7 +89,7 @@ def algo_bytes(kernel, spec):
     b = ALGO_BYTES.get(kernel, 0)
     G = spec["H"] // spec.get("Hkv", spec["H"])
     if G > 1 and kernel in KV_ROWS:
-        row = 256 if "f32" in kernel or kernel.endswith("_simt") else 128
+        row = 256 if "f32" in kernel or kernel.endswith("_simt") or "128" in kernel else 128
         b -= KV_ROWS[kernel] * row * (1 - 1 / G)
     return b
 
@@ -97,7 +100,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c5",
-                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f", "c5g", "c5r"])
+                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f", "c5g", "c5r", "c3w",
+                             "c5w"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

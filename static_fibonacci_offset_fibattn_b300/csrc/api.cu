@@ -23,7 +23,7 @@ fibattn_status check_common(int32_t B, int32_t H, int32_t T, int32_t d, int32_t 
     if (sched->n_layers < 1 || (int64_t)layer0 + n_layers_call > sched->n_layers)
         return FIBATTN_ERR_INVALID_ARG;
     if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
-    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FIBATTN_ERR_UNSUPPORTED;
     // rows of one launch layer must index within int32 grids and int64 offsets
     const int64_t rows = (int64_t)B * H * T;
     if (rows > ((int64_t)1 << 34)) return FIBATTN_ERR_INVALID_ARG;
@@ -77,10 +77,12 @@ BwdWorkspace workspace_layout(int32_t B, int32_t H, int32_t T, int32_t dtype, in
     return ws;
 }
 
-// Callers have validated the arguments (check_common), so every table builds.
-BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t dtype, int32_t W,
+// Callers have validated the arguments (check_common), so every table builds. The tensor-core
+// layout is bf16 at d = 64; everything else runs the SIMT backward (D only).
+BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
                            const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
-    if (dtype != FIBATTN_BF16) return workspace_layout(B, H, T, dtype, n_layers_call, 0, false);
+    if (dtype != FIBATTN_BF16 || d != 64)
+        return workspace_layout(B, H, T, FIBATTN_F32, n_layers_call, 0, false);
     int32_t n_max = 0;
     for (int32_t c = 0; c < n_layers_call; ++c) {
         Alpha a;
@@ -194,7 +196,7 @@ fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv};
+        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv, d};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t koff = (size_t)c * per_layer_kv * d * es;
         const char* qc = (const char*)q + off;
@@ -205,8 +207,10 @@ fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void
         if (dtype == FIBATTN_F32)
             st = launch_fwd_simt_f32((const float*)qc, (const float*)kc, (const float*)vc,
                                      (float*)oc, lc, sh, t, as_stream(cuda_stream));
-        else
+        else if (d == 64)
             st = launch_fwd_tc_bf16(qc, kc, vc, oc, lc, sh, t, as_stream(cuda_stream));
+        else
+            st = launch_fwd_tc128_bf16(qc, kc, vc, oc, lc, sh, t, as_stream(cuda_stream));
         if (st != FIBATTN_OK) return st;
     }
     return FIBATTN_OK;
@@ -268,7 +272,7 @@ fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int32_t T, int32
     if (!bytes) return FIBATTN_ERR_INVALID_ARG;
     fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (st != FIBATTN_OK) return st;
-    const BwdWorkspace ws = bwd_workspace(B, H, T, dtype, W, sched, layer0, n_layers_call);
+    const BwdWorkspace ws = bwd_workspace(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     *bytes = ws.total;
     return FIBATTN_OK;
 }
@@ -290,7 +294,7 @@ fibattn_status bwd_common(const void* q, const void* k, const void* v, const voi
     if (H_kv < 1 || H < 1 || H % H_kv != 0) return FIBATTN_ERR_INVALID_ARG;
     fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (st != FIBATTN_OK) return st;
-    const BwdWorkspace ws = bwd_workspace(B, H, T, dtype, W, sched, layer0, n_layers_call);
+    const BwdWorkspace ws = bwd_workspace(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (workspace_bytes < ws.total) return FIBATTN_ERR_INVALID_ARG;
     float* delta = static_cast<float*>(workspace);
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2_offset);
@@ -305,11 +309,17 @@ fibattn_status bwd_common(const void* q, const void* k, const void* v, const voi
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv};
+        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv, d};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t koff = (size_t)c * per_layer_kv * d * es;
         const size_t loff = (size_t)c * per_layer;
-        if (dtype == FIBATTN_F32) {
+        if (dtype == FIBATTN_BF16 && d != 64) {
+            st = launch_bwd_simt_bf16((const char*)q + off, (const char*)k + koff,
+                                      (const char*)v + koff, (const char*)o + off, lse + loff,
+                                      (const char*)dO + off, (char*)dq + off, (char*)dk + koff,
+                                      (char*)dv + koff, delta + loff, sh, t,
+                                      as_stream(cuda_stream));
+        } else if (dtype == FIBATTN_F32) {
             st = launch_bwd_simt_f32((const float*)((const char*)q + off),
                                      (const float*)((const char*)k + koff),
                                      (const float*)((const char*)v + koff),
@@ -353,6 +363,7 @@ fibattn_status fibattn_bwd_rope(const void* q_rot, const void* k_rot, const void
                                 int32_t n_layers_call, const float* rope_table,
                                 int32_t table_rows, void* cuda_stream) {
     if (!rope_table || !aligned16(rope_table) || table_rows < T) return FIBATTN_ERR_INVALID_ARG;
+    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;  // the rotation kernel's rows are 64 wide
     fibattn_status st = bwd_common(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace,
                                    workspace_bytes, B, H, H_kv, T, d, dtype, W, scale, sched,
                                    layer0, n_layers_call, cuda_stream);
@@ -372,6 +383,7 @@ fibattn_status fibattn_fwd_rope(const void* q, const void* k, const void* v, voi
                                 int32_t n_layers_call, const float* rope_table,
                                 int32_t table_rows, void* cuda_stream) {
     if (!rope_table || !aligned16(rope_table) || table_rows < T) return FIBATTN_ERR_INVALID_ARG;
+    if (d != 64) return FIBATTN_ERR_UNSUPPORTED;  // the rotation kernel's rows are 64 wide
     if (!q || !k || !q_rot || !k_rot || !aligned16(q) || !aligned16(k) || !aligned16(q_rot) ||
         !aligned16(k_rot))
         return FIBATTN_ERR_INVALID_ARG;

@@ -36,6 +36,14 @@
 // that row r finds both of its rows, r and r + 1, in the slot; the score is the lerp of the
 // two row dot products and the value update two axpys with p (1 - w) and p w. A distance
 // with w = 0 takes the static code path, so integer alphas give the static results.
+//
+// Head size 128 (kWide): rows are two 64-column halves (two 128-byte swizzle atoms). Each
+// tile is taken by two CTAs, CTA half h writing output columns [64h, 64h+64): both compute
+// the full scores (S over both halves of Q and K: 8 MMA k-steps; the offsets' row dots over
+// 128 dims), and each accumulates P V and the offsets' p v over its own half of V, so TMEM
+// (S 192 + O 64 columns), the ring and the row threads' O registers keep their 64-wide form.
+// Ring items of a group: two Q items (the halves), one K chunk per slot (both halves), the
+// own half of the V chunks two per slot; per offset the two K halves and the own V half.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -106,15 +114,21 @@ struct FwdArgs<true> : FwdParams {
 };
 
 // The band and offset extents of one tile; every role derives the same item sequence.
+template <bool kWide>
 struct Plan {
+    static constexpr int kQItems = kWide ? 2 : 1;   // Q copy items per group
+    static constexpr int kKItems = kWide ? 2 : 1;   // K items per offset
     int32_t i0, klast, c_lo, n_chunks, n_groups, n_act;
     __device__ __forceinline__ int nch(int g) const {
         return min(kMaxGroupChunks, n_chunks - g * kMaxGroupChunks);
     }
     __device__ __forceinline__ int band_slots(int g) const { return (nch(g) + 1) / 2; }
-    // ring items of group g: a copy of the Q tile, its K slots, its V slots (at most 5, so a
-    // group never waits on a later item of the ring)
-    __device__ __forceinline__ uint32_t group_items(int g) const { return 1 + 2 * band_slots(g); }
+    __device__ __forceinline__ int k_slots(int g) const { return kWide ? nch(g) : band_slots(g); }
+    // ring items of group g: the Q copy, its K slots, its V slots (at most 5 before the V
+    // slots, so a group never waits on a later item of the ring)
+    __device__ __forceinline__ uint32_t group_items(int g) const {
+        return kQItems + k_slots(g) + band_slots(g);
+    }
     __device__ __forceinline__ uint32_t band_items() const {
         uint32_t n = 0;
         for (int g = 0; g < n_groups; ++g) n += group_items(g);
@@ -122,8 +136,9 @@ struct Plan {
     }
 };
 
-__device__ __forceinline__ Plan make_plan(const FwdParams& p, int layer, int32_t i0) {
-    Plan pl;
+template <bool kWide>
+__device__ __forceinline__ Plan<kWide> make_plan(const FwdParams& p, int layer, int32_t i0) {
+    Plan<kWide> pl;
     pl.i0 = i0;
     const int32_t kstart = i0 - p.W + 1 > 0 ? i0 - p.W + 1 : 0;
     pl.klast = (i0 + kRows - 1 < p.T - 1) ? i0 + kRows - 1 : p.T - 1;
@@ -138,9 +153,18 @@ __device__ __forceinline__ Plan make_plan(const FwdParams& p, int layer, int32_t
     return pl;
 }
 
-template <bool kFrac>
+// Tile walk: at head size 128 each tile is taken twice, by output half (the fastest index).
+template <bool kWide>
+__device__ __forceinline__ ring::Tile tile_at(const FwdParams& p, uint32_t idx, int& half) {
+    half = kWide ? (int)(idx & 1u) : 0;
+    return ring::tile_of(kWide ? idx >> 1 : idx, p.tiles_per_slice, p.slices_per_layer);
+}
+
+template <bool kFrac, bool kWide>
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
+    static_assert(!(kFrac && kWide), "the fractional mode is for head size 64");
+    using PL = Plan<kWide>;
     using L = Layout<kFrac>;
     constexpr uint32_t kOffTmemSlot = tmem_slot_off<kFrac>();
     extern __shared__ uint8_t smem_raw[];
@@ -190,31 +214,46 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             }
             uint32_t seq = 0;
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
-                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer);
-                const Plan pl = make_plan(p, tl.layer, tl.row0);
+                int half;
+                const ring::Tile tl = tile_at<kWide>(p, idx, half);
+                const PL pl = make_plan<kWide>(p, tl.layer, tl.row0);
                 const int32_t z = (int32_t)tl.zl;
+                const int32_t xv = 64 * half;  // the own half of V
                 // the kv slice: query head h of batch b reads kv head h / group
                 const int32_t zk = (int32_t)((int64_t)tl.layer * p.slices_per_layer_kv +
                                              (uint32_t)tl.s / p.group);
                 // band: per group a copy of Q, its K chunks, then its V chunks (two per slot)
                 for (int g = 0; g < pl.n_groups; ++g) {
-                    if (rg.acquire(seq, aborted, p.err)) {
+                    for (int qh = 0; qh < PL::kQItems; ++qh, ++seq) {  // Q (head size 128: by halves)
+                        if (!rg.acquire(seq, aborted, p.err)) continue;
                         mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes);
-                        tma_load_3d(rg.addr(seq), &p.tm_q, rg.full(seq), 0, pl.i0, z);
-                        tma_load_3d(rg.addr(seq) + kChunkBytes, &p.tm_q, rg.full(seq), 0, pl.i0 + kChunk, z);
+                        tma_load_3d(rg.addr(seq), &p.tm_q, rg.full(seq), 64 * qh, pl.i0, z);
+                        tma_load_3d(rg.addr(seq) + kChunkBytes, &p.tm_q, rg.full(seq), 64 * qh,
+                                    pl.i0 + kChunk, z);
                     }
-                    ++seq;
                     const int nch = pl.nch(g);
                     for (int h = 0; h < 2; ++h) {
                         const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
+                        if (kWide && h == 0) {
+                            // one K chunk per slot: its two column halves
+                            for (int c = 0; c < nch; ++c, ++seq) {
+                                const int32_t y = (pl.c_lo + g * kMaxGroupChunks + c) * kChunk;
+                                if (!rg.acquire(seq, aborted, p.err)) continue;
+                                mbar_arrive_expect_tx(rg.full(seq), 2 * kChunkBytes);
+                                tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, zk);
+                                tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 64, y, zk);
+                            }
+                            continue;
+                        }
+                        const int32_t x = h == 0 ? 0 : xv;
                         for (int c = 0; c < nch; c += 2, ++seq) {
                             const int n2 = min(2, nch - c);
                             const int32_t y = (pl.c_lo + g * kMaxGroupChunks + c) * kChunk;
                             if (!rg.acquire(seq, aborted, p.err)) continue;
                             mbar_arrive_expect_tx(rg.full(seq), n2 * kChunkBytes);
-                            tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, zk);
+                            tma_load_3d(rg.addr(seq), map, rg.full(seq), x, y, zk);
                             if (n2 == 2)
-                                tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, zk);
+                                tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), x, y + kChunk, zk);
                         }
                     }
                 }
@@ -224,12 +263,15 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                     const int32_t y = pl.i0 - offs[k];
                     bool side = false;
                     if constexpr (kFrac) side = p.w[tl.layer][k] != 0.f;
-                    for (int h = 0; h < 2; ++h, ++seq) {
-                        const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
+                    // K_o (head size 128: its two halves), then the own half of V_o
+                    for (int h = 0; h < PL::kKItems + 1; ++h, ++seq) {
+                        const bool is_k = h < PL::kKItems;
+                        const CUtensorMap* map = is_k ? &p.tm_k : &p.tm_v;
+                        const int32_t x = is_k ? 64 * h : xv;
                         if (!rg.acquire(seq, aborted, p.err)) continue;
                         mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + (side ? 1024u : 0u));
-                        tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, y, zk);
-                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, y + kChunk, zk);
+                        tma_load_3d(rg.addr(seq), map, rg.full(seq), x, y, zk);
+                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), x, y + kChunk, zk);
                         if constexpr (kFrac) {
                             if (side)
                                 tma_load_3d(rg.addr(seq) + ring::kSlotBytes, h == 0 ? &p.tm_k8 : &p.tm_v8,
@@ -255,31 +297,45 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);
             const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x, ++tcount) {
-                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer);
-                const Plan pl = make_plan(p, tl.layer, tl.row0);
+                int half;
+                const ring::Tile tl = tile_at<kWide>(p, idx, half);
+                const PL pl = make_plan<kWide>(p, tl.layer, tl.row0);
                 // TMEM of the previous tile read out (and its PV finished) before S is rewritten
                 if (tcount > 0) mbar_wait(B_T, (tcount - 1) & 1, aborted, p.err);
                 for (int g = 0; g < pl.n_groups; ++g, ++gcount) {
                     const int nch = pl.nch(g);
                     const int ns = pl.band_slots(g);
-                    const uint32_t qseq = seq, kseq = seq + 1, vseq = seq + 1 + ns;
+                    const int nk = pl.k_slots(g);
+                    const uint32_t qseq = seq, kseq = seq + PL::kQItems, vseq = kseq + nk;
                     seq += pl.group_items(g);
-                    const uint32_t qaddr = rg.addr(qseq);
                     if (g > 0) mbar_wait(B_O, (gcount - 1) & 1, aborted, p.err);  // P of g-1 consumed
-                    rg.wait_full(qseq, aborted, p.err);
-                    for (int j = 0; j < ns; ++j) rg.wait_full(kseq + j, aborted, p.err);
+                    for (int j = 0; j < PL::kQItems; ++j) rg.wait_full(qseq + j, aborted, p.err);
+                    for (int j = 0; j < nk; ++j) rg.wait_full(kseq + j, aborted, p.err);
                     tc_fence_after();
                     for (int c = 0; c < nch; ++c) {
-                        const uint32_t kaddr = rg.addr(kseq + c / 2) + (c & 1) * kChunkBytes;
+                        if constexpr (kWide) {
+                            // K-dim 128: Q half 0 against the chunk's columns 0-63, then half 1
+                            const uint32_t kaddr = rg.addr(kseq + c);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + 64 * c, sdesc_sw128(qaddr + 32 * kk, 16, 1024),
-                                   sdesc_sw128(kaddr + 32 * kk, 16, 1024), idesc_s, kk > 0);
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_ss(tmem + 64 * c,
+                                       sdesc_sw128(rg.addr(qseq + (kk >> 2)) + 32 * (kk & 3), 16, 1024),
+                                       sdesc_sw128(kaddr + (kk >> 2) * kChunkBytes + 32 * (kk & 3), 16, 1024),
+                                       idesc_s, kk > 0);
+                        } else {
+                            const uint32_t qaddr = rg.addr(qseq);
+                            const uint32_t kaddr = rg.addr(kseq + c / 2) + (c & 1) * kChunkBytes;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tmem + 64 * c, sdesc_sw128(qaddr + 32 * kk, 16, 1024),
+                                       sdesc_sw128(kaddr + 32 * kk, 16, 1024), idesc_s, kk > 0);
+                        }
                     }
                     mma_commit(B_S);
-                    for (int j = 0; j < ns; ++j) rg.release_mma(kseq + j);
+                    for (int j = 0; j < nk; ++j) rg.release_mma(kseq + j);
                     // the last group's Q copy is released by the row warps once they hold q
-                    if (g < pl.n_groups - 1) rg.release_mma(qseq);
+                    if (g < pl.n_groups - 1)
+                        for (int j = 0; j < PL::kQItems; ++j) rg.release_mma(qseq + j);
                     mbar_wait(B_P, gcount & 1, aborted, p.err);
                     tc_fence_after();
                     for (int j = 0; j < ns; ++j) rg.wait_full(vseq + j, aborted, p.err);
@@ -294,7 +350,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                     mma_commit(B_O);
                     for (int j = 0; j < ns; ++j) rg.release_mma(vseq + j);
                 }
-                seq += 2 * pl.n_act + 1;  // offset and staging slots are the row threads'
+                seq += (PL::kKItems + 1) * pl.n_act + 1;  // offset and staging slots are the row threads'
             }
             // teardown: the last commit must have landed before TMEM is released
             if (gcount > 0) mbar_wait(B_O, (gcount - 1) & 1, aborted, p.err);
@@ -306,8 +362,9 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
         const float sl2 = p.scale_log2;
         uint32_t seq = 0, gbase = 0, tcount = 0;
         for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x, ++tcount) {
-            const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer);
-            const Plan pl = make_plan(p, tl.layer, tl.row0);
+            int half;
+            const ring::Tile tl = tile_at<kWide>(p, idx, half);
+            const PL pl = make_plan<kWide>(p, tl.layer, tl.row0);
             const int32_t i0 = pl.i0, c_lo = pl.c_lo, n_chunks = pl.n_chunks, n_groups = pl.n_groups;
             const int32_t i = i0 + r;
             const int32_t z = (int32_t)tl.zl;
@@ -398,17 +455,19 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             // q row into registers, then the Q slot goes back to the producer (every S MMA
             // reading it has completed: B_S was waited for each group). Holding the slot through
             // the offsets would stall the in-order ring.
-            uint32_t qw[32];
-            rg.wait_full(qseq, aborted, p.err);
-            {
-                const uint8_t* qrow = slot_ptr(qseq);
+            uint32_t qw[32 * PL::kQItems];  // head size 128: both halves
+#pragma unroll
+            for (int qh = 0; qh < PL::kQItems; ++qh) {
+                rg.wait_full(qseq + qh, aborted, p.err);
+                const uint8_t* qrow = slot_ptr(qseq + qh);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 w = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
-                    qw[4 * c + 0] = w.x; qw[4 * c + 1] = w.y; qw[4 * c + 2] = w.z; qw[4 * c + 3] = w.w;
+                    qw[32 * qh + 4 * c + 0] = w.x; qw[32 * qh + 4 * c + 1] = w.y;
+                    qw[32 * qh + 4 * c + 2] = w.z; qw[32 * qh + 4 * c + 3] = w.w;
                 }
+                rg.release_warp(qseq + qh, lane);
             }
-            rg.release_warp(qseq, lane);
             mbar_wait(B_L, tcount & 1, aborted, p.err);
             float m_o = m_b, l_o = 0.f;
             float oacc[64];
@@ -420,33 +479,42 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                 float wk = 0.f;  // weight of row r + 1 (fractional mode); uniform over the CTA
                 if constexpr (kFrac) wk = p.w[tl.layer][k];
                 const bool lerp = kFrac && wk != 0.f;
-                rg.wait_full(seq, aborted, p.err);
-                const uint8_t* krow = slot_ptr(seq);
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                float s = 0.f;
+                {
+                    // the row dot over the K item(s): head size 128 takes its two halves
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
-                    fma2_bf16(qw[4 * c + 0], w.x, a0, a1);
-                    fma2_bf16(qw[4 * c + 1], w.y, a2, a3);
-                    fma2_bf16(qw[4 * c + 2], w.z, a0, a1);
-                    fma2_bf16(qw[4 * c + 3], w.w, a2, a3);
-                }
-                float s = (a0 + a1) + (a2 + a3);
-                if (lerp) {
-                    // row r + 1 of the item (row 128 is the first of the 8 extra rows)
-                    float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+                    for (int kh = 0; kh < PL::kKItems; ++kh) {
+                        rg.wait_full(seq, aborted, p.err);
+                        const uint8_t* krow = slot_ptr(seq);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r + 1, c));
-                        fma2_bf16(qw[4 * c + 0], w.x, b0, b1);
-                        fma2_bf16(qw[4 * c + 1], w.y, b2, b3);
-                        fma2_bf16(qw[4 * c + 2], w.z, b0, b1);
-                        fma2_bf16(qw[4 * c + 3], w.w, b2, b3);
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
+                            fma2_bf16(qw[32 * kh + 4 * c + 0], w.x, a0, a1);
+                            fma2_bf16(qw[32 * kh + 4 * c + 1], w.y, a2, a3);
+                            fma2_bf16(qw[32 * kh + 4 * c + 2], w.z, a0, a1);
+                            fma2_bf16(qw[32 * kh + 4 * c + 3], w.w, a2, a3);
+                        }
+                        if (kh == PL::kKItems - 1) {
+                            s = (a0 + a1) + (a2 + a3);
+                            if (lerp) {
+                                // row r + 1 of the item (row 128 is the first of the 8 extra rows)
+                                float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r + 1, c));
+                                    fma2_bf16(qw[4 * c + 0], w.x, b0, b1);
+                                    fma2_bf16(qw[4 * c + 1], w.y, b2, b3);
+                                    fma2_bf16(qw[4 * c + 2], w.z, b0, b1);
+                                    fma2_bf16(qw[4 * c + 3], w.w, b2, b3);
+                                }
+                                s = fmaf(wk, ((b0 + b1) + (b2 + b3)) - s, s);
+                            }
+                        }
+                        rg.release_warp(seq, lane);
+                        ++seq;
                     }
-                    s = fmaf(wk, ((b0 + b1) + (b2 + b3)) - s, s);
                 }
-                rg.release_warp(seq, lane);
-                ++seq;
                 const float sc = valid ? s * sl2 : -INFINITY;
                 if (sc > m_o + 8.f) {
                     const float corr = m_o == -INFINITY ? 0.f : ex2(m_o - sc);
@@ -521,13 +589,14 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             __syncwarp();
             if (lane == 0) mbar_arrive(B_T);  // TMEM free for the next tile's MMAs
             gbase += n_groups;
-            if (i < T) p.lse[tl.zl * T + i] = (m + lg2(l)) * 0.69314718055994531f;
+            if (i < T && half == 0) p.lse[tl.zl * T + i] = (m + lg2(l)) * 0.69314718055994531f;
             fence_proxy_async_smem();
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (tid == 0) {
                 if (!aborted) {
-                    tma_store_3d(&p.tm_o, rg.addr(oseq), 0, i0, z);
-                    if (i0 + kChunk < T) tma_store_3d(&p.tm_o, rg.addr(oseq) + kChunkBytes, 0, i0 + kChunk, z);
+                    const int32_t xo = 64 * half;  // the CTA's output columns
+                    tma_store_3d(&p.tm_o, rg.addr(oseq), xo, i0, z);
+                    if (i0 + kChunk < T) tma_store_3d(&p.tm_o, rg.addr(oseq) + kChunkBytes, xo, i0 + kChunk, z);
                     tma_store_commit();
                     tma_store_wait_read0();
                 }
@@ -548,13 +617,15 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
 
 namespace {
 
-template <bool kFrac>
+template <bool kFrac, bool kWide>
 fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                           const AttnShape& sh, const OffsetTables& t,
                           const float (*w)[kMaxOffsets], const char* name, cudaStream_t st) {
     const int64_t slices = sh.slices_per_layer * sh.n_layers;
     const int32_t tiles = (sh.T + kRows - 1) / kRows;
-    if (slices > 0x7fffffff || (int64_t)tiles * slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    const int64_t halves = kWide ? 2 : 1;  // CTAs per tile
+    if (slices > 0x7fffffff || (int64_t)tiles * slices * halves > 0x7fffffff)
+        return FIBATTN_ERR_INVALID_ARG;
     FwdArgs<kFrac> P;
     // the error-word lookup is a runtime call: it binds the device's primary context to this
     // thread (a fresh thread may have none), which the tensor-map encoding below needs
@@ -564,7 +635,9 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
     const void* bases[4] = {q, k, v, o};
     CUtensorMap* maps[4] = {&P.tm_q, &P.tm_k, &P.tm_v, &P.tm_o};
     for (int m = 0; m < 4; ++m) {
-        const int r = make_bf16_rows_map(maps[m], bases[m], (m == 1 || m == 2) ? slices_kv : slices, sh.T);
+        const int64_t sl = (m == 1 || m == 2) ? slices_kv : slices;
+        const int r = kWide ? make_bf16_rows_map_d(maps[m], bases[m], sl, sh.T, 128)
+                            : make_bf16_rows_map(maps[m], bases[m], sl, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (fwd)");
     }
     if constexpr (kFrac) {
@@ -578,7 +651,7 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
     P.slices_per_layer = (uint32_t)sh.slices_per_layer;
     P.group = (uint32_t)sh.group;
     P.slices_per_layer_kv = (uint32_t)(sh.slices_per_layer / sh.group);
-    P.total_tiles = (uint32_t)((int64_t)tiles * slices);
+    P.total_tiles = (uint32_t)((int64_t)tiles * slices * halves);
     P.T = sh.T;
     P.W = sh.W;
     P.tiles_per_slice = tiles;
@@ -591,8 +664,8 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
     static int n_sm[64] = {};
     if (dev < 0 || dev >= 64) return FIBATTN_ERR_UNSUPPORTED;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel<kFrac>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_alloc<kFrac>());
+        e = cudaFuncSetAttribute(fwd_tc_kernel<kFrac, kWide>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc<kFrac>());
         if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaFuncSetAttribute (fwd)");
         e = cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaDeviceGetAttribute");
@@ -601,7 +674,7 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
     const int64_t grid = (int64_t)P.total_tiles < 2LL * n_sm[dev] ? (int64_t)P.total_tiles : 2LL * n_sm[dev];
     {
         KernelScope ks(name, st);
-        fwd_tc_kernel<kFrac><<<(unsigned)grid, kThreads, smem_alloc<kFrac>(), st>>>(P);
+        fwd_tc_kernel<kFrac, kWide><<<(unsigned)grid, kThreads, smem_alloc<kFrac>(), st>>>(P);
     }
     return launch_status(name);
 }
@@ -610,13 +683,19 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
 
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
-    return launch_fwd<false>(q, k, v, o, lse, sh, t, nullptr, "fwd_tc_bf16", st);
+    return launch_fwd<false, false>(q, k, v, o, lse, sh, t, nullptr, "fwd_tc_bf16", st);
+}
+
+fibattn_status launch_fwd_tc128_bf16(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, const AttnShape& sh, const OffsetTables& t,
+                                     cudaStream_t st) {
+    return launch_fwd<false, true>(q, k, v, o, lse, sh, t, nullptr, "fwd_tc128_bf16", st);
 }
 
 fibattn_status launch_fwd_frac_tc_bf16(const void* q, const void* k, const void* v, void* o,
                                        float* lse, const AttnShape& sh, const FracTables& t,
                                        cudaStream_t st) {
-    return launch_fwd<true>(q, k, v, o, lse, sh, t.c, t.w, "fwd_frac_tc_bf16", st);
+    return launch_fwd<true, false>(q, k, v, o, lse, sh, t.c, t.w, "fwd_frac_tc_bf16", st);
 }
 
 }  // namespace fibattn

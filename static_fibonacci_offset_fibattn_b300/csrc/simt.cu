@@ -1,8 +1,9 @@
 // simt.cu -- SIMT (CUDA-core) kernels: the fp32 forward and the backward.
 //
-// One warp owns one row; lane l holds head dims 2l and 2l+1 (d = 64), so every K/V/Q
-// row is read by one coalesced warp access and dot products finish with an xor
-// shuffle reduction (every lane receives the sum, bit-identically).
+// One warp owns one row; lane l holds head dims N l .. N l + N - 1 (N = d / 32: 2 at d = 64,
+// 4 at d = 128), so every K/V/Q row is read by one coalesced warp access and dot products
+// finish with an xor shuffle reduction (every lane receives the sum, bit-identically). The
+// fractional-offset kernels are written for d = 64.
 //
 // Attended set ("Depth-Staggered Fibonacci Spacing for Sparse Attention", gist.science
 // explainer, Metodologia / Arquitetura, "Conjunto Atendido"): query i sees keys
@@ -33,21 +34,76 @@ struct Io<float> {
     }
 };
 
-template <>
-struct Io<__nv_bfloat16> {
-    static __device__ __forceinline__ float2 ld(const __nv_bfloat16* p) {
-        __nv_bfloat162 h = __ldg(reinterpret_cast<const __nv_bfloat162*>(p));
-        return __bfloat1622float2(h);
-    }
-    static __device__ __forceinline__ void st(__nv_bfloat16* p, float2 x) {
-        *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(x);
-    }
-};
 
 // Element offset of the kv slice read by query slice `s` of launch layer `layer` (query head h
 // of batch b reads kv head h / group of batch b; K/V hold slices_per_layer / group slices).
-__device__ __forceinline__ int64_t kv_base(const AttnShape& sh, int layer, int64_t s) {
-    return ((int64_t)layer * (sh.slices_per_layer / sh.group) + s / sh.group) * sh.T * 64;
+__device__ __forceinline__ int64_t kv_base(const AttnShape& sh, int layer, int64_t s, int d = 64) {
+    return ((int64_t)layer * (sh.slices_per_layer / sh.group) + s / sh.group) * sh.T * d;
+}
+
+// N consecutive elements of a row in fp32 registers (N = 2 or 4).
+template <int N>
+struct Vec {
+    float x[N];
+};
+
+template <typename E, int N>
+struct VIo;
+template <>
+struct VIo<float, 2> {
+    static __device__ __forceinline__ Vec<2> ld(const float* p) {
+        const float2 a = __ldg(reinterpret_cast<const float2*>(p));
+        return Vec<2>{{a.x, a.y}};
+    }
+    static __device__ __forceinline__ void st(float* p, const Vec<2>& v) {
+        *reinterpret_cast<float2*>(p) = make_float2(v.x[0], v.x[1]);
+    }
+};
+template <>
+struct VIo<float, 4> {
+    static __device__ __forceinline__ Vec<4> ld(const float* p) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        return Vec<4>{{a.x, a.y, a.z, a.w}};
+    }
+    static __device__ __forceinline__ void st(float* p, const Vec<4>& v) {
+        *reinterpret_cast<float4*>(p) = make_float4(v.x[0], v.x[1], v.x[2], v.x[3]);
+    }
+};
+template <>
+struct VIo<__nv_bfloat16, 2> {
+    static __device__ __forceinline__ Vec<2> ld(const __nv_bfloat16* p) {
+        const float2 a = __bfloat1622float2(__ldg(reinterpret_cast<const __nv_bfloat162*>(p)));
+        return Vec<2>{{a.x, a.y}};
+    }
+    static __device__ __forceinline__ void st(__nv_bfloat16* p, const Vec<2>& v) {
+        *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(make_float2(v.x[0], v.x[1]));
+    }
+};
+template <>
+struct VIo<__nv_bfloat16, 4> {
+    static __device__ __forceinline__ Vec<4> ld(const __nv_bfloat16* p) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        return Vec<4>{{a.x, a.y, b.x, b.y}};
+    }
+    static __device__ __forceinline__ void st(__nv_bfloat16* p, const Vec<4>& v) {
+        const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v.x[0], v.x[1]));
+        const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(v.x[2], v.x[3]));
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&a);
+        u.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(p) = u;
+    }
+};
+
+// this lane's part of a . b (the N = 2 form is the two-term sum x0 y0 + x1 y1)
+template <int N>
+__device__ __forceinline__ float dot_part(const Vec<N>& a, const Vec<N>& b) {
+    float s = a.x[0] * b.x[0] + a.x[1] * b.x[1];
+#pragma unroll
+    for (int t = 2; t < N; t += 2) s += a.x[t] * b.x[t] + a.x[t + 1] * b.x[t + 1];
+    return s;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -58,11 +114,12 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // ---------------------------------------------------------------- forward (fp32 path)
 // Online softmax over S_i in fp32: running max m, running sum l, accumulator acc.
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 fwd_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
                 E* __restrict__ o, float* __restrict__ lse, AttnShape sh,
                 const __grid_constant__ OffsetTables tab) {
+    constexpr int N = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t rows = sh.slices_per_layer * sh.T;
     const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -70,22 +127,24 @@ fwd_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
     if (row >= rows) return;
     const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
     const int32_t i = (int32_t)(row % sh.T);
-    const int64_t base = slice * sh.T * kD;
-    const int64_t kbase = kv_base(sh, layer, row / sh.T);
-    const float2 qv = Io<E>::ld(q + base + (int64_t)i * kD + 2 * lane);
+    const int64_t base = slice * sh.T * D;
+    const int64_t kbase = kv_base(sh, layer, row / sh.T, D);
+    const Vec<N> qv = VIo<E, N>::ld(q + base + (int64_t)i * D + N * lane);
 
     float m = -INFINITY, l = 0.f;
-    float2 acc = make_float2(0.f, 0.f);
+    Vec<N> acc;
+#pragma unroll
+    for (int t = 0; t < N; ++t) acc.x[t] = 0.f;
     auto visit = [&](int32_t j) {
-        const float2 kv = Io<E>::ld(k + kbase + (int64_t)j * kD + 2 * lane);
-        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y) * sh.scale;
-        const float2 vv = Io<E>::ld(v + kbase + (int64_t)j * kD + 2 * lane);
+        const Vec<N> kv = VIo<E, N>::ld(k + kbase + (int64_t)j * D + N * lane);
+        const float s = warp_sum(dot_part(qv, kv)) * sh.scale;
+        const Vec<N> vv = VIo<E, N>::ld(v + kbase + (int64_t)j * D + N * lane);
         const float mn = fmaxf(m, s);
         const float corr = expf(m - mn);  // m = -inf on the first key: corr = 0
         const float p = expf(s - mn);
         l = l * corr + p;
-        acc.x = acc.x * corr + p * vv.x;
-        acc.y = acc.y * corr + p * vv.y;
+#pragma unroll
+        for (int t = 0; t < N; ++t) acc.x[t] = acc.x[t] * corr + p * vv.x[t];
         m = mn;
     };
     const int n_off = tab.count[layer];
@@ -97,7 +156,9 @@ fwd_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
     for (int32_t j = j0; j <= i; ++j) visit(j);
 
     const float inv = 1.f / l;
-    Io<E>::st(o + base + (int64_t)i * kD + 2 * lane, make_float2(acc.x * inv, acc.y * inv));
+#pragma unroll
+    for (int t = 0; t < N; ++t) acc.x[t] *= inv;
+    VIo<E, N>::st(o + base + (int64_t)i * D + N * lane, acc);
     if (lane == 0) lse[slice * sh.T + i] = m + logf(l);
 }
 
@@ -156,26 +217,28 @@ fwd_frac_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* 
 
 // ---------------------------------------------------------------- backward
 // D_i = dO_i . O_i
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __restrict__ delta,
                  int64_t total_rows) {
+    constexpr int N = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (row >= total_rows) return;
-    const float2 a = Io<E>::ld(o + row * kD + 2 * lane);
-    const float2 b = Io<E>::ld(dO + row * kD + 2 * lane);
-    const float s = warp_sum(a.x * b.x + a.y * b.y);
+    const Vec<N> a = VIo<E, N>::ld(o + row * D + N * lane);
+    const Vec<N> b = VIo<E, N>::ld(dO + row * D + N * lane);
+    const float s = warp_sum(dot_part(a, b));
     if (lane == 0) delta[row] = s;
 }
 
 // dQ_i = scale * sum_{j in S_i} P_ij (dO_i . v_j - D_i) k_j   (query owner)
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 bwd_dq_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
               const float* __restrict__ lse, const E* __restrict__ dO,
               const float* __restrict__ delta, E* __restrict__ dq, AttnShape sh,
               const __grid_constant__ OffsetTables tab) {
+    constexpr int N = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t rows = sh.slices_per_layer * sh.T;
     const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -183,24 +246,26 @@ bwd_dq_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restr
     if (row >= rows) return;
     const int64_t slice = (int64_t)layer * sh.slices_per_layer + row / sh.T;
     const int32_t i = (int32_t)(row % sh.T);
-    const int64_t base = slice * sh.T * kD;
-    const int64_t ri = base + (int64_t)i * kD + 2 * lane;
-    const float2 qv = Io<E>::ld(q + ri);
-    const float2 gv = Io<E>::ld(dO + ri);
+    const int64_t base = slice * sh.T * D;
+    const int64_t ri = base + (int64_t)i * D + N * lane;
+    const Vec<N> qv = VIo<E, N>::ld(q + ri);
+    const Vec<N> gv = VIo<E, N>::ld(dO + ri);
     const float Li = lse[slice * sh.T + i];
     const float Di = delta[slice * sh.T + i];
-    const int64_t kbase = kv_base(sh, layer, row / sh.T);
-    float2 acc = make_float2(0.f, 0.f);
+    const int64_t kbase = kv_base(sh, layer, row / sh.T, D);
+    Vec<N> acc;
+#pragma unroll
+    for (int t = 0; t < N; ++t) acc.x[t] = 0.f;
     auto visit = [&](int32_t j) {
-        const int64_t rj = kbase + (int64_t)j * kD + 2 * lane;
-        const float2 kv = Io<E>::ld(k + rj);
-        const float2 vv = Io<E>::ld(v + rj);
-        const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
-        const float dp = warp_sum(gv.x * vv.x + gv.y * vv.y);
+        const int64_t rj = kbase + (int64_t)j * D + N * lane;
+        const Vec<N> kv = VIo<E, N>::ld(k + rj);
+        const Vec<N> vv = VIo<E, N>::ld(v + rj);
+        const float s = warp_sum(dot_part(qv, kv));
+        const float dp = warp_sum(dot_part(gv, vv));
         const float p = expf(s * sh.scale - Li);
         const float ds = p * (dp - Di);
-        acc.x += ds * kv.x;
-        acc.y += ds * kv.y;
+#pragma unroll
+        for (int t = 0; t < N; ++t) acc.x[t] += ds * kv.x[t];
     };
     for (int e = tab.count[layer] - 1; e >= 0; --e) {
         const int32_t j = i - tab.off[layer][e];
@@ -208,19 +273,22 @@ bwd_dq_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restr
     }
     const int32_t j0 = i - sh.W + 1 > 0 ? i - sh.W + 1 : 0;
     for (int32_t j = j0; j <= i; ++j) visit(j);
-    Io<E>::st(dq + ri, make_float2(acc.x * sh.scale, acc.y * sh.scale));
+#pragma unroll
+    for (int t = 0; t < N; ++t) acc.x[t] *= sh.scale;
+    VIo<E, N>::st(dq + ri, acc);
 }
 
 // dK_j = scale * sum_{i : j in S_i} dS_ij q_i,  dV_j = sum_{i : j in S_i} P_ij dO_i  (key owner)
 // The queries that see key j: i = j + t for 0 <= t < W, and i = j + o for table offsets o,
 // each only while i < T, in each of the `group` query heads that read this kv head. One warp
 // per kv row; no atomics: this warp is the only writer of row j.
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 bwd_dkdv_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __restrict__ v,
                 const float* __restrict__ lse, const E* __restrict__ dO,
                 const float* __restrict__ delta, E* __restrict__ dk, E* __restrict__ dv,
                 AttnShape sh, const __grid_constant__ OffsetTables tab) {
+    constexpr int N = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t spl_kv = sh.slices_per_layer / sh.group;
     const int64_t rows = spl_kv * sh.T;
@@ -229,25 +297,28 @@ bwd_dkdv_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
     if (row >= rows) return;
     const int64_t skv = row / sh.T;  // kv slice within the layer
     const int32_t j = (int32_t)(row % sh.T);
-    const int64_t rj = ((int64_t)layer * spl_kv + skv) * sh.T * kD + (int64_t)j * kD + 2 * lane;
-    const float2 kv = Io<E>::ld(k + rj);
-    const float2 vv = Io<E>::ld(v + rj);
-    float2 ak = make_float2(0.f, 0.f), av = make_float2(0.f, 0.f);
+    const int64_t rj = ((int64_t)layer * spl_kv + skv) * sh.T * D + (int64_t)j * D + N * lane;
+    const Vec<N> kv = VIo<E, N>::ld(k + rj);
+    const Vec<N> vv = VIo<E, N>::ld(v + rj);
+    Vec<N> ak, av;
+#pragma unroll
+    for (int t = 0; t < N; ++t) ak.x[t] = av.x[t] = 0.f;
     for (int g = 0; g < sh.group; ++g) {
         const int64_t slice = (int64_t)layer * sh.slices_per_layer + skv * sh.group + g;
-        const int64_t base = slice * sh.T * kD;
+        const int64_t base = slice * sh.T * D;
         auto visit = [&](int32_t i) {
-            const int64_t ri = base + (int64_t)i * kD + 2 * lane;
-            const float2 qv = Io<E>::ld(q + ri);
-            const float2 gv = Io<E>::ld(dO + ri);
-            const float s = warp_sum(qv.x * kv.x + qv.y * kv.y);
-            const float dp = warp_sum(gv.x * vv.x + gv.y * vv.y);
+            const int64_t ri = base + (int64_t)i * D + N * lane;
+            const Vec<N> qv = VIo<E, N>::ld(q + ri);
+            const Vec<N> gv = VIo<E, N>::ld(dO + ri);
+            const float s = warp_sum(dot_part(qv, kv));
+            const float dp = warp_sum(dot_part(gv, vv));
             const float p = expf(s * sh.scale - lse[slice * sh.T + i]);
             const float ds = p * (dp - delta[slice * sh.T + i]);
-            av.x += p * gv.x;
-            av.y += p * gv.y;
-            ak.x += ds * qv.x;
-            ak.y += ds * qv.y;
+#pragma unroll
+            for (int t = 0; t < N; ++t) {
+                av.x[t] += p * gv.x[t];
+                ak.x[t] += ds * qv.x[t];
+            }
         };
         const int32_t i1 = j + sh.W - 1 < sh.T - 1 ? j + sh.W - 1 : sh.T - 1;
         for (int32_t i = j; i <= i1; ++i) visit(i);
@@ -256,8 +327,10 @@ bwd_dkdv_kernel(const E* __restrict__ q, const E* __restrict__ k, const E* __res
             if (i < sh.T) visit((int32_t)i);
         }
     }
-    Io<E>::st(dk + rj, make_float2(ak.x * sh.scale, ak.y * sh.scale));
-    Io<E>::st(dv + rj, av);
+#pragma unroll
+    for (int t = 0; t < N; ++t) ak.x[t] *= sh.scale;
+    VIo<E, N>::st(dk + rj, ak);
+    VIo<E, N>::st(dv + rj, av);
 }
 
 // ---------------------------------------------------------------- fractional backward
@@ -421,7 +494,7 @@ fibattn_status launch_bwd_frac_simt_f32(const float* q, const float* k, const fl
     if (blocks > 0x7fffffff || dblocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     {
         KernelScope ks("bwd_delta_simt", st);
-        bwd_delta_kernel<float><<<(unsigned)dblocks, kWarpsPerBlock * 32, 0, st>>>(o, dO, delta, all_rows);
+        bwd_delta_kernel<float, 64><<<(unsigned)dblocks, kWarpsPerBlock * 32, 0, st>>>(o, dO, delta, all_rows);
     }
     dim3 grid((unsigned)blocks, sh.n_layers);
     {
@@ -448,7 +521,10 @@ fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* 
     if (blocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     dim3 grid((unsigned)blocks, sh.n_layers);
     KernelScope ks("fwd_simt_f32", st);
-    fwd_simt_kernel<float><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, o, lse, sh, t);
+    if (sh.d == 128)
+        fwd_simt_kernel<float, 128><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, o, lse, sh, t);
+    else
+        fwd_simt_kernel<float, 64><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, o, lse, sh, t);
     return launch_status("launch SIMT kernel");
 }
 
@@ -461,8 +537,12 @@ fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v,
     if (blocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     dim3 grid((unsigned)blocks, sh.n_layers);
     KernelScope ks("fwd_simt_bf16", st);
-    fwd_simt_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(
-        (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
+    if (sh.d == 128)
+        fwd_simt_kernel<E, 128><<<grid, kWarpsPerBlock * 32, 0, st>>>(
+            (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
+    else
+        fwd_simt_kernel<E, 64><<<grid, kWarpsPerBlock * 32, 0, st>>>(
+            (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
     return launch_status("launch SIMT kernel");
 }
 
@@ -478,7 +558,7 @@ fibattn_status launch_fwd_frac_simt_f32(const float* q, const float* k, const fl
     return launch_status("launch SIMT kernel");
 }
 
-template <typename E>
+template <typename E, int D>
 static fibattn_status bwd_typed(const E* q, const E* k, const E* v, const E* o, const float* lse,
                                 const E* dO, E* dq, E* dk, E* dv, float* delta,
                                 const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
@@ -489,19 +569,19 @@ static fibattn_status bwd_typed(const E* q, const E* k, const E* v, const E* o, 
     if (blocks > 0x7fffffff || dblocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     {
         KernelScope ks("bwd_delta_simt", st);
-        bwd_delta_kernel<E><<<(unsigned)dblocks, kWarpsPerBlock * 32, 0, st>>>(o, dO, delta, all_rows);
+        bwd_delta_kernel<E, D><<<(unsigned)dblocks, kWarpsPerBlock * 32, 0, st>>>(o, dO, delta, all_rows);
     }
     dim3 grid((unsigned)blocks, sh.n_layers);
     {
         KernelScope ks("bwd_dq_simt", st);
-        bwd_dq_kernel<E><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dq, sh, t);
+        bwd_dq_kernel<E, D><<<grid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dq, sh, t);
     }
     {
         // one warp per kv row
         const int64_t kv_rows = sh.slices_per_layer / sh.group * sh.T;
         dim3 kgrid((unsigned)((kv_rows + kWarpsPerBlock - 1) / kWarpsPerBlock), sh.n_layers);
         KernelScope ks("bwd_dkdv_simt", st);
-        bwd_dkdv_kernel<E><<<kgrid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dk, dv, sh, t);
+        bwd_dkdv_kernel<E, D><<<kgrid, kWarpsPerBlock * 32, 0, st>>>(q, k, v, lse, dO, delta, dk, dv, sh, t);
     }
     return launch_status("launch SIMT kernel");
 }
@@ -510,7 +590,20 @@ fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* 
                                    const float* lse, const float* dO, float* dq, float* dk,
                                    float* dv, float* delta, const AttnShape& sh,
                                    const OffsetTables& t, cudaStream_t st) {
-    return bwd_typed<float>(q, k, v, o, lse, dO, dq, dk, dv, delta, sh, t, st);
+    if (sh.d == 128) return bwd_typed<float, 128>(q, k, v, o, lse, dO, dq, dk, dv, delta, sh, t, st);
+    return bwd_typed<float, 64>(q, k, v, o, lse, dO, dq, dk, dv, delta, sh, t, st);
+}
+
+fibattn_status launch_bwd_simt_bf16(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dO, void* dq, void* dk,
+                                    void* dv, float* delta, const AttnShape& sh,
+                                    const OffsetTables& t, cudaStream_t st) {
+    typedef __nv_bfloat16 E;
+    if (sh.d == 128)
+        return bwd_typed<E, 128>((const E*)q, (const E*)k, (const E*)v, (const E*)o, lse,
+                                 (const E*)dO, (E*)dq, (E*)dk, (E*)dv, delta, sh, t, st);
+    return bwd_typed<E, 64>((const E*)q, (const E*)k, (const E*)v, (const E*)o, lse,
+                            (const E*)dO, (E*)dq, (E*)dk, (E*)dv, delta, sh, t, st);
 }
 
 }  // namespace fibattn

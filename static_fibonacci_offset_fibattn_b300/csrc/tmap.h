@@ -16,6 +16,10 @@ constexpr int kTmaBoxRows = 64;
 // make a runtime call that binds the device's primary context first.
 int make_bf16_rows_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T);
 
+// The same map over rows of d bf16 (d a multiple of 64): the box still spans 64 columns, a
+// copy takes the columns [x, x + 64) at an x that is a multiple of 64.
+int make_bf16_rows_map_d(CUtensorMap* m, const void* base, int64_t slices, int32_t T, int32_t d);
+
 // The same map with an 8-row box (1 KB): the rows just past a 128-row tile.
 int make_bf16_rows8_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T);
 

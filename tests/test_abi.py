@@ -127,7 +127,7 @@ def test_fwd_validates_before_launch():
     assert _fwd_raw(B=0) == fa.INVALID_ARG
     assert _fwd_raw(T=0) == fa.INVALID_ARG
     assert _fwd_raw(W=0) == fa.INVALID_ARG
-    assert _fwd_raw(d=128) == fa.UNSUPPORTED
+    assert _fwd_raw(d=96) == fa.UNSUPPORTED
     assert _fwd_raw(dtype=7) == fa.UNSUPPORTED
     assert _fwd_raw(n=2) == fa.INVALID_ARG  # schedule has one layer
     assert _fwd_raw(layer0=-1) == fa.INVALID_ARG

@@ -1,0 +1,82 @@
+"""GPU parity at head size 128 (the forward's two-CTA tensor-core mode for bf16, the SIMT
+kernels for fp32 and for the backward) against the oracle. Tolerances as at 64 (max-abs
+1e-5 fp32, 2e-2 bf16; lse 1e-5 / 1e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import fibattn_inputs as fi
+import oracle
+import static_fibonacci_offset_fibattn_b300 as fa
+from gpu_common import LSE_TOL, TOL, f64, lib_schedule, max_abs, oracle_table, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SCHED = dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16)
+
+D128 = [
+    # (Lc, B, H, Hkv, T, W)
+    (1, 1, 2, 2, 1, 4),
+    (1, 2, 2, 2, 127, 8),
+    (1, 1, 4, 4, 300, 16),
+    (2, 1, 2, 2, 1029, 64),     # ragged last tile
+    (1, 1, 4, 1, 640, 64),      # MQA
+    (1, 1, 2, 2, 700, 700),     # dense causal
+    (1, 2, 2, 2, 515, 100),     # W > 64
+]
+
+
+def _inputs(Lc, B, H, Hkv, T, dtype, seed):
+    kv = {n: (Lc, B, Hkv, T, 128) for n in ("k", "v")}
+    return fi.draw((Lc, B, H, T, 128), seed=seed, scale=0.35, dtype=dtype,
+                   names=("q", "k", "v", "dO"), shapes=kv)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", D128)
+def test_d128_fwd_bwd_matches_oracle(dtype, case):
+    Lc, B, H, Hkv, T, W = case
+    inp = _inputs(Lc, B, H, Hkv, T, dtype, 200 + T)
+    dev = to_dev(inp)
+    sc = lib_schedule(SCHED)
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], W, sc, layer0=6)
+    dq, dk, dv = fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], W, sc, layer0=6)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    tabs = [oracle_table(SCHED, 6 + l, W, T) for l in range(Lc)]
+    g = lambda n: f64(inp[n])
+    rq, rk, rv, ro, rl = oracle.bwd_gqa(g("q"), g("k"), g("v"), g("dO"), W, tabs)
+    assert max_abs(f64(o), ro) <= TOL[dtype]
+    assert max_abs(f64(lse), rl) <= LSE_TOL[dtype]
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert max_abs(f64(got), ref) <= TOL[dtype]
+
+
+def test_d128_fwd_sixteen_layers_sampled():
+    spec = fi.WORKLOADS["c3w"]
+    inp = fi.workload_inputs("c3w")
+    dev = to_dev(inp)
+    sc = lib_schedule(spec["sched"])
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], spec["W"], sc)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    for l in range(spec["Lc"]):
+        tab = oracle_table(spec["sched"], l, spec["W"], spec["T"])
+        b, h = l % spec["B"], (5 * l) % spec["H"]
+        ro, rl = oracle.fwd(f64(inp["q"][l, b, h]), f64(inp["k"][l, b, h]), f64(inp["v"][l, b, h]),
+                            spec["W"], tab)
+        assert max_abs(f64(o[l, b, h]), ro) <= TOL["bf16"], l
+        assert max_abs(f64(lse[l, b, h]), rl) <= LSE_TOL["bf16"], l
+
+
+def test_d128_deterministic_and_halves_consistent():
+    dev = to_dev(_inputs(1, 2, 2, 2, 1024, "bf16", 3))
+    sc = lib_schedule(SCHED)
+    a = fa.fwd(dev["q"], dev["k"], dev["v"], 64, sc)
+    b = fa.fwd(dev["q"], dev["k"], dev["v"], 64, sc)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    # the two output halves come from two CTAs that each compute the whole softmax: the
+    # halves of V swapped give the halves of O swapped
+    v2 = torch.cat((dev["v"][..., 64:], dev["v"][..., :64]), dim=-1).contiguous()
+    c = fa.fwd(dev["q"], dev["k"], v2, 64, sc)
+    assert torch.equal(c[0][..., :64], a[0][..., 64:]) and torch.equal(c[0][..., 64:], a[0][..., :64])
