@@ -60,6 +60,8 @@ ALGO_BYTES = {
     "bwd_dkdv_simt": 4 * 256 + 8 + 2 * 256,     # fp32: q, k, v, dO, lse, D in; dk, dv out
     "bwd_dq_tc": 5 * 128 + 4 + 128,             # q, k, v, o, dO, lse in; dq out
     "bwd_dkdv_tc": 4 * 128 + 4 + 2 * 128,       # q, k, v, dO, lse in; dk, dv out
+    "bwd_dq_tc128": 5 * 256 + 4 + 256,          # head size 128: rows of 256 B
+    "bwd_dkdv_tc128": 4 * 256 + 4 + 2 * 256,
     "bwd_dq_frac_tc": 5 * 128 + 4 + 128 + 4,    # as bwd_dq_tc, plus the dalpha partial out
     "bwd_dkdv_frac_tc": 4 * 128 + 4 + 2 * 128,
     "bwd_dq_frac_simt": 4 * 256 + 8 + 256 + 4,
@@ -70,7 +72,8 @@ ALGO_BYTES = {
 }
 # Rows per query token of each kernel that are k/v-shaped (k, v in; dk, dv out).
 KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_simt_bf16": 2, "fwd_tc128_bf16": 2, "bwd_dq_tc": 2,
-           "bwd_dkdv_tc": 4, "bwd_dq_simt": 2, "bwd_dkdv_simt": 4}
+           "bwd_dkdv_tc": 4, "bwd_dq_simt": 2, "bwd_dkdv_simt": 4, "bwd_dq_tc128": 2,
+           "bwd_dkdv_tc128": 4}
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
@@ -79,7 +82,8 @@ KERNEL_SRC = {
     "bwd_dq_frac_simt": "simt.cu", "bwd_dkdv_frac_simt": "simt.cu", "dalpha_reduce": "simt.cu",
     "rope_bf16": "rope.cu", "rope_f32": "rope.cu",
     "bwd_delta_simt": "simt.cu", "bwd_dq_simt": "simt.cu", "bwd_dkdv_simt": "simt.cu",
-    "bwd_dq_tc": "bwd_tc.cu", "bwd_dkdv_tc": "bwd_tc.cu",
+    "bwd_dq_tc": "bwd_tc.cu", "bwd_dkdv_tc": "bwd_tc.cu", "bwd_dq_tc128": "bwd_tc.cu",
+    "bwd_dkdv_tc128": "bwd_tc.cu",
 }
 
 

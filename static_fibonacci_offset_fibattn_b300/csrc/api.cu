@@ -78,10 +78,11 @@ BwdWorkspace workspace_layout(int32_t B, int32_t H, int32_t T, int32_t dtype, in
 }
 
 // Callers have validated the arguments (check_common), so every table builds. The tensor-core
-// layout is bf16 at d = 64; everything else runs the SIMT backward (D only).
+// layout is bf16 (d = 64 or 128); fp32 runs the SIMT backward (D only).
 BwdWorkspace bwd_workspace(int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
                            const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
-    if (dtype != FIBATTN_BF16 || d != 64)
+    (void)d;
+    if (dtype != FIBATTN_BF16)
         return workspace_layout(B, H, T, FIBATTN_F32, n_layers_call, 0, false);
     int32_t n_max = 0;
     for (int32_t c = 0; c < n_layers_call; ++c) {
@@ -313,13 +314,7 @@ fibattn_status bwd_common(const void* q, const void* k, const void* v, const voi
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t koff = (size_t)c * per_layer_kv * d * es;
         const size_t loff = (size_t)c * per_layer;
-        if (dtype == FIBATTN_BF16 && d != 64) {
-            st = launch_bwd_simt_bf16((const char*)q + off, (const char*)k + koff,
-                                      (const char*)v + koff, (const char*)o + off, lse + loff,
-                                      (const char*)dO + off, (char*)dq + off, (char*)dk + koff,
-                                      (char*)dv + koff, delta + loff, sh, t,
-                                      as_stream(cuda_stream));
-        } else if (dtype == FIBATTN_F32) {
+        if (dtype == FIBATTN_F32) {
             st = launch_bwd_simt_f32((const float*)((const char*)q + off),
                                      (const float*)((const char*)k + koff),
                                      (const float*)((const char*)v + koff),

@@ -113,7 +113,7 @@ __device__ __forceinline__ uint32_t bar_at(uint32_t sbase, uint32_t off, int idx
     return sbase + off + 8u * idx;
 }
 
-__device__ __forceinline__ void load_row_sw(const uint8_t* tile, int r, uint32_t (&w)[32]) {
+__device__ __forceinline__ void load_row_sw(const uint8_t* tile, int r, uint32_t* w) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         const uint4 x = *reinterpret_cast<const uint4*>(tile + sw128_off(r, c));
@@ -128,17 +128,21 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 64, kColP = 128;  // dQ accumulator in columns [0, 64)
 
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffDO = kOffQ + kTileBytes;
-constexpr uint32_t kOffK = kOffDO + kTileBytes;      // 2 stages x 8 KB
-constexpr uint32_t kOffV = kOffK + 2 * kChunkBytes;  // 2 stages x 8 KB
-constexpr uint32_t kOffRing = kOffV + 2 * kChunkBytes;
 // barriers: 0 q+dO, 1-2 band K/V full, 3 S/dP ready, 4 dS written (128), 5 dQ MMA done,
 // 6-7 ring full, 8-9 ring empty (128)
 constexpr int kNumBars = 10;
-// the two ring slots: a tile, plus (fractional mode) the 8 rows after it
-template <bool kFrac>
+// Shared memory: the Q and dO tiles, two stages of K and V chunks, the two ring slots (a
+// tile, plus in the fractional mode the 8 rows after it). Head size 128 (kWide) doubles the
+// tiles and the chunk stages (two 64-column halves each).
+template <bool kFrac, bool kWide = false>
 struct Layout {
+    static constexpr uint32_t kTileQ = kWide ? 2 * kTileBytes : kTileBytes;
+    static constexpr uint32_t kStage = kWide ? 2 * kChunkBytes : kChunkBytes;
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffDO = kOffQ + kTileQ;
+    static constexpr uint32_t kOffK = kOffDO + kTileQ;  // 2 stages
+    static constexpr uint32_t kOffV = kOffK + 2 * kStage;  // 2 stages
+    static constexpr uint32_t kOffRing = kOffV + 2 * kStage;
     static constexpr uint32_t kSlot = kTileBytes + (kFrac ? 1024u : 0u);
     static constexpr uint32_t kOffBar = kOffRing + 2 * kSlot;
     static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -146,22 +150,32 @@ struct Layout {
     static constexpr uint32_t kSmemAlloc = kOffRed + 16 + 1024;
 };
 
-template <bool kFrac>
-__global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_constant__ BwdArgs<kFrac> p) {
-    using L = Layout<kFrac>;
+// Head size 128 (kWide): two CTAs per tile (blockIdx.x = 2 * tile index + half); both form
+// the full S = Q K^T and dP = dO V^T (8 MMA k-steps over the two column halves) and the full
+// offset dots, and each accumulates dq for its own 64 output columns (dS K_half); half 0
+// alone writes D, lse log2(e) and the (P, dS) pairs.
+template <bool kFrac, bool kWide>
+__global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(const __grid_constant__ BwdArgs<kFrac> p) {
+    static_assert(!(kFrac && kWide), "the fractional mode is for head size 64");
+    using L = Layout<kFrac, kWide>;
     constexpr uint32_t kOffBar = L::kOffBar, kOffTmemSlot = L::kOffTmemSlot, kSlot = L::kSlot;
+    constexpr uint32_t kOffQ = L::kOffQ, kOffDO = L::kOffDO, kOffK = L::kOffK, kOffV = L::kOffV,
+                       kOffRing = L::kOffRing, kStage = L::kStage;
+    constexpr int kHalves = kWide ? 2 : 1;  // 64-column halves of a row
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int layer = blockIdx.y;
-    const int tile = blockIdx.x % p.tiles_per_slice;
-    const int64_t zl = (int64_t)layer * p.slices_per_layer + blockIdx.x / p.tiles_per_slice;
+    const int half = kWide ? (int)(blockIdx.x & 1u) : 0;
+    const uint32_t bt = kWide ? blockIdx.x >> 1 : blockIdx.x;
+    const int tile = bt % p.tiles_per_slice;
+    const int64_t zl = (int64_t)layer * p.slices_per_layer + bt / p.tiles_per_slice;
     const int32_t z = (int32_t)zl;
     // the kv slice: query head h of batch b reads kv head h / group
     const int32_t zk = (int32_t)((int64_t)layer * p.slices_per_layer_kv32 +
-                                 (uint32_t)(blockIdx.x / p.tiles_per_slice) / p.group);
+                                 (uint32_t)(bt / p.tiles_per_slice) / p.group);
     const int32_t T = p.T, W = p.W;
     const int32_t i0 = tile * kRows;
 
@@ -202,17 +216,22 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
             prefetch_tmap(&p.tm_do);
             prefetch_tmap(&p.tm_k);
             prefetch_tmap(&p.tm_v);
-            mbar_arrive_expect_tx(B_QDO, 2 * kTileBytes);
-            tma_load_3d(sbase + kOffQ, &p.tm_q, B_QDO, 0, i0, z);
-            tma_load_3d(sbase + kOffQ + kChunkBytes, &p.tm_q, B_QDO, 0, i0 + kChunk, z);
-            tma_load_3d(sbase + kOffDO, &p.tm_do, B_QDO, 0, i0, z);
-            tma_load_3d(sbase + kOffDO + kChunkBytes, &p.tm_do, B_QDO, 0, i0 + kChunk, z);
+            mbar_arrive_expect_tx(B_QDO, 2 * L::kTileQ);
+            for (int qh = 0; qh < kHalves; ++qh) {
+                const uint32_t o = qh * kTileBytes;
+                tma_load_3d(sbase + kOffQ + o, &p.tm_q, B_QDO, 64 * qh, i0, z);
+                tma_load_3d(sbase + kOffQ + o + kChunkBytes, &p.tm_q, B_QDO, 64 * qh, i0 + kChunk, z);
+                tma_load_3d(sbase + kOffDO + o, &p.tm_do, B_QDO, 64 * qh, i0, z);
+                tma_load_3d(sbase + kOffDO + o + kChunkBytes, &p.tm_do, B_QDO, 64 * qh, i0 + kChunk, z);
+            }
             auto load_chunk = [&](int c) {
                 const int s = c & 1;
                 const int32_t y = (c_lo + c) * kChunk;
-                mbar_arrive_expect_tx(B_KV(s), 2 * kChunkBytes);
-                tma_load_3d(sbase + kOffK + s * kChunkBytes, &p.tm_k, B_KV(s), 0, y, zk);
-                tma_load_3d(sbase + kOffV + s * kChunkBytes, &p.tm_v, B_KV(s), 0, y, zk);
+                mbar_arrive_expect_tx(B_KV(s), 2 * kStage);
+                for (int qh = 0; qh < kHalves; ++qh) {
+                    tma_load_3d(sbase + kOffK + s * kStage + qh * kChunkBytes, &p.tm_k, B_KV(s), 64 * qh, y, zk);
+                    tma_load_3d(sbase + kOffV + s * kStage + qh * kChunkBytes, &p.tm_v, B_KV(s), 64 * qh, y, zk);
+                }
             };
             load_chunk(0);
             if (n_chunks > 1) load_chunk(1);
@@ -224,22 +243,29 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                 mbar_wait(B_KV(s), (c >> 1) & 1, aborted, p.err);
                 if (c > 0) mbar_wait(B_DQ, (c - 1) & 1, aborted, p.err);
                 tc_fence_after();
-                const uint32_t kaddr = sbase + kOffK + s * kChunkBytes;
-                const uint32_t vaddr = sbase + kOffV + s * kChunkBytes;
+                const uint32_t kaddr = sbase + kOffK + s * kStage;
+                const uint32_t vaddr = sbase + kOffV + s * kStage;
+                // K-dim over the row halves: k-steps 4h .. 4h+3 read half h of Q/dO and of K/V
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem + kColS, sdesc_sw128(sbase + kOffQ + 32 * kk, 16, 1024),
-                           sdesc_sw128(kaddr + 32 * kk, 16, 1024), idesc_s, kk > 0);
+                for (int kk = 0; kk < 4 * kHalves; ++kk)
+                    mma_ss(tmem + kColS,
+                           sdesc_sw128(sbase + kOffQ + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024),
+                           sdesc_sw128(kaddr + (kk >> 2) * kChunkBytes + 32 * (kk & 3), 16, 1024),
+                           idesc_s, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem + kColP, sdesc_sw128(sbase + kOffDO + 32 * kk, 16, 1024),
-                           sdesc_sw128(vaddr + 32 * kk, 16, 1024), idesc_s, kk > 0);
+                for (int kk = 0; kk < 4 * kHalves; ++kk)
+                    mma_ss(tmem + kColP,
+                           sdesc_sw128(sbase + kOffDO + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024),
+                           sdesc_sw128(vaddr + (kk >> 2) * kChunkBytes + 32 * (kk & 3), 16, 1024),
+                           idesc_s, kk > 0);
                 mma_commit(B_S);
                 mbar_wait(B_DS, c & 1, aborted, p.err);
                 tc_fence_after();
+                // dQ (own output half) += dS K_half
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tmem, tmem + kColS + 8 * kk, sdesc_sw128(kaddr + 2048 * kk, 0, 1024),
+                    mma_ts(tmem, tmem + kColS + 8 * kk,
+                           sdesc_sw128(kaddr + half * kChunkBytes + 2048 * kk, 0, 1024),
                            idesc_q, (c > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(B_DQ);
                 if (c + 2 < n_chunks) {
@@ -257,26 +283,31 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                 prefetch_tmap(&p.tm_k8);
                 prefetch_tmap(&p.tm_v8);
             }
-            mbar_arrive_expect_tx(B_FULL(0), kTileBytes);
-            tma_load_3d(sbase + kOffRing, &p.tm_o, B_FULL(0), 0, i0, z);
-            tma_load_3d(sbase + kOffRing + kChunkBytes, &p.tm_o, B_FULL(0), 0, i0 + kChunk, z);
-            uint32_t seq = 1;
+            // items: the O tile (head size 128: its two halves), then per offset K_o and V_o
+            // (each by halves at head size 128)
+            uint32_t seq = 0;
+            auto put = [&](const CUtensorMap* map, int32_t x, int32_t y, int32_t zz, bool side8) {
+                const int s = seq & 1;
+                const uint32_t dst = sbase + kOffRing + s * kSlot;
+                mbar_wait(B_EMPTY(s), ((seq >> 1) & 1) ^ 1, aborted, p.err);
+                mbar_arrive_expect_tx(B_FULL(s), side8 ? kSlot : kTileBytes);
+                tma_load_3d(dst, map, B_FULL(s), x, y, zz);
+                tma_load_3d(dst + kChunkBytes, map, B_FULL(s), x, y + kChunk, zz);
+                return dst;
+            };
+            for (int qh = 0; qh < kHalves; ++qh, ++seq) put(&p.tm_o, 64 * qh, i0, z, false);
             for (int k = 0; k < n_act; ++k) {
                 const int32_t y = i0 - offs[k];
-                for (int h = 0; h < 2; ++h, ++seq) {
-                    const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
-                    const int s = seq & 1;
-                    const uint32_t dst = sbase + kOffRing + s * kSlot;
-                    mbar_wait(B_EMPTY(s), ((seq >> 1) & 1) ^ 1, aborted, p.err);
-                    // fractional mode: every item also carries the 8 rows after its tile (the
-                    // derivative in d needs row lo + 1 even where w = 0)
-                    mbar_arrive_expect_tx(B_FULL(s), kSlot);
-                    tma_load_3d(dst, map, B_FULL(s), 0, y, zk);
-                    tma_load_3d(dst + kChunkBytes, map, B_FULL(s), 0, y + kChunk, zk);
-                    if constexpr (kFrac)
-                        tma_load_3d(dst + kTileBytes, h == 0 ? &p.tm_k8 : &p.tm_v8, B_FULL(s), 0,
-                                    y + kRows, zk);
-                }
+                for (int h = 0; h < 2; ++h)
+                    for (int qh = 0; qh < kHalves; ++qh, ++seq) {
+                        const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
+                        // fractional mode: every item also carries the 8 rows after its tile
+                        // (the derivative in d needs row lo + 1 even where w = 0)
+                        const uint32_t dst = put(map, 64 * qh, y, zk, kFrac);
+                        if constexpr (kFrac)
+                            tma_load_3d(dst + kTileBytes, h == 0 ? &p.tm_k8 : &p.tm_v8,
+                                        B_FULL(seq & 1), 0, y + kRows, zk);
+                    }
             }
             for (uint32_t q = seq > 2 ? seq - 2 : 0; q < seq; ++q)
                 mbar_wait(B_FULL(q & 1), (q >> 1) & 1, aborted, p.err);
@@ -292,27 +323,31 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
         const int64_t wrow = zl * p.T_pad + i;  // row index into the workspace arrays
         const float lse2 = row_ok ? p.lse[grow] * kLog2e : 0.f;
 
-        // D_i = dO_i . o_i (dO from its tile, o from the first ring item)
+        // D_i = dO_i . o_i (dO from its tile, o from the first ring item(s))
         mbar_wait(B_QDO, 0, aborted, p.err);
-        uint32_t gw[32];  // dO row (bf16 pairs)
-        load_row_sw(smem + kOffDO, r, gw);
+        uint32_t gw[32 * kHalves];  // dO row (bf16 pairs)
+#pragma unroll
+        for (int qh = 0; qh < kHalves; ++qh) load_row_sw(smem + kOffDO + qh * kTileBytes, r, gw + 32 * qh);
         float D;
         {
-            mbar_wait(B_FULL(0), 0, aborted, p.err);
-            const uint8_t* orow = smem + kOffRing;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 x = *reinterpret_cast<const uint4*>(orow + sw128_off(r, c));
-                fma2_bf16(gw[4 * c + 0], x.x, a0, a1);
-                fma2_bf16(gw[4 * c + 1], x.y, a2, a3);
-                fma2_bf16(gw[4 * c + 2], x.z, a0, a1);
-                fma2_bf16(gw[4 * c + 3], x.w, a2, a3);
+            for (int qh = 0; qh < kHalves; ++qh) {  // items 0 (and 1): slots 0 (and 1), phase 0
+                mbar_wait(B_FULL(qh), 0, aborted, p.err);
+                const uint8_t* orow = smem + kOffRing + qh * kSlot;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(orow + sw128_off(r, c));
+                    fma2_bf16(gw[32 * qh + 4 * c + 0], x.x, a0, a1);
+                    fma2_bf16(gw[32 * qh + 4 * c + 1], x.y, a2, a3);
+                    fma2_bf16(gw[32 * qh + 4 * c + 2], x.z, a0, a1);
+                    fma2_bf16(gw[32 * qh + 4 * c + 3], x.w, a2, a3);
+                }
+                mbar_arrive(B_EMPTY(qh));
             }
             D = (a0 + a1) + (a2 + a3);
-            mbar_arrive(B_EMPTY(0));
         }
-        if (row_ok) {
+        if (row_ok && half == 0) {
             p.delta[wrow] = D;
             p.lse2[wrow] = lse2;
         }
@@ -359,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
         float dq[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) dq[c] = 0.f;
-        uint32_t seq = 1;  // ring item 0 was the O tile
+        uint32_t seq = kHalves;  // the first ring item(s) held the O tile
         const int64_t pds_row = (int64_t)z * p.n_max * p.T_pad + i;
         float ga = 0.f;  // fractional mode: this query's share of dL/dalpha
 #pragma unroll 1
@@ -424,6 +459,55 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                 const uint32_t dsb = pair >> 16;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) axpy2_bf16(dsb, kt[c], dq[2 * c], dq[2 * c + 1]);
+                continue;
+            }
+            if constexpr (kWide) {
+                // both halves of K_o for the score, the own half kept for dq; both halves of V_o
+                uint32_t kw[32];
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                for (int qh = 0; qh < 2; ++qh, ++seq) {
+                    const int s = seq & 1;
+                    mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
+                    const uint8_t* krow = smem + kOffRing + s * kSlot;
+                    const uint8_t* qrow = smem + kOffQ + qh * kTileBytes;
+                    if (qh == half) load_row_sw(krow, r, kw);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
+                        const uint4 y = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
+                        fma2_bf16(x.x, y.x, a0, a1);
+                        fma2_bf16(x.y, y.y, a2, a3);
+                        fma2_bf16(x.z, y.z, a0, a1);
+                        fma2_bf16(x.w, y.w, a2, a3);
+                    }
+                    mbar_arrive(B_EMPTY(s));
+                }
+                const float sdot = (a0 + a1) + (a2 + a3);
+                float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll
+                for (int qh = 0; qh < 2; ++qh, ++seq) {
+                    const int s = seq & 1;
+                    mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
+                    const uint8_t* vrow = smem + kOffRing + s * kSlot;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(vrow + sw128_off(r, c));
+                        fma2_bf16(gw[32 * qh + 4 * c + 0], x.x, b0, b1);
+                        fma2_bf16(gw[32 * qh + 4 * c + 1], x.y, b2, b3);
+                        fma2_bf16(gw[32 * qh + 4 * c + 2], x.z, b0, b1);
+                        fma2_bf16(gw[32 * qh + 4 * c + 3], x.w, b2, b3);
+                    }
+                    mbar_arrive(B_EMPTY(s));
+                }
+                const float dpd = (b0 + b1) + (b2 + b3);
+                const float pr = valid ? ex2(sdot * sl2 - lse2) : 0.f;
+                const float ds = pr * (dpd - D);
+                const uint32_t pair = pack_bf16x2(pr, ds);  // lo = P, hi = dS
+                if (valid && half == 0) p.pds[pds_row + (int64_t)k * p.T_pad - offs[k]] = pair;
+                const uint32_t dsb = pair >> 16;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) axpy2_bf16(dsb, kw[c], dq[2 * c], dq[2 * c + 1]);
                 continue;
             }
             int s = seq & 1;
@@ -513,8 +597,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
             }
         }
         if (tid == 0 && !aborted) {
-            tma_store_3d(&p.tm_dq, sbase + kOffQ, 0, i0, z);
-            if (i0 + kChunk < T) tma_store_3d(&p.tm_dq, sbase + kOffQ + kChunkBytes, 0, i0 + kChunk, z);
+            const int32_t xo = 64 * half;  // the CTA's output columns
+            tma_store_3d(&p.tm_dq, sbase + kOffQ, xo, i0, z);
+            if (i0 + kChunk < T) tma_store_3d(&p.tm_dq, sbase + kOffQ + kChunkBytes, xo, i0 + kChunk, z);
             tma_store_commit();
             tma_store_wait_read0();
         }
@@ -562,12 +647,18 @@ struct Layout {
 
 // Band queries [j0, min(T-1, j0+127+W-1)] in 64-query chunks, grouped by kMaxGroupChunks
 // (each group re-reads the K and V tiles, so no ring item waits on a later one); active
-// offsets o <= T-1-j0.
+// offsets o <= T-1-j0. Head size 128 (kWide): K and V take two items each (their column
+// halves) and a chunk two (Q, dO: both halves each), so a group holds one chunk (6 items).
+template <bool kWide>
 struct Plan {
+    static constexpr int kKV = kWide ? 2 : 1;        // items per K (and per V) tile
+    static constexpr int kCI = kWide ? 2 : 1;        // items per band chunk
+    static constexpr int kMaxGC = kWide ? 1 : kMaxGroupChunks;
     int32_t j0, q_lo, n_chunks, n_groups, n_act;
     __device__ __forceinline__ int nch(int g) const {
-        return min(kMaxGroupChunks, n_chunks - g * kMaxGroupChunks);
+        return min(kMaxGC, n_chunks - g * kMaxGC);
     }
+    __device__ __forceinline__ uint32_t group_items(int g) const { return 2 * kKV + kCI * nch(g); }
 };
 
 // Launch query slice of query head hq (of the `group` heads that read the tile's kv head).
@@ -575,14 +666,15 @@ __device__ __forceinline__ int64_t query_slice(const BwdParams& p, const ring::T
     return (int64_t)tl.layer * p.slices_per_layer + (int64_t)tl.s * p.group + hq;
 }
 
-__device__ __forceinline__ Plan make_plan(const BwdParams& p, int layer, int32_t j0) {
-    Plan pl;
+template <bool kWide>
+__device__ __forceinline__ Plan<kWide> make_plan(const BwdParams& p, int layer, int32_t j0) {
+    Plan<kWide> pl;
     pl.j0 = j0;
     const int64_t qlast64 = (int64_t)j0 + kRows - 1 + p.W - 1;
     const int32_t qlast = qlast64 < p.T - 1 ? (int32_t)qlast64 : p.T - 1;
     pl.q_lo = j0 / kChunk;
     pl.n_chunks = qlast / kChunk - pl.q_lo + 1;
-    pl.n_groups = (pl.n_chunks + kMaxGroupChunks - 1) / kMaxGroupChunks;
+    pl.n_groups = (pl.n_chunks + Plan<kWide>::kMaxGC - 1) / Plan<kWide>::kMaxGC;
     const int32_t* offs = p.tabs.off[layer];
     int32_t n = 0;
     for (int e = 0; e < p.tabs.count[layer]; ++e)
@@ -591,8 +683,21 @@ __device__ __forceinline__ Plan make_plan(const BwdParams& p, int layer, int32_t
     return pl;
 }
 
-template <bool kFrac>
+// Tile walk: at head size 128 each kv tile is taken twice, by output half (the fastest index).
+template <bool kWide>
+__device__ __forceinline__ ring::Tile tile_at(const BwdParams& p, uint32_t idx, int& half) {
+    half = kWide ? (int)(idx & 1u) : 0;
+    return ring::tile_of(kWide ? idx >> 1 : idx, p.tiles_per_slice, p.slices_per_layer_kv32);
+}
+
+// Head size 128 (kWide): two CTAs per kv tile, one per half of the dK/dV columns; both form
+// the full S^T = K Q^T and dP^T = V dO^T (8 k-steps over the column halves), each takes
+// dV_half += P^T dO_half and dK_half += dS^T Q_half and, in the offsets, the own half of
+// the Q_o / dO_o rows.
+template <bool kFrac, bool kWide>
 __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs<kFrac> p) {
+    static_assert(!(kFrac && kWide), "the fractional mode is for head size 64");
+    using PL = Plan<kWide>;
     using L = Layout<kFrac>;
     constexpr uint32_t kOffBar = L::kOffBar, kOffTmemSlot = L::kOffTmemSlot, kPre = L::kPre;
     extern __shared__ uint8_t smem_raw[];
@@ -644,8 +749,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             uint32_t seq = 0;
             const int32_t Tp = p.T_pad;
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
-                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer_kv32);
-                const Plan pl = make_plan(p, tl.layer, tl.row0);
+                int half;
+                const ring::Tile tl = tile_at<kWide>(p, idx, half);
+                const PL pl = make_plan<kWide>(p, tl.layer, tl.row0);
                 const int32_t z = (int32_t)tl.zl;  // the kv slice of the tile
                 for (int hq = 0; hq < (int)p.group; ++hq)
                 for (int g = 0; g < pl.n_groups; ++g) {
@@ -654,24 +760,42 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                     const int32_t zq = (int32_t)zq64;
                     const float* l2_row = p.lse2 + zq64 * Tp;
                     const float* d_row = p.delta + zq64 * Tp;
-                    // K and V tiles
-                    for (int h = 0; h < 2; ++h, ++seq) {
-                        if (!rg.acquire(seq, aborted, p.err)) continue;
-                        const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
-                        mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes);
-                        tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, pl.j0, z);
-                        tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 0, pl.j0 + kChunk, z);
-                    }
+                    // K and V tiles (head size 128: each by column halves)
+                    for (int h = 0; h < 2; ++h)
+                        for (int xh = 0; xh < PL::kKV; ++xh, ++seq) {
+                            if (!rg.acquire(seq, aborted, p.err)) continue;
+                            const CUtensorMap* map = h == 0 ? &p.tm_k : &p.tm_v;
+                            mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes);
+                            tma_load_3d(rg.addr(seq), map, rg.full(seq), 64 * xh, pl.j0, z);
+                            tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 64 * xh,
+                                        pl.j0 + kChunk, z);
+                        }
                     // band chunks: Q and dO rows qb.., with lse*log2(e) and D of those rows
-                    for (int c = 0; c < pl.nch(g); ++c, ++seq) {
-                        if (!rg.acquire(seq, aborted, p.err)) continue;
-                        const int32_t qb = (pl.q_lo + g * kMaxGroupChunks + c) * kChunk;
+                    // (head size 128: the Q chunk's two halves, then the dO chunk's)
+                    for (int c = 0; c < pl.nch(g); ++c) {
+                        const int32_t qb = (pl.q_lo + g * PL::kMaxGC + c) * kChunk;
                         const uint32_t side_bytes = 4u * (uint32_t)min(kChunk, Tp - qb);
+                        if constexpr (kWide) {
+                            for (int h = 0; h < 2; ++h, ++seq) {
+                                if (!rg.acquire(seq, aborted, p.err)) continue;
+                                const CUtensorMap* map = h == 0 ? &p.tm_q : &p.tm_do;
+                                mbar_arrive_expect_tx(rg.full(seq), 2 * kChunkBytes + (h == 0 ? 2 * side_bytes : 0u));
+                                tma_load_3d(rg.addr(seq), map, rg.full(seq), 0, qb, zq);
+                                tma_load_3d(rg.addr(seq) + kChunkBytes, map, rg.full(seq), 64, qb, zq);
+                                if (h == 0) {
+                                    bulk_load(side_addr(seq), l2_row + qb, side_bytes, rg.full(seq));
+                                    bulk_load(side_addr(seq) + 256, d_row + qb, side_bytes, rg.full(seq));
+                                }
+                            }
+                            continue;
+                        }
+                        if (!rg.acquire(seq, aborted, p.err)) { ++seq; continue; }
                         mbar_arrive_expect_tx(rg.full(seq), 2 * kChunkBytes + 2 * side_bytes);
                         tma_load_3d(rg.addr(seq), &p.tm_q, rg.full(seq), 0, qb, zq);
                         tma_load_3d(rg.addr(seq) + kChunkBytes, &p.tm_do, rg.full(seq), 0, qb, zq);
                         bulk_load(side_addr(seq), l2_row + qb, side_bytes, rg.full(seq));
                         bulk_load(side_addr(seq) + 256, d_row + qb, side_bytes, rg.full(seq));
+                        ++seq;
                     }
                 }
                 // Q_o of every offset, then dO_o of every offset; both carry the (P, dS) pairs of
@@ -693,8 +817,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                         bool pre = false;
                         if constexpr (kFrac) pre = p.w[tl.layer][k] != 0.f;
                         mbar_arrive_expect_tx(rg.full(seq), ring::kSlotBytes + (pre ? 1024u : 0u) + pair_bytes);
-                        tma_load_3d(rg.addr(seq) + kPre, map, rg.full(seq), 0, y, zq);
-                        tma_load_3d(rg.addr(seq) + kPre + kChunkBytes, map, rg.full(seq), 0, y + kChunk, zq);
+                        const int32_t xo = 64 * half;  // the own half (head size 128)
+                        tma_load_3d(rg.addr(seq) + kPre, map, rg.full(seq), xo, y, zq);
+                        tma_load_3d(rg.addr(seq) + kPre + kChunkBytes, map, rg.full(seq), xo, y + kChunk, zq);
                         if constexpr (kFrac) {
                             if (pre)
                                 tma_load_3d(rg.addr(seq), h == 0 ? &p.tm_q8 : &p.tm_do8, rg.full(seq), 0,
@@ -724,51 +849,65 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             // descriptors of shared address sbase; an operand at sbase + x adds x >> 4
             const uint64_t dkm = sdesc_sw128(sbase, 16, 1024), dmn = sdesc_sw128(sbase, 0, 1024);
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x, ++tcount) {
-                const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer_kv32);
-                const Plan pl = make_plan(p, tl.layer, tl.row0);
+                int half;
+                const ring::Tile tl = tile_at<kWide>(p, idx, half);
+                const PL pl = make_plan<kWide>(p, tl.layer, tl.row0);
                 if (tcount > 0) mbar_wait(B_T, (tcount - 1) & 1, aborted, p.err);
                 int cg = 0;  // chunk index within the tile (over every query head)
                 for (int hq = 0; hq < (int)p.group; ++hq)
                 for (int g = 0; g < pl.n_groups; ++g) {
                     const int nch = pl.nch(g);
-                    const uint32_t kseq = seq, vseq = seq + 1, bseq = seq + 2;
-                    seq += 2 + nch;
-                    rg.wait_full(kseq, aborted, p.err);
-                    rg.wait_full(vseq, aborted, p.err);
-                    const uint32_t kaddr = rg.addr(kseq), vaddr = rg.addr(vseq);
+                    const uint32_t kseq = seq, vseq = seq + PL::kKV, bseq = seq + 2 * PL::kKV;
+                    seq += pl.group_items(g);
+                    for (int j = 0; j < PL::kKV; ++j) {
+                        rg.wait_full(kseq + j, aborted, p.err);
+                        rg.wait_full(vseq + j, aborted, p.err);
+                    }
                     for (int c = 0; c < nch; ++c, ++cg, ++mcount) {
-                        const uint32_t qaddr = rg.addr(bseq + c), gaddr = qaddr + kChunkBytes;
-                        rg.wait_full(bseq + c, aborted, p.err);
+                        // the chunk's Q (and dO) operands; head size 128: two items, each the
+                        // chunk's two column halves
+                        const uint32_t qaddr = rg.addr(bseq + PL::kCI * c);
+                        const uint32_t gaddr = kWide ? rg.addr(bseq + PL::kCI * c + 1) : qaddr + kChunkBytes;
+                        for (int j = 0; j < PL::kCI; ++j) rg.wait_full(bseq + PL::kCI * c + j, aborted, p.err);
                         // S^T/dP^T columns hold the previous chunk's P^T/dS^T until its MMAs finish
                         if (cg > 0) mbar_wait(B_M, (mcount - 1) & 1, aborted, p.err);
                         tc_fence_after();
-                        const uint64_t dk_a = dkm + ((kaddr - sbase) >> 4), dv_a = dkm + ((vaddr - sbase) >> 4);
-                        const uint64_t dq_b = dkm + ((qaddr - sbase) >> 4), dg_b = dkm + ((gaddr - sbase) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + kColS, dk_a + 2 * kk, dq_b + 2 * kk, idesc_s, kk > 0);
+                        for (int kk = 0; kk < 4 * PL::kKV; ++kk) {
+                            // k-steps 4h .. 4h+3: column half h of K (its item) and of the Q chunk
+                            const uint64_t a = dkm + ((rg.addr(kseq + (kk >> 2)) - sbase) >> 4) + 2 * (kk & 3);
+                            const uint64_t b = dkm + ((qaddr + (kk >> 2) * kChunkBytes - sbase) >> 4) + 2 * (kk & 3);
+                            mma_ss(tmem + kColS, a, b, idesc_s, kk > 0);
+                        }
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + kColP, dv_a + 2 * kk, dg_b + 2 * kk, idesc_s, kk > 0);
+                        for (int kk = 0; kk < 4 * PL::kKV; ++kk) {
+                            const uint64_t a = dkm + ((rg.addr(vseq + (kk >> 2)) - sbase) >> 4) + 2 * (kk & 3);
+                            const uint64_t b = dkm + ((gaddr + (kk >> 2) * kChunkBytes - sbase) >> 4) + 2 * (kk & 3);
+                            mma_ss(tmem + kColP, a, b, idesc_s, kk > 0);
+                        }
                         mma_commit(B_S);
                         if (c == nch - 1) {
-                            rg.release_mma(kseq);
-                            rg.release_mma(vseq);
+                            for (int j = 0; j < PL::kKV; ++j) {
+                                rg.release_mma(kseq + j);
+                                rg.release_mma(vseq + j);
+                            }
                         }
                         mbar_wait(B_P, mcount & 1, aborted, p.err);
                         tc_fence_after();
                         // P^T / dS^T of queries 32h..32h+31 sit in columns [32h, 32h+16) of their block
+                        // dV (own half) += P^T dO_half, dK (own half) += dS^T Q_half
+                        const uint32_t ho = kWide ? half * kChunkBytes : 0u;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t acol = 32 * (kk >> 1) + 8 * (kk & 1);
                             const uint32_t acc = (cg > 0 || kk > 0) ? 1u : 0u;
                             mma_ts(tmem + kColDV, tmem + kColS + acol,
-                                   dmn + ((gaddr - sbase) >> 4) + 128 * kk, idesc_o, acc);
+                                   dmn + ((gaddr + ho - sbase) >> 4) + 128 * kk, idesc_o, acc);
                             mma_ts(tmem + kColDK, tmem + kColP + acol,
-                                   dmn + ((qaddr - sbase) >> 4) + 128 * kk, idesc_o, acc);
+                                   dmn + ((qaddr + ho - sbase) >> 4) + 128 * kk, idesc_o, acc);
                         }
                         mma_commit(B_M);
-                        rg.release_mma(bseq + c);
+                        for (int j = 0; j < PL::kCI; ++j) rg.release_mma(bseq + PL::kCI * c + j);
                     }
                 }
                 seq += 2 * p.group * pl.n_act + 2;
@@ -783,8 +922,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
         const float sl2 = p.scale_log2;
         uint32_t seq = 0, mcount = 0;
         for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x) {
-            const ring::Tile tl = ring::tile_of(idx, p.tiles_per_slice, p.slices_per_layer_kv32);
-            const Plan pl = make_plan(p, tl.layer, tl.row0);
+            int half;
+            const ring::Tile tl = tile_at<kWide>(p, idx, half);
+            const PL pl = make_plan<kWide>(p, tl.layer, tl.row0);
             const int32_t j0 = pl.j0;
             const int32_t j = j0 + r;
             const bool row_ok = j < T;
@@ -795,16 +935,17 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             for (int hq = 0; hq < (int)p.group; ++hq)
             for (int g = 0; g < pl.n_groups; ++g) {
                 const int nch = pl.nch(g);
-                const uint32_t bseq = seq + 2;
-                seq += 2 + nch;
+                const uint32_t bseq = seq + 2 * PL::kKV;
+                seq += pl.group_items(g);
                 for (int c = 0; c < nch; ++c, ++mcount) {
-                    const int32_t qb = (pl.q_lo + g * kMaxGroupChunks + c) * kChunk + 32 * h;
+                    const int32_t qb = (pl.q_lo + g * PL::kMaxGC + c) * kChunk + 32 * h;
+                    const uint32_t cseq = bseq + PL::kCI * c;  // the chunk's (first) item
                     mbar_wait(B_S, mcount & 1, aborted, p.err);
-                    rg.wait_full(bseq + c, aborted, p.err);  // lse*log2(e) / D side data
+                    rg.wait_full(cseq, aborted, p.err);  // lse*log2(e) / D side data
                     tc_fence_after();
                     const int32_t klo = j0 + 32 * q4;
                     const bool need = (qb + 31 - klo >= 0) && (qb - (klo + 31) < W) && qb < T;
-                    const float* L = side_ptr(bseq + c) + 32 * h;
+                    const float* L = side_ptr(cseq) + 32 * h;
                     const float* Dd = L + kChunk;
                     const int32_t dist0 = qb - j;
 #pragma unroll
@@ -964,11 +1105,12 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             if (tid == 0) {
                 if (!aborted) {
                     const int32_t z = (int32_t)tl.zl;
-                    tma_store_3d(&p.tm_dk, rg.addr(kst), 0, j0, z);
-                    tma_store_3d(&p.tm_dv, rg.addr(vst), 0, j0, z);
+                    const int32_t xo = 64 * half;  // the CTA's output columns
+                    tma_store_3d(&p.tm_dk, rg.addr(kst), xo, j0, z);
+                    tma_store_3d(&p.tm_dv, rg.addr(vst), xo, j0, z);
                     if (j0 + kChunk < T) {
-                        tma_store_3d(&p.tm_dk, rg.addr(kst) + kChunkBytes, 0, j0 + kChunk, z);
-                        tma_store_3d(&p.tm_dv, rg.addr(vst) + kChunkBytes, 0, j0 + kChunk, z);
+                        tma_store_3d(&p.tm_dk, rg.addr(kst) + kChunkBytes, xo, j0 + kChunk, z);
+                        tma_store_3d(&p.tm_dv, rg.addr(vst) + kChunkBytes, xo, j0 + kChunk, z);
                     }
                     tma_store_commit();
                     tma_store_wait_read0();
@@ -1006,7 +1148,7 @@ fibattn_status set_smem(const void* fn, uint32_t bytes, bool (&done)[64]) {
 
 namespace {
 
-template <bool kFrac>
+template <bool kFrac, bool kWide>
 fibattn_status launch_bwd(const void* q, const void* k, const void* v, const void* o,
                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
                           float* delta, float* lse2, uint32_t* pds, int32_t n_max,
@@ -1016,8 +1158,9 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
     if (slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     const int64_t slices_kv = slices / sh.group;
     const int32_t tiles = (sh.T + kRows - 1) / kRows;
-    const int64_t gx = (int64_t)tiles * sh.slices_per_layer;
-    if (gx > 0x7fffffff || (int64_t)tiles * slices > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
+    const int64_t halves = kWide ? 2 : 1;  // CTAs per tile (head size 128: one per column half)
+    const int64_t gx = (int64_t)tiles * sh.slices_per_layer * halves;
+    if (gx > 0x7fffffff || (int64_t)tiles * slices * halves > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
     BwdArgs<kFrac> P;
     // the error-word lookup is a runtime call: it binds the device's primary context to this
     // thread (a fresh thread, e.g. autograd's, may have none), which the encoding needs
@@ -1028,7 +1171,9 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
     for (int m = 0; m < 8; ++m) {
         // k, v, dk, dv (maps 1, 2, 5, 6) over the kv slices
         const bool kvmap = m == 1 || m == 2 || m == 5 || m == 6;
-        const int r = make_bf16_rows_map(maps[m], bases[m], kvmap ? slices_kv : slices, sh.T);
+        const int64_t sl = kvmap ? slices_kv : slices;
+        const int r = kWide ? make_bf16_rows_map_d(maps[m], bases[m], sl, sh.T, 128)
+                            : make_bf16_rows_map(maps[m], bases[m], sl, sh.T);
         if (r != 0) return cuda_fail(r, "cuTensorMapEncodeTiled (bwd)");
     }
     if constexpr (kFrac) {
@@ -1052,7 +1197,7 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
     P.slices_per_layer = sh.slices_per_layer;
     P.group = (uint32_t)sh.group;
     P.slices_per_layer_kv32 = (uint32_t)(sh.slices_per_layer / sh.group);
-    P.total_tiles = (uint32_t)((int64_t)tiles * slices_kv);  // the key owner walks kv tiles
+    P.total_tiles = (uint32_t)((int64_t)tiles * slices_kv * halves);  // the key owner walks kv tiles
     P.T = sh.T;
     P.W = sh.W;
     P.T_pad = (sh.T + 3) & ~3;
@@ -1063,11 +1208,11 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
     P.tabs = t;
     static bool dq_set[64] = {}, dkdv_set[64] = {};
     static int n_sm[64] = {};
-    fibattn_status s0 = set_smem((const void*)dq::bwd_dq_tc_kernel<kFrac>,
-                                 dq::Layout<kFrac>::kSmemAlloc, dq_set);
+    fibattn_status s0 = set_smem((const void*)dq::bwd_dq_tc_kernel<kFrac, kWide>,
+                                 dq::Layout<kFrac, kWide>::kSmemAlloc, dq_set);
     if (s0 != FIBATTN_OK) return s0;
-    s0 = set_smem((const void*)dkdv::bwd_dkdv_tc_kernel<kFrac>, dkdv::Layout<kFrac>::kSmemAlloc,
-                  dkdv_set);
+    s0 = set_smem((const void*)dkdv::bwd_dkdv_tc_kernel<kFrac, kWide>,
+                  dkdv::Layout<kFrac>::kSmemAlloc, dkdv_set);
     if (s0 != FIBATTN_OK) return s0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1079,17 +1224,18 @@ fibattn_status launch_bwd(const void* q, const void* k, const void* v, const voi
     }
     const int64_t pgrid = (int64_t)P.total_tiles < 2LL * n_sm[dev] ? (int64_t)P.total_tiles : 2LL * n_sm[dev];
     dim3 grid((unsigned)gx, sh.n_layers);
-    const char* n_dq = kFrac ? "bwd_dq_frac_tc" : "bwd_dq_tc";
-    const char* n_kv = kFrac ? "bwd_dkdv_frac_tc" : "bwd_dkdv_tc";
+    const char* n_dq = kFrac ? "bwd_dq_frac_tc" : (kWide ? "bwd_dq_tc128" : "bwd_dq_tc");
+    const char* n_kv = kFrac ? "bwd_dkdv_frac_tc" : (kWide ? "bwd_dkdv_tc128" : "bwd_dkdv_tc");
     {
         KernelScope ks(n_dq, st);
-        dq::bwd_dq_tc_kernel<kFrac><<<grid, dq::kThreads, dq::Layout<kFrac>::kSmemAlloc, st>>>(P);
+        dq::bwd_dq_tc_kernel<kFrac, kWide>
+            <<<grid, dq::kThreads, dq::Layout<kFrac, kWide>::kSmemAlloc, st>>>(P);
     }
     s0 = launch_status(n_dq);
     if (s0 != FIBATTN_OK) return s0;
     {
         KernelScope ks(n_kv, st);
-        dkdv::bwd_dkdv_tc_kernel<kFrac>
+        dkdv::bwd_dkdv_tc_kernel<kFrac, kWide>
             <<<(unsigned)pgrid, dkdv::kThreads, dkdv::Layout<kFrac>::kSmemAlloc, st>>>(P);
     }
     return launch_status(n_kv);
@@ -1101,8 +1247,11 @@ fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, c
                                   const float* lse, const void* dO, void* dq, void* dk, void* dv,
                                   float* delta, float* lse2, uint32_t* pds, int32_t n_max,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
-    return launch_bwd<false>(q, k, v, o, lse, dO, dq, dk, dv, delta, lse2, pds, n_max, sh, t,
-                             nullptr, nullptr, st);
+    if (sh.d == 128)
+        return launch_bwd<false, true>(q, k, v, o, lse, dO, dq, dk, dv, delta, lse2, pds, n_max, sh,
+                                       t, nullptr, nullptr, st);
+    return launch_bwd<false, false>(q, k, v, o, lse, dO, dq, dk, dv, delta, lse2, pds, n_max, sh, t,
+                                    nullptr, nullptr, st);
 }
 
 fibattn_status launch_bwd_frac_tc_bf16(const void* q, const void* k, const void* v, const void* o,
@@ -1110,8 +1259,8 @@ fibattn_status launch_bwd_frac_tc_bf16(const void* q, const void* k, const void*
                                        void* dv, float* delta, float* lse2, uint32_t* pds,
                                        int32_t n_max, float* galpha, const AttnShape& sh,
                                        const FracTables& t, cudaStream_t st) {
-    return launch_bwd<true>(q, k, v, o, lse, dO, dq, dk, dv, delta, lse2, pds, n_max, sh, t.c,
-                            &t, galpha, st);
+    return launch_bwd<true, false>(q, k, v, o, lse, dO, dq, dk, dv, delta, lse2, pds, n_max, sh,
+                                   t.c, &t, galpha, st);
 }
 
 }  // namespace fibattn

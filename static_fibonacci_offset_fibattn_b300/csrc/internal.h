@@ -95,7 +95,7 @@ struct AttnShape {
     int32_t group = 1;         // query heads per kv head: K/V (and dK/dV) have
                                // slices_per_layer / group slices per layer, query head h of
                                // batch b reading kv head h / group of batch b
-    int32_t d = 64;            // head size: 64, or 128 (SIMT kernels and the d = 128 forward)
+    int32_t d = 64;            // head size: 64 or 128
 };
 
 fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o,
@@ -117,11 +117,7 @@ fibattn_status launch_fwd_frac_simt_f32(const float* q, const float* k, const fl
 fibattn_status launch_fwd_frac_tc_bf16(const void* q, const void* k, const void* v, void* o,
                                        float* lse, const AttnShape& sh, const FracTables& t,
                                        cudaStream_t st);
-// SIMT backward: D into `delta`, then dQ, then dK/dV (fp32; bf16 at d = 128).
-fibattn_status launch_bwd_simt_bf16(const void* q, const void* k, const void* v, const void* o,
-                                    const float* lse, const void* dO, void* dq, void* dk,
-                                    void* dv, float* delta, const AttnShape& sh,
-                                    const OffsetTables& t, cudaStream_t st);
+// SIMT backward (fp32 path, d = 64 or 128): D into `delta`, then dQ, then dK/dV.
 fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* v, const float* o,
                                    const float* lse, const float* dO, float* dq, float* dk,
                                    float* dv, float* delta, const AttnShape& sh,

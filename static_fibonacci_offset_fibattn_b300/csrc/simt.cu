@@ -594,16 +594,4 @@ fibattn_status launch_bwd_simt_f32(const float* q, const float* k, const float* 
     return bwd_typed<float, 64>(q, k, v, o, lse, dO, dq, dk, dv, delta, sh, t, st);
 }
 
-fibattn_status launch_bwd_simt_bf16(const void* q, const void* k, const void* v, const void* o,
-                                    const float* lse, const void* dO, void* dq, void* dk,
-                                    void* dv, float* delta, const AttnShape& sh,
-                                    const OffsetTables& t, cudaStream_t st) {
-    typedef __nv_bfloat16 E;
-    if (sh.d == 128)
-        return bwd_typed<E, 128>((const E*)q, (const E*)k, (const E*)v, (const E*)o, lse,
-                                 (const E*)dO, (E*)dq, (E*)dk, (E*)dv, delta, sh, t, st);
-    return bwd_typed<E, 64>((const E*)q, (const E*)k, (const E*)v, (const E*)o, lse,
-                            (const E*)dO, (E*)dq, (E*)dk, (E*)dv, delta, sh, t, st);
-}
-
 }  // namespace fibattn
