@@ -23,8 +23,9 @@
  *   - Nothing is printed. Errors are returned as fibattn_status; kernel-side
  *     failures (a bounded wait that ran out) are latched in the device error word
  *     and reported by fibattn_poll_device_error().
- *   - d (head size) must be 64; dtype FIBATTN_F32 or FIBATTN_BF16, the same for
- *     every q/k/v/o/dO/dq/dk/dv tensor of a call.
+ *   - d (head size) is 64, or 128 for the static and grouped-query forward and backward
+ *     (the fractional-offset and RoPE calls take 64); dtype FIBATTN_F32 or FIBATTN_BF16, the
+ *     same for every q/k/v/o/dO/dq/dk/dv tensor of a call.
  */
 #ifndef FIBATTN_H
 #define FIBATTN_H
@@ -119,7 +120,8 @@ FIBATTN_API fibattn_status fibattn_offsets_device(const fibattn_schedule* sched,
  *   lse     : [Lc][B][H][T] float32 device, written: log sum_j exp(scale * q_i.k_j).
  *   scale   : <= 0 selects 1/sqrt(d).
  *   W >= 1 (W >= T gives dense causal attention). bf16 runs on the tcgen05 tensor-core
- *   kernel; f32 on the SIMT fp32 kernel.
+ *   kernel (d = 128: two CTAs per 128-query tile, one per half of the output columns); f32 on
+ *   the SIMT fp32 kernel.
  * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (a layer table above FIBATTN_MAX_OFFSETS),
  * CUDA (launch failure).
  */
