@@ -46,7 +46,7 @@ extern "C" {
 typedef enum {
     FIBATTN_OK = 0,
     FIBATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad schedule */
-    FIBATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (d != 64, unknown dtype) */
+    FIBATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (a head size or dtype) */
     FIBATTN_ERR_CAPACITY = 3,    /* an offset table does not fit the given capacity */
     FIBATTN_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
     FIBATTN_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (device error word) */
