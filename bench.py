@@ -115,6 +115,20 @@ def parse():
     return a
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: the job's time when every rank runs its own batch."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's units over the max-over-ranks step time."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -325,13 +339,9 @@ def run_ours(a, spec, world, rank, local):
         torch.distributed.barrier()
     fa.poll_device_error(dev)
     step_ms = [s.elapsed_time(e) for s, e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / a.steps
-    value = world * tokens(spec) / (ms_per_step / 1e3)
+    value = job_rate(tokens(spec), world, ms_per_step)
 
     # ---- roofline of the dominant kernel
     hbm, peak_kind = peaks()
@@ -473,12 +483,8 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None, table=None
         step()
     e.record(stream)
     torch.cuda.synchronize(dev)
-    ms = s.elapsed_time(e)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(world * tokens(spec) / (ms / steps / 1e3), 1), "unit": UNIT,
+    ms = max_over_ranks(s.elapsed_time(e), world, dev)
+    return {"value": round(job_rate(tokens(spec), world, ms / steps), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(ms / steps, 3)}
 
