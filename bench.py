@@ -7,7 +7,7 @@ backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
 stagger alpha 0.5 -> 2.0, bf16, forward + backward.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload c5|c4|c2|c3|c3p|c3f|c5f|c5g|c5r|c3w|c5w]
+                  [--workload c5|c4|c2|c1|c3|c3p|c3f|c5f|c5g|c5r|c3w|c5w]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
@@ -104,8 +104,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c5",
-                    choices=["c5", "c4", "c2", "c3", "c3p", "c3f", "c5f", "c5g", "c5r", "c3w",
-                             "c5w"])
+                    choices=["c5", "c4", "c2", "c1", "c3", "c3p", "c3f", "c5f", "c5g", "c5r",
+                             "c3w", "c5w"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
