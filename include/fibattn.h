@@ -353,6 +353,15 @@ FIBATTN_API fibattn_status fibattn_bwd_rope(const void* q_rot, const void* k_rot
  */
 FIBATTN_API fibattn_status fibattn_poll_device_error(void* cuda_stream);
 
+/*
+ * A check of the failure path, for tests: launches one small kernel whose thread waits, with
+ * the bounded wait every attention kernel uses (limit_ms, 1..10000), on an mbarrier that
+ * nothing arrives on. The wait runs out, the kernel latches the device error word and
+ * returns; fibattn_poll_device_error then reports TIMEOUT once (and clears it), and the
+ * context stays usable. No fault, trap or hang is involved. Errors: INVALID_ARG, CUDA.
+ */
+FIBATTN_API fibattn_status fibattn_debug_wait_timeout(int32_t limit_ms, void* cuda_stream);
+
 /* Static English text for a status value (never NULL). */
 FIBATTN_API const char* fibattn_status_string(fibattn_status status);
 

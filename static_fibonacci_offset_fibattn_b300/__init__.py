@@ -25,7 +25,7 @@ __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd"
            "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
            "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac", "bwd_frac",
            "bwd_frac_workspace_size", "FibFracAttention", "rope_table", "rope", "fwd_rope",
-           "bwd_rope"]
+           "bwd_rope", "debug_wait_timeout"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
@@ -119,6 +119,8 @@ def lib():
                                                  ctypes.POINTER(u64)]
         L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32, i32,
                                   i32, i32, f32, sp, i32, i32, vp]
+        L.fibattn_debug_wait_timeout.argtypes = [i32, vp]
+        L.fibattn_debug_wait_timeout.restype = i32
         L.fibattn_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
         L.fibattn_rope.argtypes = [vp, vp, ctypes.c_int64, i32, i32, i32, vp, i32, i32, vp]
         L.fibattn_fwd_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
@@ -542,3 +544,11 @@ def bwd_rope(q_rot, k_rot, v, o, lse, dO, W: int, sched: Schedule, table: torch.
                                 layer0, Lc, _ptr(table), table.shape[0], _stream(q_rot))
     _check(st, "fibattn_bwd_rope")
     return dq, dk, dv
+
+
+def debug_wait_timeout(limit_ms: int = 50, device="cuda"):
+    """Launch the failure-path check (fibattn_debug_wait_timeout): a bounded wait that runs
+    out; poll_device_error() afterwards raises FibAttnError with status TIMEOUT."""
+    st = lib().fibattn_debug_wait_timeout(
+        int(limit_ms), ctypes.c_void_p(torch.cuda.current_stream(torch.device(device)).cuda_stream))
+    _check(st, "fibattn_debug_wait_timeout")

@@ -259,3 +259,9 @@ def test_rope_entry_points_validate_before_launch():
                               None) == fa.INVALID_ARG
     assert L.fibattn_bwd_rope(*([ok] * 10), ctypes.c_uint64(1 << 40), 1, 4, 2, 8, 64, 1, 4, 0.0,
                               ctypes.byref(sc), 0, 1, None, 8, None) == fa.INVALID_ARG
+
+
+def test_debug_wait_timeout_validates_before_launch():
+    L = fa.lib()
+    for bad in (0, -5, 10001):
+        assert L.fibattn_debug_wait_timeout(bad, None) == fa.INVALID_ARG
