@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                     fma2_bf16(gw[32 * qh + 4 * c + 2], x.z, a0, a1);
                     fma2_bf16(gw[32 * qh + 4 * c + 3], x.w, a2, a3);
                 }
+                fence_proxy_async_smem();  // generic reads before the TMA refill
                 mbar_arrive(B_EMPTY(qh));
             }
             D = (a0 + a1) + (a2 + a3);
@@ -358,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
             const int32_t d0 = i - kb;
             mbar_wait(B_S, c & 1, aborted, p.err);
             tc_fence_after();
+            __syncwarp();  // converged for the warp-collective TMEM accesses below
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 // does any (row of this warp, key of this 32-column half) pair lie in the window?
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                     uint32_t sv[32], dv[32];
                     tmem_ld32(tmem + lane_base + kColS + 32 * hh, sv);
                     tmem_ld32(tmem + lane_base + kColP + 32 * hh, dv);
-                    tmem_ld_wait();
+                    tmem_ld_wait(sv, dv);
                     const int32_t dj = d0 - 32 * hh;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -427,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                     kt[4 * c + 2] = lerp_bf16x2(x.z, y.z, wk);
                     kt[4 * c + 3] = lerp_bf16x2(x.w, y.w, wk);
                 }
+                fence_proxy_async_smem();  // generic reads before the TMA refill
                 mbar_arrive(B_EMPTY(s));
                 ++seq;
                 const float slo = (a0 + a1) + (a2 + a3), shi = (b0 + b1) + (b2 + b3);
@@ -447,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                     fma2_bf16(gw[4 * c + 2], y.z, b0, b1);
                     fma2_bf16(gw[4 * c + 3], y.w, b2, b3);
                 }
+                fence_proxy_async_smem();  // generic reads before the TMA refill
                 mbar_arrive(B_EMPTY(s));
                 ++seq;
                 const float dlo = (a0 + a1) + (a2 + a3), dhi = (b0 + b1) + (b2 + b3);
@@ -481,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                         fma2_bf16(x.z, y.z, a0, a1);
                         fma2_bf16(x.w, y.w, a2, a3);
                     }
+                    fence_proxy_async_smem();  // generic reads before the TMA refill
                     mbar_arrive(B_EMPTY(s));
                 }
                 const float sdot = (a0 + a1) + (a2 + a3);
@@ -498,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                         fma2_bf16(gw[32 * qh + 4 * c + 2], x.z, b0, b1);
                         fma2_bf16(gw[32 * qh + 4 * c + 3], x.w, b2, b3);
                     }
+                    fence_proxy_async_smem();  // generic reads before the TMA refill
                     mbar_arrive(B_EMPTY(s));
                 }
                 const float dpd = (b0 + b1) + (b2 + b3);
@@ -514,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
             mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
             uint32_t kw[32];
             load_row_sw(smem + kOffRing + s * kSlot, r, kw);
+            fence_proxy_async_smem();  // generic reads before the TMA refill
             mbar_arrive(B_EMPTY(s));
             ++seq;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -543,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                     fma2_bf16(gw[4 * c + 3], x.w, b2, b3);
                 }
             }
+            fence_proxy_async_smem();  // generic reads before the TMA refill
             mbar_arrive(B_EMPTY(s));
             ++seq;
             const float dpd = (b0 + b1) + (b2 + b3);
@@ -567,11 +575,12 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
         // ---- epilogue: dq = scale (dQ_band + dq_off), staged in the Q tile, TMA store
         mbar_wait(B_DQ, (n_chunks - 1) & 1, aborted, p.err);
         tc_fence_after();
+        __syncwarp();  // converged for the warp-collective TMEM accesses below
         uint8_t* stage = smem + kOffQ;
         for (int h = 0; h < 2; ++h) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_base + 32 * h, v);
-            tmem_ld_wait();
+            tmem_ld_wait(v);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int e = 8 * c, d = 32 * h + e;
@@ -943,6 +952,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                     mbar_wait(B_S, mcount & 1, aborted, p.err);
                     rg.wait_full(cseq, aborted, p.err);  // lse*log2(e) / D side data
                     tc_fence_after();
+                    __syncwarp();  // converged for the warp-collective TMEM accesses below
                     const int32_t klo = j0 + 32 * q4;
                     const bool need = (qb + 31 - klo >= 0) && (qb - (klo + 31) < W) && qb < T;
                     const float* L = side_ptr(cseq) + 32 * h;
@@ -956,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                             uint32_t sv[16], dv[16];
                             tmem_ld16(tmem + lane_base + kColS + col, sv);
                             tmem_ld16(tmem + lane_base + kColP + col, dv);
-                            tmem_ld_wait();
+                            tmem_ld_wait(sv, dv);
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 const int ee = 16 * half + e;
@@ -978,6 +988,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                     }
                     tmem_st_wait();
                     tc_fence_before();
+                    // the item's side data was read with generic loads; the MMA warp releases
+                    // the slot to the next bulk copy after this arrival
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(B_P);
                 }
@@ -1048,12 +1061,13 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                 }
                 // add into TMEM: dK columns [32h, +32) after the first pass, dV after the second
                 if (pl.n_act > 0) {
+                    __syncwarp();  // converged for the warp-collective TMEM accesses below
                     const uint32_t col = (pass == 0 ? kColDK : kColDV) + 32 * h;
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         uint32_t v[16];
                         tmem_ld16(tmem + lane_base + col + 16 * q, v);
-                        tmem_ld_wait();
+                        tmem_ld_wait(v);
 #pragma unroll
                         for (int c = 0; c < 16; ++c)
                             v[c] = __float_as_uint(__uint_as_float(v[c]) + acc[16 * q + c]);
@@ -1068,10 +1082,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             seq += 2;
             rg.wait_full(kst, aborted, p.err);
             rg.wait_full(vst, aborted, p.err);
+            __syncwarp();  // converged for the warp-collective TMEM accesses below
             {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + kColDK + 32 * h, v);
-                tmem_ld_wait();
+                tmem_ld_wait(v);
                 uint8_t* st = slot_ptr(kst);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -1084,7 +1099,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                     *reinterpret_cast<uint4*>(st + sw128_off(r, 4 * h + c)) = w;
                 }
                 tmem_ld32(tmem + lane_base + kColDV + 32 * h, v);
-                tmem_ld_wait();
+                tmem_ld_wait(v);
                 st = slot_ptr(vst);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {

@@ -388,6 +388,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                 const int n_need = colA <= colB ? colB / 32 - ccA + 1 : 0;
                 mbar_wait(B_S, (gbase + g) & 1, aborted, p.err);
                 tc_fence_after();
+                __syncwarp();  // converged for the warp-collective TMEM accesses below
                 float mn = m_b;
                 {
                     // two passes over the reachable 32-column chunks: the row max, then the
@@ -396,7 +397,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                     float mx = -INFINITY;
                     for (int j = 0; j < n_need; ++j) {
                         tmem_ld32(tmem + lane_base + 32 * (ccA + j), v);
-                        tmem_ld_wait();
+                        tmem_ld_wait(v);
                         const int32_t dj = d0 - 32 * (ccA + j);
     #pragma unroll
                         for (int e = 0; e < 32; ++e)
@@ -410,7 +411,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                         if (__any_sync(0xffffffffu, mn != m_b)) {
                             for (int h = 0; h < 2; ++h) {
                                 tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
-                                tmem_ld_wait();
+                                tmem_ld_wait(v);
     #pragma unroll
                                 for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
                                 tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
@@ -425,7 +426,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                         uint32_t pk[16];
                         if (j >= 0 && j < n_need) {
                             tmem_ld32(tmem + lane_base + 32 * cc, v);
-                            tmem_ld_wait();
+                            tmem_ld_wait(v);
                             const int32_t dj = d0 - 32 * cc;
     #pragma unroll
                             for (int e = 0; e < 32; e += 2) {
@@ -564,11 +565,12 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             const uint32_t oseq = seq++;
             rg.wait_full(oseq, aborted, p.err);
             uint8_t* orow = slot_ptr(oseq);
+            __syncwarp();  // converged for the warp-collective TMEM accesses below
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
-                tmem_ld_wait();
+                tmem_ld_wait(v);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint4 w;

@@ -87,8 +87,12 @@ struct Ring {
     __device__ __forceinline__ bool wait_full(uint32_t seq, bool& aborted, int32_t* err) const {
         return tc::mbar_wait(full(seq), parity(seq), aborted, err);
     }
-    // row-warp release: every lane has finished reading the slot
+    // row-warp release: every lane has finished reading the slot. The lanes read it with
+    // generic loads and the next fill is a TMA write (the async proxy): without a proxy fence
+    // the mbarrier hand-off orders only the generic proxy, and the refill may land in the slot
+    // before those loads have read it.
     __device__ __forceinline__ void release_warp(uint32_t seq, int lane) const {
+        tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(empty(seq));
     }

@@ -231,6 +231,27 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// tcgen05.ld writes its destination registers asynchronously: they hold the loaded values
+// only after tcgen05.wait::ld. The wait above carries no register operands, so nothing stops
+// the compiler from scheduling arithmetic on those registers before it. These forms pass
+// every destination register through an empty volatile asm after the wait (volatile asm
+// statements keep their order), so each use of a register depends on a point after the wait.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <int N, int M>
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&a)[N], uint32_t (&b)[M]) {
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(a[i]));
+#pragma unroll
+    for (int i = 0; i < M; ++i) asm volatile("" : "+r"(b[i]));
+}
+
 // Warp-collective TMEM store of 16 consecutive 32-bit columns per lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(

@@ -80,3 +80,27 @@ def test_d128_deterministic_and_halves_consistent():
     v2 = torch.cat((dev["v"][..., 64:], dev["v"][..., :64]), dim=-1).contiguous()
     c = fa.fwd(dev["q"], dev["k"], v2, 64, sc)
     assert torch.equal(c[0][..., :64], a[0][..., 64:]) and torch.equal(c[0][..., 64:], a[0][..., :64])
+
+
+def test_d128_training_step_sampled():
+    # the head-size-128 training step at full size, in the launch configuration the bench
+    # times: forward + backward of all 16 layers in one call each; per layer one (b, h)
+    # slice checked in full against the oracle
+    spec = fi.WORKLOADS["c5w"]
+    inp = fi.workload_inputs("c5w")
+    dev = to_dev(inp)
+    sc = lib_schedule(spec["sched"])
+    W = spec["W"]
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], W, sc)
+    dq, dk, dv = fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], W, sc)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    for l in range(spec["Lc"]):
+        tab = oracle_table(spec["sched"], l, W, spec["T"])
+        b, h = (3 * l) % spec["B"], (l + l // 4) % spec["H"]
+        g = lambda n: f64(inp[n][l, b, h])[None]
+        rq, rk, rv, ro, rl = oracle.bwd(g("q"), g("k"), g("v"), g("dO"), W, tab)
+        assert max_abs(f64(o[l, b, h])[None], ro) <= TOL["bf16"], l
+        assert max_abs(f64(lse[l, b, h])[None], rl) <= LSE_TOL["bf16"], l
+        for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+            assert max_abs(f64(got[l, b, h])[None], ref) <= TOL["bf16"], l

@@ -1,0 +1,65 @@
+"""Run-to-run determinism of the tensor-core kernels at sizes where every persistent CTA takes
+several tiles and two CTAs share an SM, with offsets present (the shifted-tile rings wrap many
+times per tile). Repeated calls on the same inputs must agree bit for bit: every output is
+written by exactly one CTA in a fixed order, so any difference is a race (for instance a ring
+slot refilled before the row threads have finished reading it)."""
+import pytest
+import torch
+
+import fibattn_inputs as fi
+import static_fibonacci_offset_fibattn_b300 as fa
+from gpu_common import lib_schedule, to_dev
+
+pytestmark = pytest.mark.gpu
+
+STAGGER = dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16)
+
+
+def _same(fn, reps):
+    ref = fn()
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        out = fn()
+        torch.cuda.synchronize()
+        for a, b in zip(out, ref):
+            assert torch.equal(a, b), int((a != b).sum())
+    fa.poll_device_error()
+
+
+@pytest.mark.parametrize("shape", [
+    # (Lc, B, H, T, d, W): many short slices with small offsets (11 per tile at W = 1), and
+    # the 16-layer stack at head size 64 and 128
+    (16, 64, 8, 128, 64, 1),
+    (16, 8, 8, 1024, 64, 64),
+    (16, 8, 4, 1024, 128, 64),
+])
+def test_forward_is_deterministic(shape):
+    Lc, B, H, T, d, W = shape
+    dev = to_dev(fi.draw((Lc, B, H, T, d), seed=5, scale=0.125, dtype="bf16"))
+    sc = lib_schedule(STAGGER)
+    _same(lambda: fa.fwd(dev["q"], dev["k"], dev["v"], W, sc), reps=5)
+
+
+def test_backward_is_deterministic():
+    spec = fi.WORKLOADS["c5"]
+    dev = to_dev(fi.workload_inputs("c5"))
+    sc = lib_schedule(spec["sched"])
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], spec["W"], sc)
+    _same(lambda: fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], spec["W"], sc), reps=3)
+
+
+def test_gqa_backward_is_deterministic():
+    spec = fi.WORKLOADS["c5g"]
+    dev = to_dev(fi.workload_inputs("c5g"))
+    sc = lib_schedule(spec["sched"])
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], spec["W"], sc)
+    _same(lambda: fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], spec["W"], sc), reps=2)
+
+
+def test_fractional_forward_and_backward_are_deterministic():
+    spec = fi.WORKLOADS["c3f"]
+    alphas = fi.frac_alphas(spec)
+    dev = to_dev(fi.workload_inputs("c3f", names=("q", "k", "v", "dO")))
+    _same(lambda: fa.fwd_frac(dev["q"], dev["k"], dev["v"], spec["W"], alphas), reps=4)
+    o, lse = fa.fwd_frac(dev["q"], dev["k"], dev["v"], spec["W"], alphas)
+    _same(lambda: fa.bwd_frac(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], spec["W"], alphas), reps=2)
