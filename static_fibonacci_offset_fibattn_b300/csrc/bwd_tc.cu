@@ -129,22 +129,26 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 64, kColP = 128;  // dQ accumulator in columns [0, 64)
 
 // barriers: 0 q+dO, 1-2 band K/V full, 3 S/dP ready, 4 dS written (128), 5 dQ MMA done,
-// 6-7 ring full, 8-9 ring empty (128)
-constexpr int kNumBars = 10;
+// 6-7 ring full, 8-9 ring empty (128), 10 band done (every band MMA has completed)
+constexpr int kNumBars = 11;
 // Shared memory: the Q and dO tiles, two stages of K and V chunks, the two ring slots (a
 // tile, plus in the fractional mode the 8 rows after it). Head size 128 (kWide) doubles the
-// tiles and the chunk stages (two 64-column halves each).
+// tiles (two 64-column halves each) but keeps one stage of K and V chunks (both halves: 16 KB
+// each), and that stage's memory is also the ring: slot 0 = the K stage, slot 1 = the V stage.
+// The ring's O items (for D) use it before the band, its offset items after the band. So the
+// CTA needs 97 KB and two fit on an SM.
 template <bool kFrac, bool kWide = false>
 struct Layout {
     static constexpr uint32_t kTileQ = kWide ? 2 * kTileBytes : kTileBytes;
     static constexpr uint32_t kStage = kWide ? 2 * kChunkBytes : kChunkBytes;
+    static constexpr uint32_t kStages = kWide ? 1 : 2;
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffDO = kOffQ + kTileQ;
-    static constexpr uint32_t kOffK = kOffDO + kTileQ;  // 2 stages
-    static constexpr uint32_t kOffV = kOffK + 2 * kStage;  // 2 stages
-    static constexpr uint32_t kOffRing = kOffV + 2 * kStage;
+    static constexpr uint32_t kOffK = kOffDO + kTileQ;  // kStages stages
+    static constexpr uint32_t kOffV = kOffK + kStages * kStage;  // kStages stages
+    static constexpr uint32_t kOffRing = kWide ? kOffK : kOffV + kStages * kStage;
     static constexpr uint32_t kSlot = kTileBytes + (kFrac ? 1024u : 0u);
-    static constexpr uint32_t kOffBar = kOffRing + 2 * kSlot;
+    static constexpr uint32_t kOffBar = kWide ? kOffV + kStage : kOffRing + 2 * kSlot;
     static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffRed = kOffTmemSlot + 16;  // 4 floats: per-warp dalpha sums
     static constexpr uint32_t kSmemAlloc = kOffRed + 16 + 1024;
@@ -155,7 +159,7 @@ struct Layout {
 // offset dots, and each accumulates dq for its own 64 output columns (dS K_half); half 0
 // alone writes D, lse log2(e) and the (P, dS) pairs.
 template <bool kFrac, bool kWide>
-__global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(const __grid_constant__ BwdArgs<kFrac> p) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_constant__ BwdArgs<kFrac> p) {
     static_assert(!(kFrac && kWide), "the fractional mode is for head size 64");
     using L = Layout<kFrac, kWide>;
     constexpr uint32_t kOffBar = L::kOffBar, kOffTmemSlot = L::kOffTmemSlot, kSlot = L::kSlot;
@@ -185,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
     const uint32_t B_DQ = bar_at(sbase, kOffBar, 5);
     auto B_FULL = [&](int s) { return bar_at(sbase, kOffBar, 6 + s); };
     auto B_EMPTY = [&](int s) { return bar_at(sbase, kOffBar, 8 + s); };
+    const uint32_t B_BD = bar_at(sbase, kOffBar, 10);
+    static_assert(!kWide || (L::kOffRing == L::kOffK && L::kOffV == L::kOffK + kSlot && L::kStage == kSlot),
+                  "head size 128: the ring slots are the K and V stages");
 
     const int32_t kstart = i0 - W + 1 > 0 ? i0 - W + 1 : 0;
     const int32_t klast = (i0 + kRows - 1 < T - 1) ? i0 + kRows - 1 : T - 1;
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
 
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b)
-            mbar_init(bar_at(sbase, kOffBar, b), (b == 4 || b >= 8) ? kRows : 1);
+            mbar_init(bar_at(sbase, kOffBar, b), (b == 4 || b == 8 || b == 9) ? kRows : 1);
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                 tma_load_3d(sbase + kOffDO + o + kChunkBytes, &p.tm_do, B_QDO, 64 * qh, i0 + kChunk, z);
             }
             auto load_chunk = [&](int c) {
-                const int s = c & 1;
+                const int s = kWide ? 0 : (c & 1);
                 const int32_t y = (c_lo + c) * kChunk;
                 mbar_arrive_expect_tx(B_KV(s), 2 * kStage);
                 for (int qh = 0; qh < kHalves; ++qh) {
@@ -233,14 +240,21 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                     tma_load_3d(sbase + kOffV + s * kStage + qh * kChunkBytes, &p.tm_v, B_KV(s), 64 * qh, y, zk);
                 }
             };
-            load_chunk(0);
-            if (n_chunks > 1) load_chunk(1);
+            if constexpr (kWide) {
+                // the stage memory holds the ring's O items until the row threads have formed D
+                mbar_wait(B_EMPTY(0), 0, aborted, p.err);
+                mbar_wait(B_EMPTY(1), 0, aborted, p.err);
+                load_chunk(0);
+            } else {
+                load_chunk(0);
+                if (n_chunks > 1) load_chunk(1);
+            }
             mbar_wait(B_QDO, 0, aborted, p.err);
             const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
             const uint32_t idesc_q = idesc_bf16(128, 64, 0, 1);
             for (int c = 0; c < n_chunks; ++c) {
-                const int s = c & 1;
-                mbar_wait(B_KV(s), (c >> 1) & 1, aborted, p.err);
+                const int s = kWide ? 0 : (c & 1);
+                mbar_wait(B_KV(s), (kWide ? c : c >> 1) & 1, aborted, p.err);
                 if (c > 0) mbar_wait(B_DQ, (c - 1) & 1, aborted, p.err);
                 tc_fence_after();
                 const uint32_t kaddr = sbase + kOffK + s * kStage;
@@ -268,11 +282,13 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                            sdesc_sw128(kaddr + half * kChunkBytes + 2048 * kk, 0, 1024),
                            idesc_q, (c > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(B_DQ);
-                if (c + 2 < n_chunks) {
+                const int next = c + (kWide ? 1 : 2);  // the chunk that reuses this stage
+                if (next < n_chunks) {
                     mbar_wait(B_DQ, c & 1, aborted, p.err);
-                    load_chunk(c + 2);
+                    load_chunk(next);
                 }
             }
+            mma_commit(B_BD);  // the stage memory is free for the ring once every MMA completes
             mbar_wait(B_DQ, (n_chunks - 1) & 1, aborted, p.err);
         }
     } else if (warp == 5) {
@@ -296,6 +312,9 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                 return dst;
             };
             for (int qh = 0; qh < kHalves; ++qh, ++seq) put(&p.tm_o, 64 * qh, i0, z, false);
+            if constexpr (kWide) {
+                if (n_act > 0) mbar_wait(B_BD, 0, aborted, p.err);  // the band chunks are done with the memory
+            }
             for (int k = 0; k < n_act; ++k) {
                 const int32_t y = i0 - offs[k];
                 for (int h = 0; h < 2; ++h)
@@ -495,13 +514,17 @@ __global__ void __launch_bounds__(kThreads, kWide ? 1 : 2) bwd_dq_tc_kernel(cons
                     const int s = seq & 1;
                     mbar_wait(B_FULL(s), (seq >> 1) & 1, aborted, p.err);
                     const uint8_t* vrow = smem + kOffRing + s * kSlot;
+                    // the dO row half from its resident tile (not held in registers: that keeps
+                    // the kernel within the registers of two CTAs per SM)
+                    const uint8_t* grow = smem + kOffDO + qh * kTileBytes;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const uint4 x = *reinterpret_cast<const uint4*>(vrow + sw128_off(r, c));
-                        fma2_bf16(gw[32 * qh + 4 * c + 0], x.x, b0, b1);
-                        fma2_bf16(gw[32 * qh + 4 * c + 1], x.y, b2, b3);
-                        fma2_bf16(gw[32 * qh + 4 * c + 2], x.z, b0, b1);
-                        fma2_bf16(gw[32 * qh + 4 * c + 3], x.w, b2, b3);
+                        const uint4 g = *reinterpret_cast<const uint4*>(grow + sw128_off(r, c));
+                        fma2_bf16(g.x, x.x, b0, b1);
+                        fma2_bf16(g.y, x.y, b2, b3);
+                        fma2_bf16(g.z, x.z, b0, b1);
+                        fma2_bf16(g.w, x.w, b2, b3);
                     }
                     fence_proxy_async_smem();  // generic reads before the TMA refill
                     mbar_arrive(B_EMPTY(s));

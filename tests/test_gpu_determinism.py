@@ -48,6 +48,14 @@ def test_backward_is_deterministic():
     _same(lambda: fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], spec["W"], sc), reps=3)
 
 
+def test_head_size_128_backward_is_deterministic():
+    spec = fi.WORKLOADS["c5w"]
+    dev = to_dev(fi.workload_inputs("c5w"))
+    sc = lib_schedule(spec["sched"])
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], spec["W"], sc)
+    _same(lambda: fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], spec["W"], sc), reps=3)
+
+
 def test_gqa_backward_is_deterministic():
     spec = fi.WORKLOADS["c5g"]
     dev = to_dev(fi.workload_inputs("c5g"))
