@@ -1020,9 +1020,17 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             }
 
             // ---- offsets, first pass: dk_j += dS q_{j+o} over my 32 dims, then folded into the
-            // dK accumulator in TMEM (the band's MMAs are done with it)
-            mbar_wait(B_M, (mcount - 1) & 1, aborted, p.err);
-            tc_fence_after();
+            // dK accumulator in TMEM. The pass accumulates in registers, so it overlaps the band's
+            // last dK/dV MMAs; their completion is awaited only before TMEM is touched (the fold,
+            // or the epilogue when no offset is active). The ring's parity waits do not need it:
+            // every band item was known to have landed before the B_S waits above returned.
+            bool band_done = false;
+            auto await_band = [&]() {
+                if (band_done) return;
+                mbar_wait(B_M, (mcount - 1) & 1, aborted, p.err);
+                tc_fence_after();
+                band_done = true;
+            };
             float acc[32];
             for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
@@ -1084,6 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                 }
                 // add into TMEM: dK columns [32h, +32) after the first pass, dV after the second
                 if (pl.n_act > 0) {
+                    await_band();
                     __syncwarp();  // converged for the warp-collective TMEM accesses below
                     const uint32_t col = (pass == 0 ? kColDK : kColDV) + 32 * h;
 #pragma unroll
@@ -1103,6 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
             // ---- epilogue: dk = scale * dK, dv = dV (band + offsets), staged, TMA stores
             const uint32_t kst = seq, vst = seq + 1;
             seq += 2;
+            await_band();
             rg.wait_full(kst, aborted, p.err);
             rg.wait_full(vst, aborted, p.err);
             __syncwarp();  // converged for the warp-collective TMEM accesses below
