@@ -53,7 +53,6 @@ ALGO_BYTES = {
     "fwd_frac_tc_bf16": 3 * 128 + 128 + 4,     # the same for fractional offsets
     "fwd_tc128_bf16": 3 * 256 + 256 + 4,       # head size 128: rows of 256 B
     "fwd_frac_simt_f32": 3 * 256 + 256 + 4,
-    "fwd_simt_bf16": 3 * 128 + 128 + 4,
     "fwd_simt_f32": 3 * 256 + 256 + 4,
     "bwd_delta_simt": 2 * 256 + 4,              # fp32: o, dO in; D out
     "bwd_dq_simt": 4 * 256 + 8 + 256,           # fp32: q, k, v, dO, lse, D in; dq out
@@ -71,12 +70,12 @@ ALGO_BYTES = {
     "rope_f32": 2 * 256,
 }
 # Rows per query token of each kernel that are k/v-shaped (k, v in; dk, dv out).
-KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_simt_bf16": 2, "fwd_tc128_bf16": 2, "bwd_dq_tc": 2,
+KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_tc128_bf16": 2, "bwd_dq_tc": 2,
            "bwd_dkdv_tc": 4, "bwd_dq_simt": 2, "bwd_dkdv_simt": 4, "bwd_dq_tc128": 2,
            "bwd_dkdv_tc128": 4}
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
-    "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_bf16": "simt.cu", "fwd_simt_f32": "simt.cu",
+    "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_f32": "simt.cu",
     "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu", "fwd_tc128_bf16": "fwd_tc.cu",
     "bwd_dq_frac_tc": "bwd_tc.cu", "bwd_dkdv_frac_tc": "bwd_tc.cu",
     "bwd_dq_frac_simt": "simt.cu", "bwd_dkdv_frac_simt": "simt.cu", "dalpha_reduce": "simt.cu",

@@ -101,9 +101,6 @@ struct AttnShape {
 fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o,
                                    float* lse, const AttnShape& sh, const OffsetTables& t,
                                    cudaStream_t st);
-fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v, void* o,
-                                    float* lse, const AttnShape& sh, const OffsetTables& t,
-                                    cudaStream_t st);
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
 // The same forward at head size 128 (two CTAs per tile, one per half of the output columns).

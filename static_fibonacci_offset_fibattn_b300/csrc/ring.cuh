@@ -44,18 +44,6 @@ __device__ __forceinline__ Tile tile_of(uint32_t idx, uint32_t tiles_per_slice, 
     return t;
 }
 
-// A walking position in the ring (slot and the parity of its current use), advanced one
-// item at a time without divisions.
-struct Pos {
-    uint32_t slot = 0, phase = 0;
-    __device__ __forceinline__ void next(uint32_t slots) {
-        if (++slot == slots) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
-};
-
 struct Ring {
     uint32_t base;            // shared address of slot 0 (1024-byte aligned)
     uint32_t full0;           // shared address of FULL[0]; EMPTY[i] follows the FULL array
@@ -69,12 +57,6 @@ struct Ring {
     __device__ __forceinline__ uint32_t empty(uint32_t seq) const { return full0 + 8u * (slots + slot(seq)); }
     __device__ __forceinline__ uint32_t parity(uint32_t seq) const { return (seq / slots) & 1u; }
 
-    __device__ __forceinline__ uint32_t addr_at(const Pos& q) const { return base + q.slot * slot_bytes; }
-    __device__ __forceinline__ uint32_t full_at(const Pos& q) const { return full0 + 8u * q.slot; }
-    __device__ __forceinline__ uint32_t empty_at(const Pos& q) const { return full0 + 8u * (slots + q.slot); }
-    __device__ __forceinline__ bool acquire_at(const Pos& q, bool& aborted, int32_t* err) const {
-        return tc::mbar_wait(empty_at(q), q.phase ^ 1u, aborted, err);
-    }
 
     // producer: wait until the slot of `seq` is free
     __device__ __forceinline__ bool acquire(uint32_t seq, bool& aborted, int32_t* err) const {

@@ -9,7 +9,6 @@
 // explainer, Metodologia / Arquitetura, "Conjunto Atendido"): query i sees keys
 // i - W + 1 .. i (clipped at 0) and i - o for each table offset o <= i. Table offsets
 // are >= W, so the two parts never overlap.
-#include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -67,33 +66,6 @@ struct VIo<float, 4> {
     }
     static __device__ __forceinline__ void st(float* p, const Vec<4>& v) {
         *reinterpret_cast<float4*>(p) = make_float4(v.x[0], v.x[1], v.x[2], v.x[3]);
-    }
-};
-template <>
-struct VIo<__nv_bfloat16, 2> {
-    static __device__ __forceinline__ Vec<2> ld(const __nv_bfloat16* p) {
-        const float2 a = __bfloat1622float2(__ldg(reinterpret_cast<const __nv_bfloat162*>(p)));
-        return Vec<2>{{a.x, a.y}};
-    }
-    static __device__ __forceinline__ void st(__nv_bfloat16* p, const Vec<2>& v) {
-        *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(make_float2(v.x[0], v.x[1]));
-    }
-};
-template <>
-struct VIo<__nv_bfloat16, 4> {
-    static __device__ __forceinline__ Vec<4> ld(const __nv_bfloat16* p) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-        return Vec<4>{{a.x, a.y, b.x, b.y}};
-    }
-    static __device__ __forceinline__ void st(__nv_bfloat16* p, const Vec<4>& v) {
-        const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v.x[0], v.x[1]));
-        const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(v.x[2], v.x[3]));
-        uint2 u;
-        u.x = *reinterpret_cast<const uint32_t*>(&a);
-        u.y = *reinterpret_cast<const uint32_t*>(&b);
-        *reinterpret_cast<uint2*>(p) = u;
     }
 };
 
@@ -528,23 +500,6 @@ fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* 
     return launch_status("launch SIMT kernel");
 }
 
-fibattn_status launch_fwd_simt_bf16(const void* q, const void* k, const void* v, void* o,
-                                    float* lse, const AttnShape& sh, const OffsetTables& t,
-                                    cudaStream_t st) {
-    typedef __nv_bfloat16 E;
-    const int64_t rows = sh.slices_per_layer * sh.T;
-    const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (blocks > 0x7fffffff) return FIBATTN_ERR_INVALID_ARG;
-    dim3 grid((unsigned)blocks, sh.n_layers);
-    KernelScope ks("fwd_simt_bf16", st);
-    if (sh.d == 128)
-        fwd_simt_kernel<E, 128><<<grid, kWarpsPerBlock * 32, 0, st>>>(
-            (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
-    else
-        fwd_simt_kernel<E, 64><<<grid, kWarpsPerBlock * 32, 0, st>>>(
-            (const E*)q, (const E*)k, (const E*)v, (E*)o, lse, sh, t);
-    return launch_status("launch SIMT kernel");
-}
 
 fibattn_status launch_fwd_frac_simt_f32(const float* q, const float* k, const float* v, float* o,
                                         float* lse, const AttnShape& sh, const FracTables& t,

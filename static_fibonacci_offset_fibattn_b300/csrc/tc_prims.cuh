@@ -91,19 +91,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& a
     }
 }
 
-// ------------------------------------------------------------------ cp.async (side data)
-// 4-byte asynchronous global -> shared copy; src_bytes = 0 writes zero without reading.
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
-// One arrival on `bar` once every cp.async this thread issued before has completed (the
-// arrival counts toward the barrier's expected count).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // ------------------------------------------------------------------ TMA
 // 3D tiled load, box written to smem with the tensor map's swizzle; completion is
 // signalled as transaction bytes on `bar`.

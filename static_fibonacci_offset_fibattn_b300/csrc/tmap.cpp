@@ -53,8 +53,4 @@ int make_bf16_rows8_map(CUtensorMap* m, const void* base, int64_t slices, int32_
     return make_map(m, base, slices, T, 8);
 }
 
-int make_bf16_tile_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T) {
-    return make_map(m, base, slices, T, 2 * kTmaBoxRows);
-}
-
 }  // namespace fibattn

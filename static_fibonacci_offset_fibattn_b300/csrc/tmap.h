@@ -23,7 +23,4 @@ int make_bf16_rows_map_d(CUtensorMap* m, const void* base, int64_t slices, int32
 // The same map with an 8-row box (1 KB): the rows just past a 128-row tile.
 int make_bf16_rows8_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T);
 
-// The same map with a 128-row box (one 16 KB copy per 128-row tile).
-int make_bf16_tile_map(CUtensorMap* m, const void* base, int64_t slices, int32_t T);
-
 }  // namespace fibattn
