@@ -108,6 +108,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the 4x-length forward and dense-context records")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -188,13 +190,14 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.window = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.windows = {}
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="fibattn_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
                                           f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
@@ -203,8 +206,8 @@ class Clocks:
             self.proc = None
         return self
 
-    def mark(self, t0, t1):
-        self.window = (t0, t1)
+    def mark(self, t0, t1, name="main"):
+        self.windows[name] = (t0, t1)
 
     def stop(self):
         if self.proc is not None:
@@ -216,9 +219,14 @@ class Clocks:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self):
+    def cleanup(self):
+        if self.path and os.path.exists(self.path):
+            os.remove(self.path)
+
+    def summary(self, name="main"):
         import datetime
-        if self.proc is None or not os.path.exists(self.path) or self.window is None:
+        window = self.windows.get(name)
+        if self.proc is None or not self.path or not os.path.exists(self.path) or window is None:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         rows = []
@@ -234,7 +242,7 @@ class Clocks:
                 continue
         if not rows:
             return None
-        t0, t1 = self.window
+        t0, t1 = window
         inside = [r for r in rows if t0 <= r[0] <= t1]
         picked = inside
         if not picked:
@@ -245,6 +253,119 @@ class Clocks:
         return {"sm_mhz": statistics.median(r[1] for r in picked), "sm_max_mhz": picked[-1][2],
                 "reasons": sorted(reasons), "samples_in_window": len(inside),
                 "samples_used": len(picked), "window_ms": round((t1 - t0) * 1e3, 2)}
+
+
+def read_profile(L):
+    """Per-kernel (total ms, launches) since the previous read, from the library's events."""
+    names = ctypes.create_string_buffer(64 * 32)
+    tot = (ctypes.c_double * 32)()
+    cnt = (ctypes.c_int64 * 32)()
+    nk = L.fibattn_profile_read(names, 64, tot, cnt, 32)
+    per_kernel = {}
+    for i in range(min(nk, 32)):
+        nm = names.raw[i * 64:(i + 1) * 64].split(b"\0")[0].decode()
+        if cnt[i]:
+            per_kernel[nm] = (tot[i], int(cnt[i]))
+    return per_kernel
+
+
+def timed_calls(fn, steps, warmup, flush, stream, dev, L, clk=None, name=None):
+    """`warmup` untimed calls of fn(), then `steps` calls each between CUDA events on the
+    launch stream, L2 flushed between calls outside the event pairs. Returns (mean ms per
+    call, {kernel: (total ms, launches)} of the library's kernels in the timed calls)."""
+    for _ in range(warmup):
+        fn()
+        flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+    L.fibattn_profile_read(None, 0, None, None, 0)
+    L.fibattn_profile_enable(1)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    t0 = time.time()
+    for s, e in evs:
+        s.record(stream)
+        fn()
+        e.record(stream)
+        flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+    if clk is not None:
+        clk.mark(t0, time.time(), name)
+    L.fibattn_profile_enable(0)
+    per_kernel = read_profile(L)
+    return sum(s.elapsed_time(e) for s, e in evs) / steps, per_kernel
+
+
+def kernel_roofline(kernel, per_kernel, spec, workload, hbm, peak_kind):
+    """The roofline record of one kernel: algorithmic bytes of one launch (ALGO_BYTES per
+    query token times the tokens of a launch, at most 16 layers) over its mean launch time."""
+    ms, n = per_kernel[kernel]
+    per_launch_tokens = tokens(spec) / max(1, math.ceil(spec["Lc"] / 16))
+    algo = algo_bytes(kernel, spec) * per_launch_tokens
+    avg_s = ms / n / 1e3
+    achieved = algo / avg_s / 1e9
+    traffic_pt = committed_traffic(kernel, workload)
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm,
+            "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "traffic": None if traffic_pt is None else round(traffic_pt * per_launch_tokens),
+            "algorithmic_bytes_per_launch": int(algo), "avg_launch_us": round(avg_s * 1e6, 2)}
+
+
+def extrapolation_forward_record(fa, L, dev, stream, flush, a, clk, hbm, peak_kind):
+    """The 4x-length forward (16 layers x B2 H8 T4096 d64, W=64, linear stagger 0.5 -> 2.0)
+    timed like the main step: its roofline fraction is the forward's target at T = 4096."""
+    spec = fi.WORKLOADS["c4"]
+    x = {n: t.to(dev) for n, t in fi.workload_inputs("c4").items()}
+    sched = fa.Schedule(**spec["sched"])
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
+    ms, pk = timed_calls(lambda: fa.fwd(x["q"], x["k"], x["v"], spec["W"], sched, out=o, lse=lse),
+                         a.steps, a.warmup, flush, stream, dev, L, clk, "c4_fwd")
+    fa.poll_device_error(dev)
+    roof = kernel_roofline("fwd_tc_bf16", pk, spec, "c4", hbm, peak_kind)
+    return {"workload": f"c4: {spec['desc']}", "ms_per_call": round(ms, 4),
+            "query_tokens_per_s": round(tokens(spec) / (ms / 1e3), 1),
+            "roofline": roof, "target_frac": 0.60, "calls": a.steps,
+            "clocks": clk.summary("c4_fwd") if clk is not None else None}
+
+
+def dense_context_record(fa, L, dev, stream, flush, a, clk):
+    """Dense causal attention on one layer of the 4x-length inputs (B2 H8 T4096 d64, bf16) for
+    context: this library's forward with W = T (no offsets survive: the window covers every
+    earlier key), and torch's scaled_dot_product_attention(is_causal=True) on the same
+    tensors. Compute-bound: 4 d T (T + 1) / 2 flops per (b, h) slice."""
+    spec = fi.WORKLOADS["c4"]
+    x = {n: t.to(dev) for n, t in fi.workload_inputs("c4", layers=[0]).items()}
+    T, d = spec["T"], spec["d"]
+    sched = fa.Schedule(**spec["sched"])
+    assert fa.offsets(sched, 0, T, T) == []
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
+    flops = 4.0 * d * T * (T + 1) / 2 * spec["B"] * spec["H"]
+    steps = max(5, min(a.steps, 20))
+    ms_ours, _ = timed_calls(lambda: fa.fwd(x["q"], x["k"], x["v"], T, sched, out=o, lse=lse),
+                             steps, a.warmup, flush, stream, dev, L, clk, "dense")
+    fa.poll_device_error(dev)
+    q, k, v = x["q"][0], x["k"][0], x["v"][0]
+    sdpa = torch.nn.functional.scaled_dot_product_attention
+    ms_sdpa, _ = timed_calls(lambda: sdpa(q, k, v, is_causal=True), steps, a.warmup, flush,
+                             stream, dev, L)
+    err = float((sdpa(q, k, v, is_causal=True).float() - o[0].float()).abs().max())
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+        pk = "measured"
+    except Exception:
+        peak, pk = 1800.0, "fallback"
+    tf = lambda ms: flops / (ms / 1e3) / 1e12
+    return {"workload": "one layer of c4's inputs, dense causal (B2 H8 T4096 d64, bf16)",
+            "gflop": round(flops / 1e9, 2), "peak_tflops": peak,
+            "peak_kind": f"{pk} cuBLAS bf16 GEMM (burst)",
+            "ours_W_eq_T": {"ms": round(ms_ours, 4), "tflops": round(tf(ms_ours), 1),
+                            "frac": round(tf(ms_ours) / peak, 4)},
+            "torch_sdpa_causal": {"ms": round(ms_sdpa, 4), "tflops": round(tf(ms_sdpa), 1),
+                                  "frac": round(tf(ms_sdpa) / peak, 4)},
+            "max_abs_diff_vs_sdpa": err, "calls": steps}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -322,18 +443,9 @@ def run_ours(a, spec, world, rank, local):
         flush.fill_(1.0)
     torch.cuda.synchronize(dev)
     clk.mark(t_host0, time.time())
-    clk.stop()
     launches = L.fibattn_launch_count() - n0
     L.fibattn_profile_enable(0)
-    names = ctypes.create_string_buffer(64 * 32)
-    tot = (ctypes.c_double * 32)()
-    cnt = (ctypes.c_int64 * 32)()
-    nk = L.fibattn_profile_read(names, 64, tot, cnt, 32)
-    per_kernel = {}
-    for i in range(min(nk, 32)):
-        nm = names.raw[i * 64:(i + 1) * 64].split(b"\0")[0].decode()
-        if cnt[i]:
-            per_kernel[nm] = (tot[i], int(cnt[i]))
+    per_kernel = read_profile(L)
     if world > 1:
         torch.distributed.barrier()
     fa.poll_device_error(dev)
@@ -342,26 +454,20 @@ def run_ours(a, spec, world, rank, local):
     ms_per_step = total_ms / a.steps
     value = job_rate(tokens(spec), world, ms_per_step)
 
-    # ---- roofline of the dominant kernel
+    # ---- roofline of the dominant kernel, and of every kernel of the step
     hbm, peak_kind = peaks()
     dom = max(per_kernel, key=lambda k: per_kernel[k][0]) if per_kernel else None
     roof = None
     if dom:
-        ms, n = per_kernel[dom]
-        per_launch_tokens = tokens(spec) / max(1, math.ceil(spec["Lc"] / 16))
-        algo = algo_bytes(dom, spec) * per_launch_tokens
-        avg_s = ms / n / 1e3
-        achieved = algo / avg_s / 1e9
-        traffic_pt = committed_traffic(dom, a.workload)
-        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
-                "frac": round(achieved / hbm, 4),
-                "traffic": None if traffic_pt is None else round(traffic_pt * per_launch_tokens),
-                "algorithmic_bytes_per_launch": int(algo),
-                "avg_launch_us": round(avg_s * 1e6, 2),
-                "share_of_step": round(ms / total_ms if world == 1 else ms / sum(step_ms), 4)}
-    kernels = {k: {"avg_us": round(v[0] / v[1] * 1e3, 2), "launches_per_step": v[1] / a.steps,
-                   "share": round(v[0] / sum(step_ms), 4)} for k, v in per_kernel.items()}
+        roof = kernel_roofline(dom, per_kernel, spec, a.workload, hbm, peak_kind)
+        roof["share_of_step"] = round(per_kernel[dom][0] / total_ms if world == 1
+                                      else per_kernel[dom][0] / sum(step_ms), 4)
+    kernels = {}
+    for k, v in per_kernel.items():
+        kr = kernel_roofline(k, per_kernel, spec, a.workload, hbm, peak_kind)
+        kernels[k] = {"avg_us": round(v[0] / v[1] * 1e3, 2), "launches_per_step": v[1] / a.steps,
+                      "share": round(v[0] / sum(step_ms), 4), "achieved_GBps": kr["achieved"],
+                      "frac": kr["frac"]}
 
     # ---- end to end through the public API, host buffers, copies inside the timed region
     e2e = None
@@ -403,6 +509,14 @@ def run_ours(a, spec, world, rank, local):
                        "frac_over_static": round(ms_per_step / cms, 3)}
         del cin
 
+    # ---- the forward at 4x length and the dense causal context (one GPU runs only)
+    extras = {}
+    if world == 1 and not a.no_extras:
+        extras["c4_fwd"] = extrapolation_forward_record(fa, L, dev, stream, flush, a, clk, hbm,
+                                                        peak_kind)
+        extras["dense_context_c4"] = dense_context_record(fa, L, dev, stream, flush, a, clk)
+    clk.stop()
+
     out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec["dtype"],
@@ -419,6 +533,8 @@ def run_ours(a, spec, world, rank, local):
            "clocks": clk.summary(), "e2e": e2e}
     if counterpart:
         out["static_counterpart"] = counterpart
+    out.update(extras)
+    clk.cleanup()
     return out
 
 
@@ -636,13 +752,23 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     out = run_ours(a, spec, world, rank, local)
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        import oracle
+        all_threads = oracle.threads(0)
         n = calibrate_slices(spec, 15.0)
         secs, toks, threads = oracle_sample(spec, n)
+        passes = 'fwd+bwd' if 'bwd' in spec['passes'] else 'fwd'
+        # the same oracle on one thread (then the thread count is put back)
+        s0, t0, _ = oracle_sample(spec, 4, 1)
+        n1 = max(1, int(6.0 * 4 / max(s0, 1e-6)))
+        s1, t1, _ = oracle_sample(spec, n1, 1)
+        oracle.threads(all_threads)
         out["cpu_baseline"] = {
             "value": round(toks / secs, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} (layer,b,h) slices of T={spec['T']} "
-                      f"({'fwd+bwd' if 'bwd' in spec['passes'] else 'fwd'}, fp64, OpenMP), "
-                      f"{secs:.1f} s"}
+            "sample": f"{n} (layer,b,h) slices of T={spec['T']} ({passes}, fp64, OpenMP), "
+                      f"{secs:.1f} s",
+            "single_thread": {"value": round(t1 / s1, 1), "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} (layer,b,h) slices of T={spec['T']} ({passes}, "
+                                        f"fp64, one thread), {s1:.1f} s"}}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

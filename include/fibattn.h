@@ -252,7 +252,10 @@ FIBATTN_API fibattn_status fibattn_bwd_workspace_size(int32_t B, int32_t H, int3
  *   dq, dk, dv     : written (every element; no accumulation into old contents).
  *   workspace      : device scratch owned by the caller, 256-byte aligned, at least
  *                    fibattn_bwd_workspace_size() bytes (workspace_bytes says how many);
- *                    every byte read is first written by the same call.
+ *                    its contents on entry do not matter: the backward writes every value
+ *                    it uses, and the few bytes it reads without writing (the pad rows of
+ *                    D and lse * log2(e) past T, pairs of queries past T) are discarded by
+ *                    selects, so stale or non-finite contents cannot reach the outputs.
  * bf16 runs two tcgen05 tensor-core kernels (query owner: D and dq; key owner: dk, dv);
  * f32 runs SIMT kernels. No atomics: each dq/dk/dv row is summed by the one thread block
  * that owns it.
@@ -280,9 +283,11 @@ FIBATTN_API fibattn_status fibattn_bwd(const void* q, const void* k, const void*
  *     B=8, H=8, T=1024, W=64 bf16 training step (32 MiB) fits.
  *   - The first call on a device (that device current) looks up the array's device
  *     address with cudaGetSymbolAddress; make that first call before any stream capture.
- *   - All calls on a device share the array and it keeps the last call's contents (every
- *     byte the backward reads is written earlier in the same call, so nothing needs
- *     clearing). Calls whose kernels can overlap on the GPU (unordered streams) race on it.
+ *   - All calls on a device share the array and it keeps the last call's contents. Nothing
+ *     needs clearing: the backward writes every value it uses, and what it reads without
+ *     writing (pad rows past T, pairs of queries past T) is discarded by selects, so an
+ *     earlier call's contents, even non-finite ones, cannot reach the outputs. Calls whose
+ *     kernels can overlap on the GPU (unordered streams) race on it.
  */
 #define FIBATTN_NOALLOC_SCRATCH_BYTES (40ull << 20)
 FIBATTN_API fibattn_status fibattn_bwd_noalloc(const void* q, const void* k, const void* v,

@@ -16,9 +16,11 @@
 //     device (that device current) looks the address up with cudaGetSymbolAddress and
 //     caches it; make that first call before any stream capture begins.
 //   - Every call on a device shares the one array, and it keeps the last call's contents.
-//     The backward writes every workspace byte it reads earlier in the same call, so
-//     nothing needs clearing; but calls whose kernels overlap on the GPU (different
-//     streams, no ordering between them) race on the array.
+//     Nothing needs clearing: the backward writes every workspace value it uses, and the
+//     bytes it reads without writing (the pad rows of D and lse * log2(e) past T, the pairs
+//     of queries past T) are discarded by selects, so an earlier call's contents, even
+//     non-finite ones, cannot reach the outputs. Calls whose kernels overlap on the GPU
+//     (different streams, no ordering between them) race on the array.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>

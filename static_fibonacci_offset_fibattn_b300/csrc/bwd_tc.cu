@@ -998,8 +998,12 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                                 const float p0 = ok0 ? ex2(__uint_as_float(sv[e]) * sl2 - L[ee]) : 0.f;
                                 const float p1 = ok1 ? ex2(__uint_as_float(sv[e + 1]) * sl2 - L[ee + 1]) : 0.f;
                                 pp[e >> 1] = pack_bf16x2(p0, p1);
-                                pd[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - Dd[ee]),
-                                                         p1 * (__uint_as_float(dv[e + 1]) - Dd[ee + 1]));
+                                // selects, not products with p = 0: for a query column at or
+                                // past T, Dd holds bytes this call never wrote (pad rows of the
+                                // workspace, or slot memory past the side copy), possibly
+                                // non-finite, and 0 * NaN would reach dK through the MMA
+                                pd[e >> 1] = pack_bf16x2(ok0 ? p0 * (__uint_as_float(dv[e]) - Dd[ee]) : 0.f,
+                                                         ok1 ? p1 * (__uint_as_float(dv[e + 1]) - Dd[ee + 1]) : 0.f);
                             }
                         } else {
 #pragma unroll

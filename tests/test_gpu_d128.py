@@ -8,7 +8,7 @@ import torch
 import fibattn_inputs as fi
 import oracle
 import static_fibonacci_offset_fibattn_b300 as fa
-from gpu_common import LSE_TOL, TOL, f64, lib_schedule, max_abs, oracle_table, to_dev
+from gpu_common import LSE_TOL, TOL, assert_grad, f64, lib_schedule, max_abs, oracle_table, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -48,8 +48,8 @@ def test_d128_fwd_bwd_matches_oracle(dtype, case):
     rq, rk, rv, ro, rl = oracle.bwd_gqa(g("q"), g("k"), g("v"), g("dO"), W, tabs)
     assert max_abs(f64(o), ro) <= TOL[dtype]
     assert max_abs(f64(lse), rl) <= LSE_TOL[dtype]
-    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
-        assert max_abs(f64(got), ref) <= TOL[dtype]
+    for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert_grad(n, f64(got), ref, dtype)
 
 
 def test_d128_fwd_sixteen_layers_sampled():
@@ -102,5 +102,5 @@ def test_d128_training_step_sampled():
         rq, rk, rv, ro, rl = oracle.bwd(g("q"), g("k"), g("v"), g("dO"), W, tab)
         assert max_abs(f64(o[l, b, h])[None], ro) <= TOL["bf16"], l
         assert max_abs(f64(lse[l, b, h])[None], rl) <= LSE_TOL["bf16"], l
-        for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
-            assert max_abs(f64(got[l, b, h])[None], ref) <= TOL["bf16"], l
+        for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            assert_grad(n, f64(got[l, b, h])[None], ref, "bf16", l)

@@ -12,7 +12,7 @@ import torch
 import fibattn_inputs as fi
 import oracle
 import static_fibonacci_offset_fibattn_b300 as fa
-from gpu_common import LSE_TOL, TOL, f64, max_abs, sample_slices, to_dev
+from gpu_common import LSE_TOL, TOL, assert_grad, f64, max_abs, sample_slices, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -156,7 +156,7 @@ def _check_frac_bwd(inp, W, alphas, base, dtype, layers_full=None, picks=None):
     by_layer = {}
     for (l, b, h) in need:
         by_layer.setdefault(l, []).append((b, h))
-    worst = dict(dq=0.0, dk=0.0, dv=0.0, o=0.0)
+    worst_o = 0.0
     for l, bhs in by_layer.items():
         a = f32(alphas[l])
         dists = oracle.frac_distances(a, base, W, T)
@@ -165,17 +165,16 @@ def _check_frac_bwd(inp, W, alphas, base, dtype, layers_full=None, picks=None):
         rq, rk, rv, ro, rl, rdd = oracle.bwd_frac(g("q"), g("k"), g("v"), g("dO"), W, dists)
         for n, (b, h) in enumerate(bhs):
             if (l, b, h) in picks:
-                worst["dq"] = max(worst["dq"], max_abs(f64(dq[l, b, h]), rq[n]))
-                worst["dk"] = max(worst["dk"], max_abs(f64(dk[l, b, h]), rk[n]))
-                worst["dv"] = max(worst["dv"], max_abs(f64(dv[l, b, h]), rv[n]))
-                worst["o"] = max(worst["o"], max_abs(f64(o[l, b, h]), ro[n]))
+                assert_grad("dq", f64(dq[l, b, h]), rq[n], dtype, (l, b, h))
+                assert_grad("dk", f64(dk[l, b, h]), rk[n], dtype, (l, b, h))
+                assert_grad("dv", f64(dv[l, b, h]), rv[n], dtype, (l, b, h))
+                worst_o = max(worst_o, max_abs(f64(o[l, b, h]), ro[n]))
         if l in layers_full and len(fb):
             ref = float((rdd[:, : len(fb)] * fb).sum())
             mag = float((np.abs(rdd[:, : len(fb)]) * fb).sum())
             err = abs(float(da[l]) - ref)
             assert err <= DALPHA_TOL[dtype] * max(mag, 1e-6), (l, float(da[l]), ref, mag)
-    for key, val in worst.items():
-        assert val <= TOL[dtype], (key, val)
+    assert worst_o <= TOL[dtype], worst_o
 
 
 FRAC_BWD_EDGE = [

@@ -10,7 +10,7 @@ import torch
 import fibattn_inputs as fi
 import oracle
 import static_fibonacci_offset_fibattn_b300 as fa
-from gpu_common import LSE_TOL, TOL, f64, lib_schedule, max_abs, oracle_table, to_dev
+from gpu_common import LSE_TOL, TOL, assert_grad, f64, lib_schedule, max_abs, oracle_table, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -51,8 +51,8 @@ def test_gqa_fwd_bwd_matches_oracle(dtype, case):
     rq, rk, rv, ro, rl = oracle.bwd_gqa(g("q"), g("k"), g("v"), g("dO"), W, tabs)
     assert max_abs(f64(o), ro) <= TOL[dtype]
     assert max_abs(f64(lse), rl) <= LSE_TOL[dtype]
-    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
-        assert max_abs(f64(got), ref) <= TOL[dtype]
+    for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert_grad(n, f64(got), ref, dtype)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -96,9 +96,9 @@ def test_gqa_training_step_sampled():
             rq, rk, rv, ro, rl = oracle.bwd_gqa(g("q", hs), g("k", slice(hk, hk + 1)),
                                                 g("v", slice(hk, hk + 1)), g("dO", hs), W, tab)
             assert max_abs(f64(o[l, b, hs])[None], ro) <= TOL["bf16"], (l, b)
-            assert max_abs(f64(dq[l, b, hs])[None], rq) <= TOL["bf16"], (l, b)
-            assert max_abs(f64(dk[l, b, hk:hk + 1])[None], rk) <= TOL["bf16"], (l, b)
-            assert max_abs(f64(dv[l, b, hk:hk + 1])[None], rv) <= TOL["bf16"], (l, b)
+            assert_grad("dq", f64(dq[l, b, hs])[None], rq, "bf16", (l, b))
+            assert_grad("dk", f64(dk[l, b, hk:hk + 1])[None], rk, "bf16", (l, b))
+            assert_grad("dv", f64(dv[l, b, hk:hk + 1])[None], rv, "bf16", (l, b))
 
 
 def test_gqa_autograd_wrapper():

@@ -14,8 +14,9 @@ import torch
 import fibattn_inputs as fi
 import oracle
 import static_fibonacci_offset_fibattn_b300 as fa
-from gpu_common import (LSE_TOL, TOL, f64, lib_schedule, max_abs, oracle_bwd_slices,
-                        oracle_fwd_slices, oracle_table, sample_slices, to_dev)
+from gpu_common import (LSE_TOL, TOL, assert_grad, f64, lib_schedule, max_abs,
+                        oracle_bwd_slices, oracle_fwd_slices, oracle_table, sample_slices,
+                        to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -219,6 +220,9 @@ def test_fwd_deterministic():
 # ------------------------------------------------------------------ backward
 
 def _run_bwd(name, picks_per_layer, **override):
+    """Forward and backward of a whole workload in the bench's launch configuration; every
+    picked slice's dq, dk, dv against the oracle under the absolute and the relative gate.
+    Returns the worst max-abs error and relative error per tensor (printed, for the record)."""
     spec = dict(fi.WORKLOADS[name], **override)
     inp = fi.workload_inputs(name, **override)
     dev = to_dev(inp)
@@ -230,19 +234,27 @@ def _run_bwd(name, picks_per_layer, **override):
     picks = [(l, b, h) for l in range(spec["Lc"])
              for (b, h) in sample_slices(spec["B"], spec["H"], picks_per_layer)]
     ref = oracle_bwd_slices(inp, spec["sched"], spec["W"], 0, picks)
-    worst = dict(dq=0.0, dk=0.0, dv=0.0, o=0.0)
+    worst = {n: (0.0, 0.0) for n in ("dq", "dk", "dv")}
+    worst_o = 0.0
     for (l, b, h), (rq, rk, rv, ro, rl) in ref.items():
-        worst["dq"] = max(worst["dq"], max_abs(f64(dq[l, b, h]), rq))
-        worst["dk"] = max(worst["dk"], max_abs(f64(dk[l, b, h]), rk))
-        worst["dv"] = max(worst["dv"], max_abs(f64(dv[l, b, h]), rv))
-        worst["o"] = max(worst["o"], max_abs(f64(o[l, b, h]), ro))
+        for n, got, want in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            err, rel = assert_grad(n, f64(got[l, b, h]), want, "bf16", (l, b, h))
+            worst[n] = (max(worst[n][0], err), max(worst[n][1], rel))
+        worst_o = max(worst_o, max_abs(f64(o[l, b, h]), ro))
+    assert worst_o <= TOL["bf16"], worst_o
+    print(f"{name} {override or ''} backward worst (max-abs, relative):",
+          {n: (float(f"{e:.3g}"), float(f"{r:.3g}")) for n, (e, r) in worst.items()})
     return worst
 
 
 def test_bwd_c5_training_step_sampled():
-    worst = _run_bwd("c5", 2)
-    for name, e in worst.items():
-        assert e <= TOL["bf16"], (name, e)
+    _run_bwd("c5", 2)
+
+
+def test_bwd_c5_training_step_large_gradients_sampled():
+    # the same full-size step (every persistent CTA takes many tiles) with inputs four times
+    # larger (N(0,1)/2), where the gradients are far from the absolute bound's floor
+    _run_bwd("c5", 2, scale=0.5)
 
 
 BWD_EDGE = [
@@ -272,11 +284,9 @@ def test_bwd_edge_cases(dtype, case):
     torch.cuda.synchronize()
     picks = [(0, b, h) for b in range(B) for h in range(H)]
     ref = oracle_bwd_slices(inp, sched, W, layer, picks)
-    tol = TOL[dtype] if dtype == "bf16" else 1e-4
     for (l, b, h), (rq, rk, rv, ro, rl) in ref.items():
-        assert max_abs(f64(dq[l, b, h]), rq) <= tol
-        assert max_abs(f64(dk[l, b, h]), rk) <= tol
-        assert max_abs(f64(dv[l, b, h]), rv) <= tol
+        for n, got, want in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            assert_grad(n, f64(got[l, b, h]), want, dtype, (b, h))
 
 
 def test_autograd_wrapper_matches_bwd():
@@ -303,8 +313,8 @@ def test_bwd_empty_table_is_sliding_window_gradient():
     dq, dk, dv = fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], 16, sc)
     ref = oracle_bwd_slices(inp, sched, 16, 0, [(0, 0, h) for h in range(2)])
     for (l, b, h), (rq, rk, rv, ro, rl) in ref.items():
-        for got, want in ((dq, rq), (dk, rk), (dv, rv)):
-            assert max_abs(f64(got[l, b, h]), want) <= TOL["bf16"]
+        for n, got, want in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            assert_grad(n, f64(got[l, b, h]), want, "bf16", h)
 
 
 def test_bwd_more_layers_than_one_launch_equals_per_layer_calls():

@@ -11,7 +11,7 @@ import torch
 import fibattn_inputs as fi
 import oracle
 import static_fibonacci_offset_fibattn_b300 as fa
-from gpu_common import LSE_TOL, TOL, f64, lib_schedule, max_abs, oracle_table, to_dev
+from gpu_common import LSE_TOL, TOL, assert_grad, f64, lib_schedule, max_abs, oracle_table, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -75,8 +75,8 @@ def test_attention_through_rope_matches_oracle(dtype, case):
     rq, rk, rv, ro, rl = oracle.bwd_rope(g("q"), g("k"), g("v"), g("dO"), W, tabs)
     assert max_abs(f64(o), ro) <= TOL[dtype]
     assert max_abs(f64(lse), rl) <= LSE_TOL[dtype]
-    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
-        assert max_abs(f64(got), ref) <= TOL[dtype]
+    for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert_grad(n, f64(got), ref, dtype)
 
 
 def test_rope_training_step_sampled():
@@ -96,5 +96,6 @@ def test_rope_training_step_sampled():
         g = lambda n: f64(inp[n][l, b, h])[None]
         rq, rk, rv, ro, rl = oracle.bwd_rope(g("q"), g("k"), g("v"), g("dO"), W, tab,
                                              spec["rope_base"])
-        for got, ref in ((o, ro), (dq, rq), (dk, rk), (dv, rv)):
-            assert max_abs(f64(got[l, b, h])[None], ref) <= TOL["bf16"], l
+        assert max_abs(f64(o[l, b, h])[None], ro) <= TOL["bf16"], l
+        for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            assert_grad(n, f64(got[l, b, h])[None], ref, "bf16", l)
