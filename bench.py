@@ -7,7 +7,7 @@ backward (D = rowsum(dO * O), dQ, dK, dV). Default workload: 16 layers x
 stagger alpha 0.5 -> 2.0, bf16, forward + backward.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload c5|c4|c2|c1|c3|c3p|c3f|c5f|c5g|c5r|c3w|c5w]
+                  [--workload c5|c4|c2|c1|c3|c3p|c3f|c5f|c5g|c5r|c3r|c3w|c5w]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own full batch
@@ -19,7 +19,9 @@ gradient of every layer's alpha) on the c3 / c5 shapes; their lines add
 "static_counterpart", the static c3 / c5 step (same shape and alpha range) timed in the
 same process, and the latency ratio. c5g is the c5 step with 8 query heads sharing 2 kv heads;
 c5r the c5 step with RoPE on q and k before the gather (the cos/sin table is built once,
-outside the timed region), with the static c5 step as its counterpart; c3w / c5w the c3
+outside the timed region), with the static c5 step as its counterpart; c3r the c3-shaped
+forward with RoPE applied inside the attention kernel, its line adding "unfused_counterpart",
+the same forward through two rotation launches and rotated copies; c3w / c5w the c3
 forward / c5 step at head size 128 (4 heads of 128).
 """
 from __future__ import annotations
@@ -51,6 +53,7 @@ UNIT = "query-tokens/s"
 ALGO_BYTES = {
     "fwd_tc_bf16": 3 * 128 + 128 + 4,          # q, k, v in; o, lse out
     "fwd_frac_tc_bf16": 3 * 128 + 128 + 4,     # the same for fractional offsets
+    "fwd_rope_tc_bf16": 3 * 128 + 128 + 4,     # the same with RoPE inside (table rows in L2)
     "fwd_tc128_bf16": 3 * 256 + 256 + 4,       # head size 128: rows of 256 B
     "fwd_frac_simt_f32": 3 * 256 + 256 + 4,
     "fwd_simt_f32": 3 * 256 + 256 + 4,
@@ -77,6 +80,7 @@ KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_tc128_bf16": 2, "bwd_dq_tc"
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_f32": "simt.cu",
     "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu", "fwd_tc128_bf16": "fwd_tc.cu",
+    "fwd_rope_tc_bf16": "fwd_tc.cu",
     "bwd_dq_frac_tc": "bwd_tc.cu", "bwd_dkdv_frac_tc": "bwd_tc.cu",
     "bwd_dq_frac_simt": "simt.cu", "bwd_dkdv_frac_simt": "simt.cu", "dalpha_reduce": "simt.cu",
     "rope_bf16": "rope.cu", "rope_f32": "rope.cu",
@@ -104,7 +108,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c5",
                     choices=["c5", "c4", "c2", "c1", "c3", "c3p", "c3f", "c5f", "c5g", "c5r",
-                             "c3w", "c5w"])
+                             "c3r", "c3w", "c5w"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -378,6 +382,7 @@ def run_ours(a, spec, world, rank, local):
     L = fa.lib()
     frac = "alphas" in spec
     use_rope = "rope_base" in spec
+    fused_rope = spec.get("rope_fused", False)
     sched = None if frac else fa.Schedule(**spec["sched"])
     alphas = fi.frac_alphas(spec) if frac else None
     inp = fi.workload_inputs(a.workload)
@@ -406,6 +411,9 @@ def run_ours(a, spec, world, rank, local):
             if train:
                 fa.bwd_frac(x["q"], x["k"], x["v"], o, lse, x["dO"], W, alphas, spec["base"],
                             dq=dq, dk=dk, dv=dv, dalpha=dalpha, workspace=ws)
+            return
+        if fused_rope:
+            fa.fwd_rope_fused(x["q"], x["k"], x["v"], W, sched, table, out=o, lse=lse)
             return
         if use_rope:
             fa.fwd_rope(x["q"], x["k"], x["v"], W, sched, table, out=o, lse=lse, rotated=rotated)
@@ -475,9 +483,22 @@ def run_ours(a, spec, world, rank, local):
         e2e = run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas,
                       table if use_rope else None)
 
-    # ---- fractional workload: the static step of the same shape, timed the same way
+    # ---- fractional workload: the static step of the same shape, timed the same way; RoPE
+    # inside the kernel: the two-rotation path on the same inputs
     counterpart = None
-    if frac or use_rope:
+    if fused_rope:
+        def ustep():
+            fa.fwd_rope(d_in["q"], d_in["k"], d_in["v"], W, sched, table, out=o, lse=lse,
+                        rotated=rotated)
+
+        cms, cpk = timed_calls(ustep, a.steps, a.warmup, flush, stream, dev, L)
+        fa.poll_device_error(dev)
+        counterpart = {"workload": "the same forward with q and k rotated into copies first "
+                                   "(fibattn_fwd_rope: two rotation launches, then the attention)",
+                       "ms_per_step": round(cms, 4),
+                       "kernels_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in cpk.items()},
+                       "fused_over_unfused": round(ms_per_step / cms, 3)}
+    elif frac or use_rope:
         cname = "c5" if train else "c3"
         cspec = fi.WORKLOADS[cname]
         csched = fa.Schedule(**cspec["sched"])
@@ -532,7 +553,7 @@ def run_ours(a, spec, world, rank, local):
            "roofline": roof, "kernels": kernels, "gpu_launches": int(launches),
            "clocks": clk.summary(), "e2e": e2e}
     if counterpart:
-        out["static_counterpart"] = counterpart
+        out["unfused_counterpart" if fused_rope else "static_counterpart"] = counterpart
     out.update(extras)
     clk.cleanup()
     return out
@@ -584,6 +605,8 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None, table=None
                 fa.bwd_frac(x["q"], x["k"], x["v"], r["o"], r["lse"], x["dO"], W, alphas,
                             spec["base"], dq=r["dq"], dk=r["dk"], dv=r["dv"], dalpha=r["dalpha"],
                             workspace=ws)
+        elif table is not None and spec.get("rope_fused", False):
+            fa.fwd_rope_fused(x["q"], x["k"], x["v"], W, sched, table, out=r["o"], lse=r["lse"])
         elif table is not None:
             fa.fwd_rope(x["q"], x["k"], x["v"], W, sched, table, out=r["o"], lse=r["lse"],
                         rotated=rot)

@@ -92,6 +92,12 @@ WORKLOADS = {
                 names=("q", "k", "v", "dO"), passes=("fwd", "bwd"), rope_base=10000.0,
                 sched=dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
                            n_layers=16, coprime_c=5)),
+    "c3r": dict(desc="16-layer stack forward with RoPE on q and k (base 10000) applied inside "
+                     "the attention kernel (no rotated copies), linear stagger 0.5->2.0, bf16",
+                dtype="bf16", Lc=16, B=8, H=8, T=1024, d=64, W=64, seed="per_layer:2", scale=0.125,
+                names=("q", "k", "v"), passes=("fwd",), rope_base=10000.0, rope_fused=True,
+                sched=dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
+                           n_layers=16)),
     "c3w": dict(desc="16-layer stack at head size 128 (4 heads x 128 = the same hidden 512), "
                      "linear stagger 0.5->2.0, bf16", dtype="bf16", Lc=16, B=8, H=4, T=1024, d=128,
                 W=64, seed="per_layer:2", scale=0.125, names=("q", "k", "v"), passes=("fwd",),

@@ -341,6 +341,25 @@ FIBATTN_API fibattn_status fibattn_fwd_rope(const void* q, const void* k, const 
                                             const fibattn_schedule* sched, int32_t layer0,
                                             int32_t n_layers_call, const float* rope_table,
                                             int32_t table_rows, void* cuda_stream);
+/*
+ * The forward with RoPE applied inside the attention kernel (same passages as
+ * fibattn_fwd_rope): q and k are read unrotated and no rotated copy is written. The band's
+ * Q and K tiles are rotated in shared memory (the standalone rotation's arithmetic and bf16
+ * rounding). Each offset's score is taken as (R_o q_i) . k_(i-o), equal to the rotated
+ * tensors' score since rotations compose, with the angle o theta_p of table row o. Results
+ * agree with fibattn_fwd_rope to rounding; o and lse as fibattn_fwd.
+ * For callers without room or use for the rotated copies: a forward-only (inference) pass
+ * that keeps no q_rot/k_rot buffers, 2 x [Lc][B][H(_kv)][T][d] bf16 less memory. Training keeps
+ * fibattn_fwd_rope, whose rotated tensors the backward needs.
+ * bf16, d = 64 (others: UNSUPPORTED). Other arguments and errors as fibattn_fwd_rope.
+ */
+FIBATTN_API fibattn_status fibattn_fwd_rope_fused(const void* q, const void* k, const void* v,
+                                                  void* o, float* lse, int32_t B, int32_t H,
+                                                  int32_t H_kv, int32_t T, int32_t d,
+                                                  int32_t dtype, int32_t W, float scale,
+                                                  const fibattn_schedule* sched, int32_t layer0,
+                                                  int32_t n_layers_call, const float* rope_table,
+                                                  int32_t table_rows, void* cuda_stream);
 FIBATTN_API fibattn_status fibattn_bwd_rope(const void* q_rot, const void* k_rot, const void* v,
                                             const void* o, const float* lse, const void* dO,
                                             void* dq, void* dk, void* dv, void* workspace,

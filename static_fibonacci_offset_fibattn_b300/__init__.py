@@ -25,7 +25,7 @@ __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd"
            "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
            "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac", "bwd_frac",
            "bwd_frac_workspace_size", "FibFracAttention", "rope_table", "rope", "fwd_rope",
-           "bwd_rope", "debug_wait_timeout"]
+           "bwd_rope", "fwd_rope_fused", "debug_wait_timeout"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
@@ -125,6 +125,8 @@ def lib():
         L.fibattn_rope.argtypes = [vp, vp, ctypes.c_int64, i32, i32, i32, vp, i32, i32, vp]
         L.fibattn_fwd_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                        i32, f32, sp, i32, i32, vp, i32, vp]
+        L.fibattn_fwd_rope_fused.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                             f32, sp, i32, i32, vp, i32, vp]
         L.fibattn_bwd_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
                                        i32, i32, i32, i32, f32, sp, i32, i32, vp, i32, vp]
         L.fibattn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
@@ -150,7 +152,7 @@ def lib():
                      "fibattn_bwd_noalloc", "fibattn_keyset_debug", "fibattn_poll_device_error",
                      "fibattn_frac_offsets", "fibattn_fwd_frac", "fibattn_bwd_frac",
                      "fibattn_fwd_gqa", "fibattn_bwd_gqa", "fibattn_rope_table", "fibattn_rope",
-                     "fibattn_fwd_rope", "fibattn_bwd_rope",
+                     "fibattn_fwd_rope", "fibattn_bwd_rope", "fibattn_fwd_rope_fused",
                      "fibattn_bwd_frac_workspace_size"):
             getattr(L, name).restype = i32
         _lib = L
@@ -518,6 +520,29 @@ def fwd_rope(q, k, v, W: int, sched: Schedule, table: torch.Tensor, layer0: int 
                                 _stream(q))
     _check(st, "fibattn_fwd_rope")
     return o, lse, (qr, kr)
+
+
+def fwd_rope_fused(q, k, v, W: int, sched: Schedule, table: torch.Tensor, layer0: int = 0,
+                   scale: Optional[float] = None, out=None, lse=None):
+    """Forward with RoPE applied inside the attention kernel (fibattn_fwd_rope_fused): q and k
+    are read unrotated and no rotated copy is written, for forward-only callers (bf16, d = 64).
+    Returns (o, lse); agrees with fwd_rope to rounding."""
+    Lc, B, H, T, d = _shape(q)
+    Hkv = _kv_heads(q, k, v)
+    o = torch.empty_like(q) if out is None else out
+    _check_tensors(q, o)
+    _check_tensors(k, v)
+    _check_table(table, T, q)
+    if k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("q/k/v must share device and dtype")
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    s = sched.to_c()
+    st = lib().fibattn_fwd_rope_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, T,
+                                      d, _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s),
+                                      layer0, Lc, _ptr(table), table.shape[0], _stream(q))
+    _check(st, "fibattn_fwd_rope_fused")
+    return o, lse
 
 
 def bwd_rope(q_rot, k_rot, v, o, lse, dO, W: int, sched: Schedule, table: torch.Tensor,

@@ -371,6 +371,41 @@ fibattn_status fibattn_bwd_rope(const void* q_rot, const void* k_rot, const void
                         table_rows, 1, cuda_stream);
 }
 
+fibattn_status fibattn_fwd_rope_fused(const void* q, const void* k, const void* v, void* o,
+                                      float* lse, int32_t B, int32_t H, int32_t H_kv, int32_t T,
+                                      int32_t d, int32_t dtype, int32_t W, float scale,
+                                      const fibattn_schedule* sched, int32_t layer0,
+                                      int32_t n_layers_call, const float* rope_table,
+                                      int32_t table_rows, void* cuda_stream) {
+    if (!rope_table || !aligned16(rope_table) || table_rows < T) return FIBATTN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !lse) return FIBATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FIBATTN_ERR_INVALID_ARG;
+    if (H_kv < 1 || H < 1 || H % H_kv != 0) return FIBATTN_ERR_INVALID_ARG;
+    fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
+    if (st != FIBATTN_OK) return st;
+    if (dtype != FIBATTN_BF16 || d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    const int64_t per_layer = (int64_t)B * H * T;
+    const int64_t per_layer_kv = (int64_t)B * H_kv * T;
+    const size_t es = elt_size(dtype);
+    for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
+        const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
+        OffsetTables t;
+        st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
+        if (st != FIBATTN_OK) return st;
+        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv, d};
+        const size_t off = (size_t)c * per_layer * d * es;
+        const size_t koff = (size_t)c * per_layer_kv * d * es;
+        st = launch_fwd_rope_tc_bf16((const char*)q + off, (const char*)k + koff,
+                                     (const char*)v + koff, (char*)o + off,
+                                     lse + (size_t)c * per_layer, sh, t, rope_table,
+                                     as_stream(cuda_stream));
+        if (st != FIBATTN_OK) return st;
+    }
+    return FIBATTN_OK;
+}
+
 fibattn_status fibattn_fwd_rope(const void* q, const void* k, const void* v, void* q_rot,
                                 void* k_rot, void* o, float* lse, int32_t B, int32_t H,
                                 int32_t H_kv, int32_t T, int32_t d, int32_t dtype, int32_t W,

@@ -37,6 +37,18 @@
 // two row dot products and the value update two axpys with p (1 - w) and p w. A distance
 // with w = 0 takes the static code path, so integer alphas give the static results.
 //
+// RoPE inside the kernel (kRope; Metodologia / Arquitetura, "Implementacao": RoPE applied
+// before the gather, vanilla, no scaling): q and k arrive unrotated with the cos/sin table of
+// every position. Before each band group's S MMAs the row threads rotate the group's Q copy
+// and K chunks in their ring slots (row i by i theta_p, the unfused rotation's arithmetic and
+// bf16 rounding), so the band is the attention of the rotated tensors. The offsets need no
+// rotated copy: with R_a the rotation by the angles a theta_p,
+//   (R_i q_i) . (R_(i-o) k_(i-o)) = (R_o q_i) . k_(i-o),
+// one angle per offset for the whole tile, taken from table row o. Per pair p, with
+// a = q_2p k_2p + q_2p+1 k_2p+1 and b = q_2p k_2p+1 - q_2p+1 k_2p, the score gains
+// cos(o theta_p) a + sin(o theta_p) b. The row threads keep their unrotated q row in
+// registers for this (read before the rotation), and v is never rotated.
+//
 // Head size 128 (kWide): rows are two 64-column halves (two 128-byte swizzle atoms). Each
 // tile is taken by two CTAs, CTA half h writing output columns [64h, 64h+64): both compute
 // the full scores (S over both halves of Q and K: 8 MMA k-steps; the offsets' row dots over
@@ -82,8 +94,8 @@ struct Layout {
 // warp signals once it has waited for every band item of the tile -- a parity wait is only
 // exact when the slot's previous use is known to have landed.
 constexpr uint32_t kBarS = 2 * kSlots, kBarP = kBarS + 1, kBarO = kBarS + 2, kBarT = kBarS + 3,
-                   kBarL = kBarS + 4;
-constexpr uint32_t kNumBars = kBarL + 1;
+                   kBarL = kBarS + 4, kBarR = kBarS + 5;
+constexpr uint32_t kNumBars = kBarR + 1;  // kBarR: a group's Q and K rotated (RoPE mode)
 template <bool kFrac>
 __host__ __device__ constexpr uint32_t tmem_slot_off() { return Layout<kFrac>::kOffBar + kNumBars * 8; }
 template <bool kFrac>
@@ -102,6 +114,7 @@ struct FwdParams {
     int32_t tiles_per_slice;
     float scale_log2;  // scale * log2(e)
     OffsetTables tabs;          // fractional mode: ceil(d) of each real distance d
+    const float4* rope;         // RoPE mode: cos/sin table [rows][16] (pairs (cos, sin))
 };
 
 template <bool kFrac>
@@ -160,10 +173,47 @@ __device__ __forceinline__ ring::Tile tile_at(const FwdParams& p, uint32_t idx, 
     return ring::tile_of(kWide ? idx >> 1 : idx, p.tiles_per_slice, p.slices_per_layer);
 }
 
-template <bool kFrac, bool kWide>
+// Rotation of one bf16 pair (x0, x1) by the angle with cosine c and sine s, rounded to bf16:
+// (x0 c - x1 s, x0 s + x1 c), the arithmetic of the standalone rotation kernel.
+__device__ __forceinline__ uint32_t rot_bf16x2(uint32_t w, float c, float s) {
+    const float x0 = bf16lo(w), x1 = bf16hi(w);
+    return pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+}
+
+// Rotates row `row` (0..127 of a 1024-byte aligned 128-byte-swizzled tile) by its position's
+// angles, table row `pos` (16 float4: (cos, sin) of pairs 2m and 2m + 1).
+__device__ __forceinline__ void rotate_row_sw(uint8_t* tile, int row, const float4* trow) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4* ptr = reinterpret_cast<uint4*>(tile + sw128_off(row, c));
+        uint4 w = *ptr;
+        const float4 t0 = __ldg(trow + 2 * c), t1 = __ldg(trow + 2 * c + 1);
+        w.x = rot_bf16x2(w.x, t0.x, t0.y);
+        w.y = rot_bf16x2(w.y, t0.z, t0.w);
+        w.z = rot_bf16x2(w.z, t1.x, t1.y);
+        w.w = rot_bf16x2(w.w, t1.z, t1.w);
+        *ptr = w;
+    }
+}
+
+// acc += c (q0 k0 + q1 k1) + s (q0 k1 - q1 k0) for one bf16 pair of q and of k: the pair's
+// share of (R q) . k with R the rotation by (c, s). Products of bf16 values are exact in fp32.
+__device__ __forceinline__ void rope_dot_pair(uint32_t q, uint32_t k, float c, float s, float& acc) {
+    asm("{\n\t.reg .b16 q0, q1, k0, k1;\n\t.reg .f32 a, b;\n\t"
+        "mov.b32 {q0, q1}, %1;\n\tmov.b32 {k0, k1}, %2;\n\t"
+        "fma.rn.f32.bf16 a, q1, k1, 0f00000000;\n\tfma.rn.f32.bf16 a, q0, k0, a;\n\t"
+        "fma.rn.f32.bf16 b, q1, k0, 0f00000000;\n\tneg.f32 b, b;\n\t"
+        "fma.rn.f32.bf16 b, q0, k1, b;\n\t"
+        "fma.rn.f32 %0, %3, a, %0;\n\tfma.rn.f32 %0, %4, b, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(q), "r"(k), "f"(c), "f"(s));
+}
+
+template <bool kFrac, bool kWide, bool kRope = false>
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
     static_assert(!(kFrac && kWide), "the fractional mode is for head size 64");
+    static_assert(!kRope || (!kFrac && !kWide), "the RoPE mode is the static head-size-64 path");
     using PL = Plan<kWide>;
     using L = Layout<kFrac>;
     constexpr uint32_t kOffTmemSlot = tmem_slot_off<kFrac>();
@@ -179,7 +229,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
     const ring::Ring rg{sbase, sbase + L::kOffBar, kSlots, 4, L::kSlot};  // 4 row warps
     auto bar = [&](uint32_t idx) { return sbase + L::kOffBar + 8u * idx; };
     const uint32_t B_S = bar(kBarS), B_P = bar(kBarP), B_O = bar(kBarO), B_T = bar(kBarT),
-                   B_L = bar(kBarL);
+                   B_L = bar(kBarL), B_R = bar(kBarR);
     auto slot_ptr = [&](uint32_t seq) { return smem + (rg.addr(seq) - sbase); };
 
     if (tid == 0) {
@@ -189,6 +239,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
         mbar_init(B_O, 1);
         mbar_init(B_T, 4);
         mbar_init(B_L, 1);
+        mbar_init(B_R, 4);
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -311,6 +362,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                     if (g > 0) mbar_wait(B_O, (gcount - 1) & 1, aborted, p.err);  // P of g-1 consumed
                     for (int j = 0; j < PL::kQItems; ++j) rg.wait_full(qseq + j, aborted, p.err);
                     for (int j = 0; j < nk; ++j) rg.wait_full(kseq + j, aborted, p.err);
+                    if constexpr (kRope) mbar_wait(B_R, gcount & 1, aborted, p.err);  // rotated in place
                     tc_fence_after();
                     for (int c = 0; c < nch; ++c) {
                         if constexpr (kWide) {
@@ -372,7 +424,9 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
 
             uint32_t qseq = seq;  // the last group's Q copy
             for (int g = 0; g + 1 < n_groups; ++g) qseq += pl.group_items(g);
+            uint32_t gseq = seq;  // the current group's first item (RoPE mode)
             seq += pl.band_items();
+            uint32_t qw[32 * PL::kQItems];  // the q row (head size 128: both halves)
 
             // ---- band: masked online softmax over the S groups. Only the 32-column chunks
             // that some row of this warp can reach are read (3 of 6 at W = 64).
@@ -386,6 +440,33 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                 const int32_t colB = min(nch * kChunk - 1, wrow + 31);
                 const int ccA = colA / 32;
                 const int n_need = colA <= colB ? colB / 32 - ccA + 1 : 0;
+                if constexpr (kRope) {
+                    // rotate the group's Q copy and K chunks in their slots before its S MMAs
+                    // (every row a thread touches is its own: no barrier among the row threads)
+                    rg.wait_full(gseq, aborted, p.err);
+                    for (int j = 0; j < pl.k_slots(g); ++j) rg.wait_full(gseq + 1 + j, aborted, p.err);
+                    uint8_t* qt = slot_ptr(gseq);
+                    if (g == n_groups - 1) {  // the unrotated q row, for the offsets
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(qt + sw128_off(r, c));
+                            qw[4 * c + 0] = w.x; qw[4 * c + 1] = w.y; qw[4 * c + 2] = w.z; qw[4 * c + 3] = w.w;
+                        }
+                    }
+                    if (i < T) rotate_row_sw(qt, r, p.rope + (int64_t)i * 16);
+                    for (int rr = r; rr < nch * kChunk; rr += kRows) {
+                        const int32_t j = kbase + rr;  // the key's position
+                        if (j < T) {
+                            const int c = rr / kChunk;
+                            uint8_t* kt = slot_ptr(gseq + 1 + c / 2) + (c & 1) * kChunkBytes;
+                            rotate_row_sw(kt, rr % kChunk, p.rope + (int64_t)j * 16);
+                        }
+                    }
+                    fence_proxy_async_smem();  // generic writes before the MMAs' reads
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B_R);
+                    gseq += pl.group_items(g);
+                }
                 mbar_wait(B_S, (gbase + g) & 1, aborted, p.err);
                 tc_fence_after();
                 __syncwarp();  // converged for the warp-collective TMEM accesses below
@@ -456,16 +537,17 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             // q row into registers, then the Q slot goes back to the producer (every S MMA
             // reading it has completed: B_S was waited for each group). Holding the slot through
             // the offsets would stall the in-order ring.
-            uint32_t qw[32 * PL::kQItems];  // head size 128: both halves
 #pragma unroll
             for (int qh = 0; qh < PL::kQItems; ++qh) {
-                rg.wait_full(qseq + qh, aborted, p.err);
-                const uint8_t* qrow = slot_ptr(qseq + qh);
+                if constexpr (!kRope) {  // (RoPE mode: read before the rotation)
+                    rg.wait_full(qseq + qh, aborted, p.err);
+                    const uint8_t* qrow = slot_ptr(qseq + qh);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
-                    qw[32 * qh + 4 * c + 0] = w.x; qw[32 * qh + 4 * c + 1] = w.y;
-                    qw[32 * qh + 4 * c + 2] = w.z; qw[32 * qh + 4 * c + 3] = w.w;
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(qrow + sw128_off(r, c));
+                        qw[32 * qh + 4 * c + 0] = w.x; qw[32 * qh + 4 * c + 1] = w.y;
+                        qw[32 * qh + 4 * c + 2] = w.z; qw[32 * qh + 4 * c + 3] = w.w;
+                    }
                 }
                 rg.release_warp(qseq + qh, lane);
             }
@@ -481,7 +563,25 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                 if constexpr (kFrac) wk = p.w[tl.layer][k];
                 const bool lerp = kFrac && wk != 0.f;
                 float s = 0.f;
-                {
+                if constexpr (kRope) {
+                    // (R_o q) . k_(i-o) from the unrotated rows: one angle per offset
+                    const float4* trow = p.rope + (int64_t)offs[k] * 16;
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    rg.wait_full(seq, aborted, p.err);
+                    const uint8_t* krow = slot_ptr(seq);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(krow + sw128_off(r, c));
+                        const float4 t0 = __ldg(trow + 2 * c), t1 = __ldg(trow + 2 * c + 1);
+                        rope_dot_pair(qw[4 * c + 0], w.x, t0.x, t0.y, a0);
+                        rope_dot_pair(qw[4 * c + 1], w.y, t0.z, t0.w, a1);
+                        rope_dot_pair(qw[4 * c + 2], w.z, t1.x, t1.y, a2);
+                        rope_dot_pair(qw[4 * c + 3], w.w, t1.z, t1.w, a3);
+                    }
+                    s = (a0 + a1) + (a2 + a3);
+                    rg.release_warp(seq, lane);
+                    ++seq;
+                } else {
                     // the row dot over the K item(s): head size 128 takes its two halves
                     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
@@ -619,10 +719,11 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
 
 namespace {
 
-template <bool kFrac, bool kWide>
+template <bool kFrac, bool kWide, bool kRope = false>
 fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                           const AttnShape& sh, const OffsetTables& t,
-                          const float (*w)[kMaxOffsets], const char* name, cudaStream_t st) {
+                          const float (*w)[kMaxOffsets], const char* name, cudaStream_t st,
+                          const float* rope = nullptr) {
     const int64_t slices = sh.slices_per_layer * sh.n_layers;
     const int32_t tiles = (sh.T + kRows - 1) / kRows;
     const int64_t halves = kWide ? 2 : 1;  // CTAs per tile
@@ -650,6 +751,7 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
             for (int e = 0; e < kMaxOffsets; ++e) P.w[l][e] = w[l][e];
     }
     P.lse = lse;
+    P.rope = reinterpret_cast<const float4*>(rope);
     P.slices_per_layer = (uint32_t)sh.slices_per_layer;
     P.group = (uint32_t)sh.group;
     P.slices_per_layer_kv = (uint32_t)(sh.slices_per_layer / sh.group);
@@ -666,7 +768,7 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
     static int n_sm[64] = {};
     if (dev < 0 || dev >= 64) return FIBATTN_ERR_UNSUPPORTED;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel<kFrac, kWide>,
+        e = cudaFuncSetAttribute(fwd_tc_kernel<kFrac, kWide, kRope>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc<kFrac>());
         if (e != cudaSuccess) return cuda_fail((int32_t)e, "cudaFuncSetAttribute (fwd)");
         e = cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
@@ -676,7 +778,7 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
     const int64_t grid = (int64_t)P.total_tiles < 2LL * n_sm[dev] ? (int64_t)P.total_tiles : 2LL * n_sm[dev];
     {
         KernelScope ks(name, st);
-        fwd_tc_kernel<kFrac, kWide><<<(unsigned)grid, kThreads, smem_alloc<kFrac>(), st>>>(P);
+        fwd_tc_kernel<kFrac, kWide, kRope><<<(unsigned)grid, kThreads, smem_alloc<kFrac>(), st>>>(P);
     }
     return launch_status(name);
 }
@@ -686,6 +788,13 @@ fibattn_status launch_fwd(const void* q, const void* k, const void* v, void* o, 
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st) {
     return launch_fwd<false, false>(q, k, v, o, lse, sh, t, nullptr, "fwd_tc_bf16", st);
+}
+
+fibattn_status launch_fwd_rope_tc_bf16(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, const AttnShape& sh, const OffsetTables& t,
+                                       const float* rope_table, cudaStream_t st) {
+    return launch_fwd<false, false, true>(q, k, v, o, lse, sh, t, nullptr, "fwd_rope_tc_bf16", st,
+                                          rope_table);
 }
 
 fibattn_status launch_fwd_tc128_bf16(const void* q, const void* k, const void* v, void* o,

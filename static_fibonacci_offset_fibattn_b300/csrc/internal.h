@@ -104,6 +104,9 @@ fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* 
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
 // The same forward at head size 128 (two CTAs per tile, one per half of the output columns).
+fibattn_status launch_fwd_rope_tc_bf16(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, const AttnShape& sh, const OffsetTables& t,
+                                       const float* rope_table, cudaStream_t st);
 fibattn_status launch_fwd_tc128_bf16(const void* q, const void* k, const void* v, void* o,
                                      float* lse, const AttnShape& sh, const OffsetTables& t,
                                      cudaStream_t st);

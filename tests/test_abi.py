@@ -259,6 +259,16 @@ def test_rope_entry_points_validate_before_launch():
                               None) == fa.INVALID_ARG
     assert L.fibattn_bwd_rope(*([ok] * 10), ctypes.c_uint64(1 << 40), 1, 4, 2, 8, 64, 1, 4, 0.0,
                               ctypes.byref(sc), 0, 1, None, 8, None) == fa.INVALID_ARG
+    # the fused form: a short table, bad head counts, then fp32 and head size 128 unsupported
+    fused = L.fibattn_fwd_rope_fused
+    assert fused(*([ok] * 5), 1, 4, 2, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 7,
+                 None) == fa.INVALID_ARG
+    assert fused(*([ok] * 5), 1, 4, 3, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 8,
+                 None) == fa.INVALID_ARG
+    assert fused(*([ok] * 5), 1, 4, 2, 8, 64, 0, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 8,
+                 None) == fa.UNSUPPORTED
+    assert fused(*([ok] * 5), 1, 4, 2, 8, 128, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 8,
+                 None) == fa.UNSUPPORTED
 
 
 def test_debug_wait_timeout_validates_before_launch():

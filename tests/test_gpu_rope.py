@@ -99,3 +99,70 @@ def test_rope_training_step_sampled():
         assert max_abs(f64(o[l, b, h])[None], ro) <= TOL["bf16"], l
         for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
             assert_grad(n, f64(got[l, b, h])[None], ref, "bf16", l)
+
+
+# ------------------------------------------------------------------ RoPE inside the forward
+
+FUSED = [
+    # (Lc, B, H, Hkv, T, W)
+    (1, 1, 2, 2, 1, 4),
+    (1, 1, 2, 1, 300, 16),
+    (2, 1, 4, 2, 1030, 64),     # ragged last tile, grouped heads, two layers
+    (1, 2, 2, 2, 257, 8),
+    (1, 1, 2, 2, 700, 200),     # several band groups per tile
+    (1, 1, 1, 1, 2049, 64),
+]
+
+
+@pytest.mark.parametrize("case", FUSED)
+def test_fused_rope_forward_matches_oracle(case):
+    # the oracle rotates in fp64 and attends over the rotated tensors (fwd_rope)
+    Lc, B, H, Hkv, T, W = case
+    kv = {n: (Lc, B, Hkv, T, 64) for n in ("k", "v")}
+    inp = fi.draw((Lc, B, H, T, 64), seed=300 + T, scale=0.5, dtype="bf16", shapes=kv)
+    dev = to_dev(inp)
+    sc = lib_schedule(SCHED)
+    table = fa.rope_table(T)
+    o, lse = fa.fwd_rope_fused(dev["q"], dev["k"], dev["v"], W, sc, table, layer0=5)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    tabs = [oracle_table(SCHED, 5 + l, W, T) for l in range(Lc)]
+    ro, rl = oracle.fwd_rope(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), W, tabs)
+    assert max_abs(f64(o), ro) <= TOL["bf16"]
+    assert max_abs(f64(lse), rl) <= LSE_TOL["bf16"]
+    # and the unfused path (rotated copies, then the attention) to rounding
+    o2, l2, _ = fa.fwd_rope(dev["q"], dev["k"], dev["v"], W, sc, table, layer0=5)
+    assert max_abs(f64(o), f64(o2)) <= TOL["bf16"]
+    assert max_abs(f64(lse), f64(l2)) <= LSE_TOL["bf16"]
+
+
+def test_fused_rope_forward_training_shape_sampled():
+    # the 16-layer training-step shape with RoPE, forward only, in one call
+    spec = fi.WORKLOADS["c5r"]
+    inp = fi.workload_inputs("c5r", names=("q", "k", "v"))
+    dev = to_dev(inp)
+    sc = lib_schedule(spec["sched"])
+    W, T = spec["W"], spec["T"]
+    table = fa.rope_table(T, spec["rope_base"])
+    o, lse = fa.fwd_rope_fused(dev["q"], dev["k"], dev["v"], W, sc, table)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    for l in (0, 9, 15):
+        tab = oracle_table(spec["sched"], l, W, T)
+        b, h = (5 * l) % spec["B"], (l + 3) % spec["H"]
+        g = lambda n: f64(inp[n][l, b, h])[None]
+        ro, rl = oracle.fwd_rope(g("q"), g("k"), g("v"), W, tab, spec["rope_base"])
+        assert max_abs(f64(o[l, b, h])[None], ro) <= TOL["bf16"], l
+        assert max_abs(f64(lse[l, b, h])[None], rl) <= LSE_TOL["bf16"], l
+
+
+def test_fused_rope_forward_deterministic_and_in_place_safe():
+    inp = to_dev(fi.draw((2, 2, 2, 1024, 64), seed=17, scale=0.5, dtype="bf16"))
+    sc = lib_schedule(SCHED)
+    table = fa.rope_table(1024)
+    q0, k0 = inp["q"].clone(), inp["k"].clone()
+    a = fa.fwd_rope_fused(inp["q"], inp["k"], inp["v"], 64, sc, table)
+    b = fa.fwd_rope_fused(inp["q"], inp["k"], inp["v"], 64, sc, table)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    # the inputs are read, never written (the rotation happens in shared memory)
+    assert torch.equal(inp["q"], q0) and torch.equal(inp["k"], k0)
