@@ -189,6 +189,28 @@ def test_fwd_dense_causal_matches_sdpa():
     assert max_abs(f64(o[0]), f64(ref)) <= TOL["bf16"]
 
 
+def test_fwd_dense_causal_at_4x_length():
+    # the dense causal context at the 4x-length shape (one layer of those inputs, W = T = 4096):
+    # no offset survives, so the forward is dense causal attention; against torch's SDPA on the
+    # same tensors and, on two slices, the oracle
+    spec = fi.WORKLOADS["c4"]
+    inp = fi.workload_inputs("c4", layers=[0])
+    dev = to_dev(inp)
+    T = spec["T"]
+    sc = lib_schedule(spec["sched"])
+    assert fa.offsets(sc, 0, T, T) == []
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], T, sc)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        dev["q"][0].float(), dev["k"][0].float(), dev["v"][0].float(), is_causal=True)
+    assert max_abs(f64(o[0]), f64(ref)) <= TOL["bf16"]
+    picks = [(0, 0, 0), (0, 1, 7)]
+    for (l, b, h), (ro, rl) in oracle_fwd_slices(inp, spec["sched"], T, 0, picks).items():
+        assert max_abs(f64(o[l, b, h]), ro) <= TOL["bf16"]
+        assert max_abs(f64(lse[l, b, h]), rl) <= LSE_TOL["bf16"]
+
+
 def test_fwd_layer_batched_equals_per_layer_calls():
     spec = fi.WORKLOADS["c3"]
     inp = to_dev(fi.workload_inputs("c3", layers=range(4), B=2, H=2))
