@@ -79,3 +79,35 @@ def test_every_timed_kernel_has_an_accounting_entry():
     for kernel, src in bench.KERNEL_SRC.items():
         assert os.path.exists(os.path.join(CSRC, src)), (kernel, src)
     assert set(bench.KERNEL_SRC) <= set(bench.ALGO_BYTES)
+
+
+def test_kernel_roofline_record():
+    # one launch covers at most 16 layers; achieved = algorithmic bytes per launch / mean time
+    c5 = fi.WORKLOADS["c5"]
+    per_kernel = {"bwd_dkdv_tc": (2 * 0.369, 2)}  # two launches of 369 us
+    r = bench.kernel_roofline("bwd_dkdv_tc", per_kernel, c5, "c5", 6508.2, "measured")
+    assert r["algorithmic_bytes_per_launch"] == 809_500_672
+    assert r["avg_launch_us"] == pytest.approx(369.0)
+    assert r["achieved"] == pytest.approx(809_500_672 / 369e-6 / 1e9, rel=1e-3)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6508.2, abs=1e-4)
+    # a 32-layer call is two launches of 16 layers each: bytes per launch halve
+    c5_32 = dict(c5, Lc=32)
+    r32 = bench.kernel_roofline("bwd_dkdv_tc", per_kernel, c5_32, "c5", 6508.2, "measured")
+    assert r32["algorithmic_bytes_per_launch"] == 809_500_672
+
+
+def test_dense_context_flops():
+    # causal attention over T keys: query i attends i + 1 keys, 4 d flops per (query, key)
+    # (q.k and p.v), so 4 d T (T + 1) / 2 per (b, h) slice; at the 4x-length shape, B2 H8:
+    c4 = fi.WORKLOADS["c4"]
+    T, d = c4["T"], c4["d"]
+    brute = sum(4 * d * (i + 1) for i in range(T)) * c4["B"] * c4["H"]
+    assert brute == 4 * d * T * (T + 1) // 2 * c4["B"] * c4["H"]
+    assert round(brute / 1e9, 2) == 34.37
+
+
+def test_fused_rope_forward_is_accounted_like_the_forward():
+    # the table rows it reads are L2-resident reuse, not compulsory traffic
+    c3r = fi.WORKLOADS["c3r"]
+    assert bench.algo_bytes("fwd_rope_tc_bf16", c3r) == bench.algo_bytes("fwd_tc_bf16", c3r) == 516
+    assert c3r.get("rope_fused") and "rope_base" in c3r
