@@ -62,6 +62,9 @@ ALGO_BYTES = {
     "bwd_dkdv_simt": 4 * 256 + 8 + 2 * 256,     # fp32: q, k, v, dO, lse, D in; dk, dv out
     "bwd_dq_tc": 5 * 128 + 4 + 128,             # q, k, v, o, dO, lse in; dq out
     "bwd_dkdv_tc": 4 * 128 + 4 + 2 * 128,       # q, k, v, dO, lse in; dk, dv out
+    "bwd_prep": 2 * 128 + 4 + 8,                # one-pass backward's pre-pass: o, dO, lse in;
+                                                # D, lse log2(e) out
+    "bwd_fused_tc": 4 * 128 + 8 + 3 * 128,      # q, k, v, dO, D, lse log2(e) in; dq, dk, dv out
     "bwd_dq_tc128": 5 * 256 + 4 + 256,          # head size 128: rows of 256 B
     "bwd_dkdv_tc128": 4 * 256 + 4 + 2 * 256,
     "bwd_dq_frac_tc": 5 * 128 + 4 + 128 + 4,    # as bwd_dq_tc, plus the dalpha partial out
@@ -74,7 +77,7 @@ ALGO_BYTES = {
 }
 # Rows per query token of each kernel that are k/v-shaped (k, v in; dk, dv out).
 KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_tc128_bf16": 2, "bwd_dq_tc": 2,
-           "bwd_dkdv_tc": 4, "bwd_dq_simt": 2, "bwd_dkdv_simt": 4, "bwd_dq_tc128": 2,
+           "bwd_dkdv_tc": 4, "bwd_fused_tc": 4, "bwd_dq_simt": 2, "bwd_dkdv_simt": 4, "bwd_dq_tc128": 2,
            "bwd_dkdv_tc128": 4}
 # Kernel -> source file, to tell whether a committed ncu traffic figure is still current.
 KERNEL_SRC = {
@@ -86,7 +89,7 @@ KERNEL_SRC = {
     "rope_bf16": "rope.cu", "rope_f32": "rope.cu",
     "bwd_delta_simt": "simt.cu", "bwd_dq_simt": "simt.cu", "bwd_dkdv_simt": "simt.cu",
     "bwd_dq_tc": "bwd_tc.cu", "bwd_dkdv_tc": "bwd_tc.cu", "bwd_dq_tc128": "bwd_tc.cu",
-    "bwd_dkdv_tc128": "bwd_tc.cu",
+    "bwd_dkdv_tc128": "bwd_tc.cu", "bwd_prep": "bwd_fused.cu", "bwd_fused_tc": "bwd_fused.cu",
 }
 
 
@@ -108,7 +111,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c5",
                     choices=["c5", "c4", "c2", "c1", "c3", "c3p", "c3f", "c5f", "c5g", "c5r",
-                             "c3r", "c3w", "c5w"])
+                             "c3r", "c3w", "c5w", "c5o"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -403,6 +406,30 @@ def dense_context_record(fa, L, dev, stream, flush, a, clk):
             "max_abs_diff_vs_sdpa": err, "calls": steps}
 
 
+def one_pass_backward_record(fa, L, d_in, spec, sched, o, lse, dq, dk, dv, dev, stream, flush,
+                             a, clk, hbm, peak_kind, two_kernel_ms):
+    """The same training step with the one-pass backward (fibattn_bwd_fused: a pre-pass for D
+    and lse log2(e), then one kernel whose thread block per tile writes dq, dk and dv), timed
+    like the main step; its outputs equal the two-kernel backward's bit for bit."""
+    ws = torch.empty(fa.bwd_fused_workspace_size(d_in["q"]), dtype=torch.uint8, device=dev)
+
+    def fstep():
+        fa.fwd(d_in["q"], d_in["k"], d_in["v"], spec["W"], sched, out=o, lse=lse)
+        fa.bwd_fused(d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dO"], spec["W"], sched,
+                     dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    ms, pk = timed_calls(fstep, a.steps, a.warmup, flush, stream, dev, L, clk, "one_pass")
+    fa.poll_device_error(dev)
+    kern = {k: {"avg_us": round(v[0] / v[1] * 1e3, 2),
+                "frac": kernel_roofline(k, pk, spec, "c5o", hbm, peak_kind)["frac"]}
+            for k, v in pk.items()}
+    return {"workload": "c5o: the c5 step with the one-pass backward",
+            "ms_per_step": round(ms, 4), "value": round(tokens(spec) / (ms / 1e3), 1),
+            "unit": UNIT, "kernels": kern,
+            "roofline": kernel_roofline("bwd_fused_tc", pk, spec, "c5o", hbm, peak_kind),
+            "over_two_kernel_step": round(ms / two_kernel_ms, 3), "steps": a.steps}
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(a, spec, world, rank, local):
@@ -414,6 +441,7 @@ def run_ours(a, spec, world, rank, local):
     frac = "alphas" in spec
     use_rope = "rope_base" in spec
     fused_rope = spec.get("rope_fused", False)
+    bwd_fused = spec.get("bwd_fused", False)
     sched = None if frac else fa.Schedule(**spec["sched"])
     alphas = fi.frac_alphas(spec) if frac else None
     inp = fi.workload_inputs(a.workload)
@@ -426,6 +454,7 @@ def run_ours(a, spec, world, rank, local):
         dq = torch.empty_like(d_in["q"])
         dk, dv = torch.empty_like(d_in["k"]), torch.empty_like(d_in["v"])
         need = (fa.bwd_frac_workspace_size(d_in["q"], W, alphas, spec["base"]) if frac
+                else fa.bwd_fused_workspace_size(d_in["q"]) if bwd_fused
                 else fa.bwd_workspace_size(d_in["q"], W, sched))
         ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
         dalpha = torch.empty(spec["Lc"], dtype=torch.float32, device=dev)
@@ -454,8 +483,9 @@ def run_ours(a, spec, world, rank, local):
             return
         fa.fwd(x["q"], x["k"], x["v"], W, sched, out=o, lse=lse)
         if train:
-            fa.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched, dq=dq, dk=dk, dv=dv,
-                   workspace=ws)
+            bwd = fa.bwd_fused if bwd_fused else fa.bwd
+            bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], W, sched, dq=dq, dk=dk, dv=dv,
+                workspace=ws)
 
     clk = Clocks(clock_index(local)).start()
     for _ in range(a.warmup):
@@ -529,7 +559,7 @@ def run_ours(a, spec, world, rank, local):
                        "ms_per_step": round(cms, 4),
                        "kernels_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in cpk.items()},
                        "fused_over_unfused": round(ms_per_step / cms, 3)}
-    elif frac or use_rope:
+    elif frac or use_rope or bwd_fused:
         cname = "c5" if train else "c3"
         cspec = fi.WORKLOADS[cname]
         csched = fa.Schedule(**cspec["sched"])
@@ -569,6 +599,10 @@ def run_ours(a, spec, world, rank, local):
         extras["c4_fwd"] = extrapolation_forward_record(fa, L, dev, stream, flush, a, clk, hbm,
                                                         peak_kind)
         extras["dense_context_c4"] = dense_context_record(fa, L, dev, stream, flush, a, clk)
+        if a.workload == "c5":
+            extras["one_pass_bwd"] = one_pass_backward_record(fa, L, d_in, spec, sched, o, lse,
+                                                              dq, dk, dv, dev, stream, flush, a,
+                                                              clk, hbm, peak_kind, ms_per_step)
     clk.stop()
 
     out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -649,8 +683,9 @@ def run_e2e(fa, a, spec, inp, sched, dev, stream, world, alphas=None, table=None
         else:
             fa.fwd(x["q"], x["k"], x["v"], W, sched, out=r["o"], lse=r["lse"])
             if train:
-                fa.bwd(x["q"], x["k"], x["v"], r["o"], r["lse"], x["dO"], W, sched, dq=r["dq"],
-                       dk=r["dk"], dv=r["dv"], workspace=ws)
+                bwd = fa.bwd_fused if spec.get("bwd_fused", False) else fa.bwd
+                bwd(x["q"], x["k"], x["v"], r["o"], r["lse"], x["dO"], W, sched, dq=r["dq"],
+                    dk=r["dk"], dv=r["dv"], workspace=ws)
 
     def step(i):
         b = i % 2

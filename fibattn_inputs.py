@@ -80,6 +80,13 @@ WORKLOADS = {
                W=64, seed=4, scale=0.125, names=("q", "k", "v", "dO"), passes=("fwd", "bwd"),
                sched=dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
                           n_layers=16, coprime_c=5)),
+    "c5o": dict(desc="training step fwd+bwd with the one-pass backward (a thread block per tile "
+                     "owns dq of its queries and dk, dv of its keys), 16 layers, coprime (5l mod 16) "
+                     "of the linear stagger 0.5->2.0, bf16", dtype="bf16", Lc=16, B=8, H=8, T=1024,
+                d=64, W=64, seed=4, scale=0.125, names=("q", "k", "v", "dO"),
+                passes=("fwd", "bwd"), bwd_fused=True,
+                sched=dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1),
+                           n_layers=16, coprime_c=5)),
     "c5g": dict(desc="training step fwd+bwd, 16 layers, grouped-query (8 query heads sharing 2 "
                      "kv heads), coprime (5l mod 16) of the linear stagger 0.5->2.0, bf16",
                 dtype="bf16", Lc=16, B=8, H=8, Hkv=2, T=1024, d=64, W=64, seed=4, scale=0.125,

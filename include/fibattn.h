@@ -269,6 +269,29 @@ FIBATTN_API fibattn_status fibattn_bwd(const void* q, const void* k, const void*
                            void* cuda_stream);
 
 /*
+ * The same backward in one pass over the tiles: a thread block per 128-row tile of a
+ * (layer, batch, head) slice writes both dq of the tile's queries and dk, dv of its keys.
+ * The key side forms each diagonal pair (key j, query j + o) again instead of reading it
+ * from a workspace, so the only workspace is D and lse * log2(e) (written by a pre-pass).
+ *   Arguments, layouts and results as fibattn_bwd; the outputs equal fibattn_bwd's bit
+ *   for bit (each P and dS is formed from the same operands in the same order, and every
+ *   sum is taken in the same order). No atomics.
+ *   workspace : 256-byte aligned, at least 2 x 256-aligned [Lc][B][H][T_pad] float32
+ *               (D, then lse * log2(e); T_pad = T rounded up to 4);
+ *               fibattn_bwd_workspace_size() bytes always suffice. Contents on entry do
+ *               not matter (the pre-pass writes every row, pad rows as 0).
+ * Errors as fibattn_bwd; UNSUPPORTED unless dtype is FIBATTN_BF16 and d is 64.
+ */
+FIBATTN_API fibattn_status fibattn_bwd_fused(const void* q, const void* k, const void* v,
+                                             const void* o, const float* lse, const void* dO,
+                                             void* dq, void* dk, void* dv, void* workspace,
+                                             uint64_t workspace_bytes, int32_t B, int32_t H,
+                                             int32_t T, int32_t d, int32_t dtype, int32_t W,
+                                             float scale, const fibattn_schedule* sched,
+                                             int32_t layer0, int32_t n_layers_call,
+                                             void* cuda_stream);
+
+/*
  * fibattn_bwd for callers that cannot allocate device memory. The paper has no
  * counterpart: this is a deployment variant of the backward above, identical in
  * arguments, results and errors except that no workspace is passed.

@@ -25,7 +25,8 @@ __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd"
            "FibSparseAttention", "MAX_OFFSETS", "bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
            "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac", "bwd_frac",
            "bwd_frac_workspace_size", "FibFracAttention", "rope_table", "rope", "fwd_rope",
-           "bwd_rope", "fwd_rope_fused", "debug_wait_timeout"]
+           "bwd_rope", "fwd_rope_fused", "bwd_fused", "bwd_fused_workspace_size",
+           "debug_wait_timeout"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
@@ -119,6 +120,8 @@ def lib():
                                                  ctypes.POINTER(u64)]
         L.fibattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32, i32,
                                   i32, i32, f32, sp, i32, i32, vp]
+        L.fibattn_bwd_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
+                                        i32, i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_debug_wait_timeout.argtypes = [i32, vp]
         L.fibattn_debug_wait_timeout.restype = i32
         L.fibattn_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
@@ -381,6 +384,39 @@ def bwd(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
                                _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0,
                                Lc, _stream(q))
     _check(st, "fibattn_bwd_gqa")
+    return dq, dk, dv
+
+
+def bwd_fused_workspace_size(q: torch.Tensor) -> int:
+    """Bytes of device workspace fibattn_bwd_fused needs for tensors shaped like q: D and
+    lse * log2(e), each [Lc][B][H][T_pad] float32 (T_pad = T rounded up to 4), 256-aligned."""
+    Lc, B, H, T, d = _shape(q)
+    rows = Lc * B * H * ((T + 3) // 4 * 4)
+    return 2 * ((rows * 4 + 255) // 256 * 256)
+
+
+def bwd_fused(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
+              scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None):
+    """The one-pass backward (fibattn_bwd_fused): one thread block per 128-row tile writes
+    dq of its queries and dk, dv of its keys. bf16, head size 64, one kv head per query head.
+    Returns (dq, dk, dv), equal to bwd()'s bit for bit. workspace: optional uint8 device
+    tensor of at least bwd_fused_workspace_size() bytes."""
+    Lc, B, H, T, d = _shape(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_tensors(q, k, v, o, dO, dq, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(bwd_fused_workspace_size(q), dtype=torch.uint8, device=q.device)
+    if workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on q's device")
+    s = sched.to_c()
+    st = lib().fibattn_bwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), B, H, T, d,
+                                 _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s),
+                                 layer0, Lc, _stream(q))
+    _check(st, "fibattn_bwd_fused")
     return dq, dk, dv
 
 

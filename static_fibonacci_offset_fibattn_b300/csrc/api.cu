@@ -442,6 +442,47 @@ fibattn_status fibattn_bwd(const void* q, const void* k, const void* v, const vo
     return fibattn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, H, H,
                            T, d, dtype, W, scale, sched, layer0, n_layers_call, cuda_stream);
 }
+fibattn_status fibattn_bwd_fused(const void* q, const void* k, const void* v, const void* o,
+                                 const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                 void* workspace, uint64_t workspace_bytes, int32_t B, int32_t H,
+                                 int32_t T, int32_t d, int32_t dtype, int32_t W, float scale,
+                                 const fibattn_schedule* sched, int32_t layer0,
+                                 int32_t n_layers_call, void* cuda_stream) {
+    const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return FIBATTN_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FIBATTN_ERR_INVALID_ARG;
+    fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
+    if (st != FIBATTN_OK) return st;
+    if (dtype != FIBATTN_BF16 || d != 64) return FIBATTN_ERR_UNSUPPORTED;
+    // D and lse * log2(e) only: the layout of the two-kernel backward without its pairs
+    const BwdWorkspace ws = workspace_layout(B, H, T, dtype, n_layers_call, 0, false);
+    if (workspace_bytes < ws.total) return FIBATTN_ERR_INVALID_ARG;
+    float* delta = static_cast<float*>(workspace);
+    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2_offset);
+    const int64_t per_layer_pad = (int64_t)B * H * ws.T_pad;
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    const int64_t per_layer = (int64_t)B * H * T;
+    const size_t es = elt_size(dtype);
+    for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
+        const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
+        OffsetTables t;
+        st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
+        if (st != FIBATTN_OK) return st;
+        AttnShape sh{(int64_t)B * H, T, W, scale, n, 1, d};
+        const size_t off = (size_t)c * per_layer * d * es;
+        const size_t poff = (size_t)c * per_layer_pad;
+        st = launch_bwd_fused_tc_bf16((const char*)q + off, (const char*)k + off,
+                                      (const char*)v + off, (const char*)o + off,
+                                      lse + (size_t)c * per_layer, (const char*)dO + off,
+                                      (char*)dq + off, (char*)dk + off, (char*)dv + off,
+                                      delta + poff, lse2 + poff, sh, t, as_stream(cuda_stream));
+        if (st != FIBATTN_OK) return st;
+    }
+    return FIBATTN_OK;
+}
+
 fibattn_status fibattn_bwd_frac_workspace_size(int32_t B, int32_t H, int32_t T, int32_t d,
                                                int32_t dtype, int32_t W, int32_t base,
                                                int64_t base_max, const float* alphas,

@@ -157,4 +157,13 @@ fibattn_status launch_bwd_tc_bf16(const void* q, const void* k, const void* v, c
                                   float* delta, float* lse2, uint32_t* pds, int32_t n_max,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
 
+// One-pass backward (bf16, head size 64, one kv head per query head): a pre-pass writes D and
+// lse log2(e) into delta / lse2 ([slices][T_pad], T_pad = T rounded up to 4), then one tensor-core
+// kernel whose thread block per 128-row tile writes dq of the tile's queries and dk, dv of its
+// keys. UNSUPPORTED for other head sizes or grouped kv heads.
+fibattn_status launch_bwd_fused_tc_bf16(const void* q, const void* k, const void* v,
+                                        const void* o, const float* lse, const void* dO, void* dq,
+                                        void* dk, void* dv, float* delta, float* lse2,
+                                        const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
+
 }  // namespace fibattn

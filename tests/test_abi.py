@@ -275,3 +275,35 @@ def test_debug_wait_timeout_validates_before_launch():
     L = fa.lib()
     for bad in (0, -5, 10001):
         assert L.fibattn_debug_wait_timeout(bad, None) == fa.INVALID_ARG
+
+
+def test_bwd_fused_validates_before_launch():
+    # null or misaligned pointers, a misaligned or short workspace: INVALID_ARG; fp32, head
+    # size 128 or a bad head size: UNSUPPORTED; all decided on the host before any launch
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    ok = ctypes.c_void_p(256)
+    big = ctypes.c_uint64(1 << 40)
+    args = [ok] * 10
+    tail = (1, 1, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1, None)
+    for bad in range(10):
+        a = list(args)
+        a[bad] = ctypes.c_void_p(0)
+        assert L.fibattn_bwd_fused(*a, big, *tail) == fa.INVALID_ARG
+    a = list(args)
+    a[0] = ctypes.c_void_p(256 + 8)
+    assert L.fibattn_bwd_fused(*a, big, *tail) == fa.INVALID_ARG
+    a = list(args)
+    a[9] = ctypes.c_void_p(256 + 16)
+    assert L.fibattn_bwd_fused(*a, big, *tail) == fa.INVALID_ARG
+    # B1 H1 T8: two 256-aligned arrays of 8 floats = 512 bytes
+    assert L.fibattn_bwd_fused(*args, ctypes.c_uint64(511), *tail) == fa.INVALID_ARG
+    for d, dtype in ((64, 0), (128, 1), (32, 1)):
+        assert L.fibattn_bwd_fused(*args, big, 1, 1, 8, d, dtype, 4, 0.0, ctypes.byref(sc), 0, 1,
+                                   None) == fa.UNSUPPORTED
+
+
+def test_bwd_fused_workspace_size_is_d_and_lse_only():
+    q = torch.empty(16, 8, 8, 1023, 64, dtype=torch.bfloat16, device="meta")
+    rows = 16 * 8 * 8 * 1024
+    assert fa.bwd_fused_workspace_size(q) == 2 * ((rows * 4 + 255) // 256 * 256)

@@ -111,3 +111,16 @@ def test_fused_rope_forward_is_accounted_like_the_forward():
     c3r = fi.WORKLOADS["c3r"]
     assert bench.algo_bytes("fwd_rope_tc_bf16", c3r) == bench.algo_bytes("fwd_tc_bf16", c3r) == 516
     assert c3r.get("rope_fused") and "rope_base" in c3r
+
+
+def test_one_pass_backward_bytes_per_token():
+    # the one-pass backward reads q, k, v, dO, D and lse log2(e) once and writes dq, dk, dv
+    # once; its pre-pass reads o, dO and lse and writes D and lse log2(e): together they count
+    # the D/lse round trip once more than the two-kernel query owner, which forms D itself
+    c5o = fi.WORKLOADS["c5o"]
+    assert bench.algo_bytes("bwd_fused_tc", c5o) == 4 * ROW_BF16_64 + 2 * 4 + 3 * ROW_BF16_64
+    assert bench.algo_bytes("bwd_prep", c5o) == 2 * ROW_BF16_64 + LSE + 2 * 4
+    assert bench.KERNEL_SRC["bwd_fused_tc"] == bench.KERNEL_SRC["bwd_prep"] == "bwd_fused.cu"
+    c5 = fi.WORKLOADS["c5"]
+    assert {k: v for k, v in c5o.items() if k not in ("desc", "bwd_fused")} == \
+        {k: v for k, v in c5.items() if k != "desc"}
