@@ -55,6 +55,7 @@ ALGO_BYTES = {
     "fwd_frac_tc_bf16": 3 * 128 + 128 + 4,     # the same for fractional offsets
     "fwd_rope_tc_bf16": 3 * 128 + 128 + 4,     # the same with RoPE inside (table rows in L2)
     "fwd_tc128_bf16": 3 * 256 + 256 + 4,       # head size 128: rows of 256 B
+    "fwd_dense_tc_bf16": 3 * 128 + 128 + 4,    # dense causal (W >= T): q, k, v in; o, lse out
     "fwd_frac_simt_f32": 3 * 256 + 256 + 4,
     "fwd_simt_f32": 3 * 256 + 256 + 4,
     "bwd_delta_simt": 2 * 256 + 4,              # fp32: o, dO in; D out
@@ -83,7 +84,7 @@ KV_ROWS = {"fwd_tc_bf16": 2, "fwd_simt_f32": 2, "fwd_tc128_bf16": 2, "bwd_dq_tc"
 KERNEL_SRC = {
     "fwd_tc_bf16": "fwd_tc.cu", "fwd_simt_f32": "simt.cu",
     "fwd_frac_tc_bf16": "fwd_tc.cu", "fwd_frac_simt_f32": "simt.cu", "fwd_tc128_bf16": "fwd_tc.cu",
-    "fwd_rope_tc_bf16": "fwd_tc.cu",
+    "fwd_rope_tc_bf16": "fwd_tc.cu", "fwd_dense_tc_bf16": "dense_tc.cu",
     "bwd_dq_frac_tc": "bwd_tc.cu", "bwd_dkdv_frac_tc": "bwd_tc.cu",
     "bwd_dq_frac_simt": "simt.cu", "bwd_dkdv_frac_simt": "simt.cu", "dalpha_reduce": "simt.cu",
     "rope_bf16": "rope.cu", "rope_f32": "rope.cu",

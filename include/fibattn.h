@@ -120,8 +120,9 @@ FIBATTN_API fibattn_status fibattn_offsets_device(const fibattn_schedule* sched,
  *   lse     : [Lc][B][H][T] float32 device, written: log sum_j exp(scale * q_i.k_j).
  *   scale   : <= 0 selects 1/sqrt(d).
  *   W >= 1 (W >= T gives dense causal attention). bf16 runs on the tcgen05 tensor-core
- *   kernel (d = 128: two CTAs per 128-query tile, one per half of the output columns); f32 on
- *   the SIMT fp32 kernel.
+ *   kernel (d = 128: two CTAs per 128-query tile, one per half of the output columns; d = 64
+ *   with W >= T: a dense causal kernel over 128 x 128 score blocks); f32 on the SIMT fp32
+ *   kernel.
  * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (a layer table above FIBATTN_MAX_OFFSETS),
  * CUDA (launch failure).
  */

@@ -208,6 +208,8 @@ fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void
         if (dtype == FIBATTN_F32)
             st = launch_fwd_simt_f32((const float*)qc, (const float*)kc, (const float*)vc,
                                      (float*)oc, lc, sh, t, as_stream(cuda_stream));
+        else if (d == 64 && W >= T)  // every earlier key: dense causal attention
+            st = launch_fwd_dense_tc_bf16(qc, kc, vc, oc, lc, sh, as_stream(cuda_stream));
         else if (d == 64)
             st = launch_fwd_tc_bf16(qc, kc, vc, oc, lc, sh, t, as_stream(cuda_stream));
         else

@@ -103,6 +103,10 @@ fibattn_status launch_fwd_simt_f32(const float* q, const float* k, const float* 
                                    cudaStream_t st);
 fibattn_status launch_fwd_tc_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   const AttnShape& sh, const OffsetTables& t, cudaStream_t st);
+// Dense causal forward (bf16, head size 64): the W >= T case, where no offset survives and
+// every earlier key is attended; 128 x 128 score blocks on the tensor cores.
+fibattn_status launch_fwd_dense_tc_bf16(const void* q, const void* k, const void* v, void* o,
+                                        float* lse, const AttnShape& sh, cudaStream_t st);
 // The same forward at head size 128 (two CTAs per tile, one per half of the output columns).
 fibattn_status launch_fwd_rope_tc_bf16(const void* q, const void* k, const void* v, void* o,
                                        float* lse, const AttnShape& sh, const OffsetTables& t,
