@@ -15,10 +15,12 @@
 //               j = 0 .. t0/128 through a five-slot ring.
 // Per key block j (keys [128j, 128j+128)):
 //   S = Q K_j^T (M=128, N=128, K=64) into TMEM columns [0, 128);
-//   each row thread takes the row max over its allowed keys (all of them, or k <= i in the
-//   diagonal block) and raises its running max m only when the block's max exceeds it by more
-//   than 2^8 (then O in TMEM and the sum l are rescaled once PV_{j-1} has completed); the
-//   exponentials 2^(s - m) <= 2^8 go back over S as bf16;
+//   each row thread reads its score row into registers (the columns are then free, and the
+//   tensor core forms S_{j+1} while the row threads work on block j), takes the row max over
+//   its allowed keys (all of them, or k <= i in the diagonal block) and raises its running
+//   max m only when the block's max exceeds it by more than 2^8 (then O and the sum l are
+//   rescaled, once PV_{j-1} has completed); the exponentials 2^(s - m) <= 2^8 go to TMEM
+//   columns [192, 256) as bf16;
 //   O += P V_j (A = P from TMEM, B = V_j MN-major) into TMEM columns [128, 192).
 // Epilogue: O / l staged in the Q buffer (every S MMA that read it has completed), TMA store;
 // lse = (m + log2 l) ln 2.
@@ -45,12 +47,14 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTileBytes = kRows * 128;     // 16 KB
 constexpr uint32_t kBoxBytes = kBox * 128;       // 8 KB
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColO = 128;       // S [0, 128), O [128, 192)
+constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;  // S [0, 128), O [128, 192), P [192, 256)
 constexpr uint32_t kSlots = 5;
 constexpr float kRescale = 8.f;                  // log2 of the largest unnormalised P
 
-// barriers: FULL[kSlots], EMPTY[kSlots], Q loaded, S ready, P written (4 warps), PV done
-constexpr uint32_t kBarQ = 2 * kSlots, kBarS = kBarQ + 1, kBarP = kBarQ + 2, kBarO = kBarQ + 3;
+// barriers: FULL[kSlots], EMPTY[kSlots], Q loaded, S ready, S read out (4 warps), P written
+// (4 warps), PV done
+constexpr uint32_t kBarQ = 2 * kSlots, kBarS = kBarQ + 1, kBarF = kBarQ + 2, kBarP = kBarQ + 3,
+                   kBarO = kBarQ + 4;
 constexpr uint32_t kNumBars = kBarO + 1;
 // shared memory: Q (later the output staging), the ring, the barriers, the TMEM address word
 constexpr uint32_t kOffQ = 0, kOffRing = kTileBytes, kOffBar = kOffRing + kSlots * kTileBytes;
@@ -87,8 +91,8 @@ __device__ __forceinline__ float row_max(const uint32_t (&v)[4][32], int r) {
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
 
-// p = 2^(s sl2 - m) of a row (0 for masked columns), written over the scores in TMEM as bf16
-// pairs (32-column chunk cc to columns 16cc ..); returns the sum of the p (four partial sums).
+// p = 2^(s sl2 - m) of a row (0 for masked columns), written to TMEM at taddr as bf16 pairs
+// (32-column chunk cc to columns 16cc ..); returns the sum of the p (four partial sums).
 template <bool kDiag>
 __device__ __forceinline__ float row_exp(const uint32_t (&v)[4][32], int r, float sl2, float m,
                                          uint32_t taddr) {
@@ -134,12 +138,14 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_dense_tc_kernel(const __grid_
 
     const ring::Ring rg{sbase + kOffRing, sbase + kOffBar, kSlots, 1, ring::kSlotBytes};
     auto bar = [&](uint32_t idx) { return sbase + kOffBar + 8u * idx; };
-    const uint32_t B_Q = bar(kBarQ), B_S = bar(kBarS), B_P = bar(kBarP), B_O = bar(kBarO);
+    const uint32_t B_Q = bar(kBarQ), B_S = bar(kBarS), B_F = bar(kBarF), B_P = bar(kBarP),
+                   B_O = bar(kBarO);
 
     if (tid == 0) {
         ring::init_ring_barriers(rg, 1);
         mbar_init(B_Q, 1);
         mbar_init(B_S, 1);
+        mbar_init(B_F, 4);
         mbar_init(B_P, 4);
         mbar_init(B_O, 1);
         fence_mbar_init();
@@ -185,29 +191,36 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_dense_tc_kernel(const __grid_
             const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);
             mbar_wait(B_Q, 0, aborted, p.err);
-            uint32_t seq = 0;
-            for (int j = 0; j < nb; ++j, seq += 2) {
-                rg.wait_full(seq, aborted, p.err);
-                if (j > 0) mbar_wait(B_O, (j - 1) & 1, aborted, p.err);  // P_{j-1} consumed
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem + kColS, sdesc_sw128(sbase + kOffQ + 32 * kk, 16, 1024),
-                           sdesc_sw128(rg.addr(seq) + 32 * kk, 16, 1024), idesc_s, kk > 0);
-                mma_commit(B_S);
-                rg.release_mma(seq);
+            // S_j as soon as the row threads hold S_{j-1} in registers, then PV_{j-1} once they
+            // have written P_{j-1}: the tensor core forms S_j while they exponentiate S_{j-1}
+            auto issue_pv = [&](int j) {
+                const uint32_t vseq = 2u * j + 1u;
                 mbar_wait(B_P, j & 1, aborted, p.err);
-                rg.wait_full(seq + 1, aborted, p.err);
+                rg.wait_full(vseq, aborted, p.err);
                 tc_fence_after();
                 // keys 16kk .. 16kk+15: P packed in columns 8kk .. 8kk+7, V rows 16kk ..
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColO, tmem + kColS + 8 * kk,
-                           sdesc_sw128(rg.addr(seq + 1) + 2048 * kk, 0, 1024), idesc_o,
+                    mma_ts(tmem + kColO, tmem + kColP + 8 * kk,
+                           sdesc_sw128(rg.addr(vseq) + 2048 * kk, 0, 1024), idesc_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(B_O);
-                rg.release_mma(seq + 1);
+                rg.release_mma(vseq);
+            };
+            for (int j = 0; j < nb; ++j) {
+                const uint32_t kseq = 2u * j;
+                rg.wait_full(kseq, aborted, p.err);
+                if (j > 0) mbar_wait(B_F, (j - 1) & 1, aborted, p.err);  // S_{j-1} read out
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem + kColS, sdesc_sw128(sbase + kOffQ + 32 * kk, 16, 1024),
+                           sdesc_sw128(rg.addr(kseq) + 32 * kk, 16, 1024), idesc_s, kk > 0);
+                mma_commit(B_S);
+                rg.release_mma(kseq);
+                if (j > 0) issue_pv(j - 1);
             }
+            issue_pv(nb - 1);
             mbar_wait(B_O, (nb - 1) & 1, aborted, p.err);
         }
     } else {
@@ -231,14 +244,20 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_dense_tc_kernel(const __grid_
             for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) asm volatile("" : "+r"(v[cc][e]));  // after the wait
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B_F);  // the S columns are free for S_{j+1}
             const float mx = (diag ? row_max<true>(v, r) : row_max<false>(v, r)) * sl2;
             // raise the running max only past 2^8: then l and (once PV_{j-1} is done) O are
             // rescaled; a warp rescales O together, rows whose max stays by a factor of 1
             const bool raise = mx > m + kRescale;
             const float corr = raise ? (m == -INFINITY ? 0.f : ex2(m - mx)) : 1.f;
-            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+            // PV_{j-1} must be done: it reads the P columns and accumulates into O
+            if (j > 0) {
                 mbar_wait(B_O, (j - 1) & 1, aborted, p.err);
                 tc_fence_after();
+            }
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
                 __syncwarp();  // converged for the warp-collective TMEM accesses below
                 // 16 columns at a time: the score row stays in registers meanwhile
                 for (int h = 0; h < 4; ++h) {
@@ -256,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_dense_tc_kernel(const __grid_
                 m = mx;
             }
             __syncwarp();
-            // exponentials, written back over S as bf16 pairs (chunk cc -> columns 16cc ..)
-            const uint32_t taddr = tmem + lane_base + kColS;
+            // exponentials into the P columns as bf16 pairs (chunk cc -> columns 16cc ..)
+            const uint32_t taddr = tmem + lane_base + kColP;
             l += diag ? row_exp<true>(v, r, sl2, m, taddr) : row_exp<false>(v, r, sl2, m, taddr);
             tmem_st_wait();
             tc_fence_before();
