@@ -407,6 +407,43 @@ def dense_context_record(fa, L, dev, stream, flush, a, clk):
             "max_abs_diff_vs_sdpa": err, "calls": steps}
 
 
+def streams_step_record(fa, d_in, spec, sched, o, lse, dq, dk, dv, dev, stream, flush, a,
+                        two_kernel_ms, n_streams=2):
+    """The same training step through fibattn_fwd_bwd: the 16 layers split into n_streams
+    groups whose forward and backward run on concurrent streams of the library (forked from and
+    joined back into the timed stream). Timed like the main step; its outputs equal the
+    sequential calls' bit for bit. Kernel times overlap here, so the per-kernel rooflines stay
+    with the sequential step."""
+    ws = torch.empty(fa.fwd_bwd_workspace_size(d_in["q"], spec["W"], sched, n_streams=n_streams),
+                     dtype=torch.uint8, device=dev)
+
+    def sstep():
+        fa.fwd_bwd(d_in["q"], d_in["k"], d_in["v"], d_in["dO"], spec["W"], sched,
+                   n_streams=n_streams, out=o, lse=lse, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(a.warmup):
+        sstep()
+        flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(a.steps)]
+    for s0, e0 in evs:
+        s0.record(stream)
+        sstep()
+        e0.record(stream)
+        flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+    fa.poll_device_error(dev)
+    ms = sum(s0.elapsed_time(e0) for s0, e0 in evs) / a.steps
+    graph = graph_step_record(lambda x: sstep(), d_in, spec, a, flush, stream, dev)
+    return {"ms_per_step": round(ms, 4), "value": round(tokens(spec) / (ms / 1e3), 1),
+            "unit": UNIT, "n_streams": n_streams, "steps": a.steps,
+            "over_sequential_step": round(ms / two_kernel_ms, 3),
+            "graph": {k: graph[k] for k in ("ms_per_step", "value", "unit")},
+            "note": "fibattn_fwd_bwd: layer groups on concurrent streams, fork and join by events; "
+                    "graph: the same step captured once and replayed"}
+
+
 def one_pass_backward_record(fa, L, d_in, spec, sched, o, lse, dq, dk, dv, dev, stream, flush,
                              a, clk, hbm, peak_kind, two_kernel_ms):
     """The same training step with the one-pass backward (fibattn_bwd_fused: a pre-pass for D
@@ -601,6 +638,8 @@ def run_ours(a, spec, world, rank, local):
                                                         peak_kind)
         extras["dense_context_c4"] = dense_context_record(fa, L, dev, stream, flush, a, clk)
         if a.workload == "c5":
+            extras["streams_step"] = streams_step_record(fa, d_in, spec, sched, o, lse, dq, dk, dv,
+                                                         dev, stream, flush, a, ms_per_step)
             extras["one_pass_bwd"] = one_pass_backward_record(fa, L, d_in, spec, sched, o, lse,
                                                               dq, dk, dv, dev, stream, flush, a,
                                                               clk, hbm, peak_kind, ms_per_step)

@@ -158,6 +158,41 @@ FIBATTN_API fibattn_status fibattn_bwd_gqa(const void* q, const void* k, const v
                                            void* cuda_stream);
 
 /*
+ * Forward and backward of a layer stack in one call (a training step of the attention):
+ * the call's Lc layers are split into min(n_streams, Lc) contiguous groups of sizes
+ * differing by at most one, and group g runs fibattn_fwd_gqa then fibattn_bwd_gqa on its
+ * layers on an internal stream of the library. The internal streams (non-blocking, created
+ * once per device) are forked from cuda_stream by an event and joined back into it by
+ * another, so the work is ordered after what cuda_stream holds and everything queued on
+ * cuda_stream later waits for it; the pattern is also valid inside CUDA-graph capture.
+ * Layers are independent problems, so the groups' kernels overlap on the GPU while every
+ * output equals the sequential fibattn_fwd_gqa + fibattn_bwd_gqa calls bit for bit.
+ *   q, k, v, dO : inputs as fibattn_bwd_gqa; o, lse : written (the forward's outputs);
+ *   dq, dk, dv  : written. n_streams in [1, FIBATTN_STEP_STREAMS_MAX]; 1 runs both calls on
+ *   cuda_stream itself.
+ *   workspace   : 256-byte aligned, at least fibattn_fwd_bwd_workspace_size() bytes: each
+ *                 group's backward workspace, 256-aligned, one after the other.
+ * Calls on different host threads share the internal streams of a device (their work is
+ * ordered, not raced). Errors: those of fibattn_fwd_gqa / fibattn_bwd_gqa, checked for every
+ * group before anything is enqueued; INVALID_ARG for n_streams out of range or a short
+ * workspace; CUDA for a failed stream or event call.
+ */
+#define FIBATTN_STEP_STREAMS_MAX 8
+FIBATTN_API fibattn_status fibattn_fwd_bwd_workspace_size(int32_t B, int32_t H, int32_t T,
+                                                          int32_t d, int32_t dtype, int32_t W,
+                                                          const fibattn_schedule* sched,
+                                                          int32_t layer0, int32_t n_layers_call,
+                                                          int32_t n_streams, uint64_t* bytes);
+FIBATTN_API fibattn_status fibattn_fwd_bwd(const void* q, const void* k, const void* v,
+                                           const void* dO, void* o, float* lse, void* dq,
+                                           void* dk, void* dv, void* workspace,
+                                           uint64_t workspace_bytes, int32_t B, int32_t H,
+                                           int32_t H_kv, int32_t T, int32_t d, int32_t dtype,
+                                           int32_t W, float scale, const fibattn_schedule* sched,
+                                           int32_t layer0, int32_t n_layers_call,
+                                           int32_t n_streams, void* cuda_stream);
+
+/*
  * Fractional-offset table of one real alpha: the learned-alpha variant of the pages
  * (Metodologia / Arquitetura, "Implementacao": keys and values are linearly interpolated
  * between rows so that the gradient reaches alpha when alpha * F is not an integer).

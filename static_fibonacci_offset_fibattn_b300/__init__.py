@@ -26,7 +26,7 @@ __all__ = ["Schedule", "FibAttnError", "offsets", "offsets_device", "fwd", "bwd"
            "bwd_workspace_size", "last_cuda_error", "frac_offsets", "fwd_frac", "bwd_frac",
            "bwd_frac_workspace_size", "FibFracAttention", "rope_table", "rope", "fwd_rope",
            "bwd_rope", "fwd_rope_fused", "bwd_fused", "bwd_fused_workspace_size",
-           "debug_wait_timeout"]
+           "fwd_bwd", "fwd_bwd_workspace_size", "STEP_STREAMS_MAX", "debug_wait_timeout"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfibattn.so")
@@ -34,6 +34,7 @@ MAX_OFFSETS = 64
 
 OK, INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA_ERR, TIMEOUT, SCRATCH_LIMIT = range(7)
 NOALLOC_SCRATCH_BYTES = 40 << 20
+STEP_STREAMS_MAX = 8
 _BASES = {"fib": 0, "pow2": 1}
 _KINDS = {"fixed": 0, "linear": 1, "coprime": 2}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
@@ -122,6 +123,10 @@ def lib():
                                   i32, i32, f32, sp, i32, i32, vp]
         L.fibattn_bwd_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
                                         i32, i32, i32, f32, sp, i32, i32, vp]
+        L.fibattn_fwd_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, sp, i32, i32,
+                                                     i32, ctypes.POINTER(u64)]
+        L.fibattn_fwd_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i32, i32, i32,
+                                      i32, i32, i32, i32, f32, sp, i32, i32, i32, vp]
         L.fibattn_debug_wait_timeout.argtypes = [i32, vp]
         L.fibattn_debug_wait_timeout.restype = i32
         L.fibattn_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
@@ -418,6 +423,55 @@ def bwd_fused(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
                                  layer0, Lc, _stream(q))
     _check(st, "fibattn_bwd_fused")
     return dq, dk, dv
+
+
+def fwd_bwd_workspace_size(q: torch.Tensor, W: int, sched: Schedule, layer0: int = 0,
+                           n_streams: int = 2) -> int:
+    """Bytes of device workspace fibattn_fwd_bwd needs for tensors shaped like q."""
+    Lc, B, H, T, d = _shape(q)
+    if q.dtype not in _DTYPES:
+        raise ValueError("dtype must be float32 or bfloat16")
+    n = ctypes.c_uint64(0)
+    s = sched.to_c()
+    _check(lib().fibattn_fwd_bwd_workspace_size(B, H, T, d, _DTYPES[q.dtype], W, ctypes.byref(s),
+                                                layer0, Lc, int(n_streams), ctypes.byref(n)),
+           "fibattn_fwd_bwd_workspace_size")
+    return int(n.value)
+
+
+def fwd_bwd(q, k, v, dO, W: int, sched: Schedule, layer0: int = 0, n_streams: int = 2,
+            scale: Optional[float] = None, out=None, lse=None, dq=None, dk=None, dv=None,
+            workspace=None):
+    """Forward and backward of the layer stack in one call (fibattn_fwd_bwd): the layers are
+    split into n_streams groups that run on concurrent streams of the library, forked from and
+    joined back into the current stream. Returns (o, lse, dq, dk, dv), equal bit for bit to
+    fwd() followed by bwd()."""
+    Lc, B, H, T, d = _shape(q)
+    Hkv = _kv_heads(q, k, v)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if lse is None else lse
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_tensors(q, o, dO, dq)
+    _check_tensors(k, v, dk, dv)
+    if k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("q/k/v must share device and dtype")
+    if lse.dtype != torch.float32 or lse.device != q.device or tuple(lse.shape) != tuple(q.shape[:-1]):
+        raise ValueError("lse must be float32 [..., T] on q's device")
+    need = fwd_bwd_workspace_size(q, W, sched, layer0, n_streams)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on q's device")
+    s = sched.to_c()
+    st = lib().fibattn_fwd_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(o), _ptr(lse), _ptr(dq),
+                               _ptr(dk), _ptr(dv), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), B, H, Hkv, T, d,
+                               _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0,
+                               Lc, int(n_streams), _stream(q))
+    _check(st, "fibattn_fwd_bwd")
+    return o, lse, dq, dk, dv
 
 
 def bwd_noalloc(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,

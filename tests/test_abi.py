@@ -307,3 +307,48 @@ def test_bwd_fused_workspace_size_is_d_and_lse_only():
     q = torch.empty(16, 8, 8, 1023, 64, dtype=torch.bfloat16, device="meta")
     rows = 16 * 8 * 8 * 1024
     assert fa.bwd_fused_workspace_size(q) == 2 * ((rows * 4 + 255) // 256 * 256)
+
+
+def test_fwd_bwd_validates_before_launch():
+    # null or misaligned pointers, n_streams out of [1, 8], a misaligned or short workspace:
+    # INVALID_ARG; a bad head size: UNSUPPORTED; all decided on the host before any launch
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    ok = ctypes.c_void_p(256)
+    big = ctypes.c_uint64(1 << 40)
+    args = [ok] * 10
+    tail = lambda ns, d=64: (1, 1, 1, 8, d, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ns, None)
+    for bad in range(10):
+        a = list(args)
+        a[bad] = ctypes.c_void_p(0)
+        assert L.fibattn_fwd_bwd(*a, big, *tail(2)) == fa.INVALID_ARG
+    for ns in (0, 9, -1):
+        assert L.fibattn_fwd_bwd(*args, big, *tail(ns)) == fa.INVALID_ARG
+    a = list(args)
+    a[9] = ctypes.c_void_p(256 + 16)
+    assert L.fibattn_fwd_bwd(*a, big, *tail(2)) == fa.INVALID_ARG
+    assert L.fibattn_fwd_bwd(*args, ctypes.c_uint64(16), *tail(2)) == fa.INVALID_ARG
+    assert L.fibattn_fwd_bwd(*args, big, *tail(2, d=32)) == fa.UNSUPPORTED
+
+
+@pytest.mark.parametrize("n_streams", [1, 2, 3, 8])
+def test_fwd_bwd_workspace_is_the_groups_workspaces(n_streams):
+    # the layers split into min(n_streams, Lc) contiguous groups; the workspace is each group's
+    # backward workspace, 256-aligned, one after the other
+    sched = dict(kind="coprime", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=16,
+                 coprime_c=5)
+    sc = fa.Schedule(**sched).to_c()
+    L = fa.lib()
+    B, H, T, W, layer0, Lc = 2, 8, 1000, 64, 1, 13
+    got = ctypes.c_uint64(0)
+    assert L.fibattn_fwd_bwd_workspace_size(B, H, T, 64, 1, W, ctypes.byref(sc), layer0, Lc,
+                                            n_streams, ctypes.byref(got)) == fa.OK
+    groups = min(n_streams, Lc)
+    want = 0
+    for g in range(groups):
+        a, b = Lc * g // groups, Lc * (g + 1) // groups
+        n = ctypes.c_uint64(0)
+        assert L.fibattn_bwd_workspace_size(B, H, T, 64, 1, W, ctypes.byref(sc), layer0 + a, b - a,
+                                            ctypes.byref(n)) == fa.OK
+        want += (n.value + 255) // 256 * 256
+    assert got.value == want
