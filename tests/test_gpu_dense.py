@@ -83,3 +83,14 @@ def test_dense_forward_deterministic_and_backward_consistent():
     from gpu_common import assert_grad
     for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         assert_grad(n, f64(got[0]), ref, "bf16")
+
+
+def test_dense_forward_more_layers_than_one_launch():
+    # 18 layers (launches of 16 + 2) equal the per-layer calls bit for bit
+    sched = dict(kind="linear", base="fib", alpha_min=(1, 2), alpha_max=(2, 1), n_layers=20)
+    sc = lib_schedule(sched)
+    dev = to_dev(fi.draw((18, 1, 2, 333, 64), seed=79, scale=0.5, dtype="bf16"))
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], 400, sc, layer0=1)
+    for c in (0, 15, 16, 17):
+        oc, lc = fa.fwd(dev["q"][c], dev["k"][c], dev["v"][c], 400, sc, layer0=1 + c)
+        assert torch.equal(oc, o[c]) and torch.equal(lc, lse[c])
