@@ -172,6 +172,8 @@ FIBATTN_API fibattn_status fibattn_bwd_gqa(const void* q, const void* k, const v
  *   cuda_stream itself.
  *   workspace   : 256-byte aligned, at least fibattn_fwd_bwd_workspace_size() bytes: each
  *                 group's backward workspace, 256-aligned, one after the other.
+ * The first call with n_streams > 1 on a device creates that device's internal streams: make
+ * it before any stream capture (creating a stream is not allowed while one is captured).
  * Calls on different host threads share the internal streams of a device (their work is
  * ordered, not raced). Errors: those of fibattn_fwd_gqa / fibattn_bwd_gqa, checked for every
  * group before anything is enqueued; INVALID_ARG for n_streams out of range or a short

@@ -445,7 +445,8 @@ def fwd_bwd(q, k, v, dO, W: int, sched: Schedule, layer0: int = 0, n_streams: in
     """Forward and backward of the layer stack in one call (fibattn_fwd_bwd): the layers are
     split into n_streams groups that run on concurrent streams of the library, forked from and
     joined back into the current stream. Returns (o, lse, dq, dk, dv), equal bit for bit to
-    fwd() followed by bwd()."""
+    fwd() followed by bwd(). The first call with n_streams > 1 on a device creates the
+    library's streams there: make it before any CUDA-graph capture."""
     Lc, B, H, T, d = _shape(q)
     Hkv = _kv_heads(q, k, v)
     o = torch.empty_like(q) if out is None else out
