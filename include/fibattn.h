@@ -20,6 +20,8 @@
  *     fibattn_bwd_noalloc (both static). Device pointers must be 16-byte aligned.
  *   - Work is enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default
  *     stream) and returns once launched; results are ready when the stream is.
+ *     (fibattn_fwd_bwd forks its work to internal streams and joins it back into
+ *     cuda_stream, so the same holds for it.)
  *   - Nothing is printed. Errors are returned as fibattn_status; kernel-side
  *     failures (a bounded wait that ran out) are latched in the device error word
  *     and reported by fibattn_poll_device_error().
