@@ -75,3 +75,22 @@ def test_dense_kernel_at_long_length_matches_sdpa():
     mask = torch.arange(T, device=s.device)[None, :] > torch.arange(T - 256, T, device=s.device)[:, None]
     s = s.masked_fill(mask, float("-inf"))
     assert max_abs(f64(lse[0, 0][:, -256:]), f64(torch.logsumexp(s, dim=-1))) <= LSE_TOL["bf16"]
+
+
+def test_fp32_path_at_long_length():
+    # the fp32 SIMT path (1e-5) on an 8,192-row sequence with offsets up to 1974 rows back
+    T, W, layer = 8192, 64, 15
+    inp = fi.draw((1, 1, 2, T, 64), seed=307, scale=0.5, dtype="f32", names=("q", "k", "v", "dO"))
+    dev = to_dev(inp)
+    sc = lib_schedule(STAGGER)
+    o, lse = fa.fwd(dev["q"], dev["k"], dev["v"], W, sc, layer0=layer)
+    dq, dk, dv = fa.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["dO"], W, sc, layer0=layer)
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    tab = oracle_table(STAGGER, layer, W, T)
+    g = lambda n: f64(inp[n][0, 0])
+    rq, rk, rv, ro, rl = oracle.bwd(g("q"), g("k"), g("v"), g("dO"), W, tab)
+    assert max_abs(f64(o[0, 0]), ro) <= TOL["f32"]
+    assert max_abs(f64(lse[0, 0]), rl) <= LSE_TOL["f32"]
+    for n, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert_grad(n, f64(got[0, 0]), ref, "f32")
