@@ -19,8 +19,9 @@
 //   tensor core forms S_{j+1} while the row threads work on block j), takes the row max over
 //   its allowed keys (all of them, or k <= i in the diagonal block) and raises its running
 //   max m only when the block's max exceeds it by more than 2^8 (then O and the sum l are
-//   rescaled, once PV_{j-1} has completed); the exponentials 2^(s - m) <= 2^8 go to TMEM
-//   columns [192, 256) as bf16;
+//   rescaled, once PV_{j-1} has completed); the exponentials 2^(s - m) <= 2^8 are formed in
+//   registers as bf16 pairs and go to TMEM columns [192, 256) once PV_{j-1}, which reads
+//   those columns, has completed (so its latency is not on the row threads' path);
 //   O += P V_j (A = P from TMEM, B = V_j MN-major) into TMEM columns [128, 192).
 // Epilogue: O / l staged in the Q buffer (every S MMA that read it has completed), TMA store;
 // lse = (m + log2 l) ln 2.
@@ -91,15 +92,15 @@ __device__ __forceinline__ float row_max(const uint32_t (&v)[4][32], int r) {
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
 
-// p = 2^(s sl2 - m) of a row (0 for masked columns), written to TMEM at taddr as bf16 pairs
-// (32-column chunk cc to columns 16cc ..); returns the sum of the p (four partial sums).
+// p = 2^(s sl2 - m) of a row (0 for masked columns) as bf16 pairs, 32-column chunk cc in
+// pk[cc] (for TMEM columns 16cc ..); returns the sum of the p (four partial sums). The pairs
+// stay in registers so that the exponentials need not wait for the previous block's P V.
 template <bool kDiag>
 __device__ __forceinline__ float row_exp(const uint32_t (&v)[4][32], int r, float sl2, float m,
-                                         uint32_t taddr) {
+                                         uint32_t (&pk)[4][16]) {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
-        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
             const int c = 32 * cc + e;
@@ -111,10 +112,9 @@ __device__ __forceinline__ float row_exp(const uint32_t (&v)[4][32], int r, floa
             a1 += p1;
             a2 += p2;
             a3 += p3;
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-            pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
+            pk[cc][e >> 1] = pack_bf16x2(p0, p1);
+            pk[cc][(e >> 1) + 1] = pack_bf16x2(p2, p3);
         }
-        tmem_st16(taddr + 16 * cc, pk);
     }
     return (a0 + a1) + (a2 + a3);
 }
@@ -249,17 +249,26 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_dense_tc_kernel(const __grid_
             if (lane == 0) mbar_arrive(B_F);  // the S columns are free for S_{j+1}
             const float mx = (diag ? row_max<true>(v, r) : row_max<false>(v, r)) * sl2;
             // raise the running max only past 2^8: then l and (once PV_{j-1} is done) O are
-            // rescaled; a warp rescales O together, rows whose max stays by a factor of 1
+            // rescaled
             const bool raise = mx > m + kRescale;
             const float corr = raise ? (m == -INFINITY ? 0.f : ex2(m - mx)) : 1.f;
-            // PV_{j-1} must be done: it reads the P columns and accumulates into O
+            if (raise) {
+                l *= corr;
+                m = mx;
+            }
+            // the exponentials into registers, as bf16 pairs: they need only the scores
+            uint32_t pk[4][16];
+            l += diag ? row_exp<true>(v, r, sl2, m, pk) : row_exp<false>(v, r, sl2, m, pk);
+            // PV_{j-1} must be done before the P columns are overwritten and before O is
+            // rescaled: it reads the P columns and accumulates into O
             if (j > 0) {
                 mbar_wait(B_O, (j - 1) & 1, aborted, p.err);
                 tc_fence_after();
             }
+            __syncwarp();  // converged for the warp-collective TMEM accesses below
             if (j > 0 && __any_sync(0xffffffffu, raise)) {
-                __syncwarp();  // converged for the warp-collective TMEM accesses below
-                // 16 columns at a time: the score row stays in registers meanwhile
+                // a warp rescales O together, rows whose max stays by a factor of 1;
+                // 16 columns at a time: the P pairs stay in registers meanwhile
                 for (int h = 0; h < 4; ++h) {
                     uint32_t w[16];
                     tmem_ld16(tmem + lane_base + kColO + 16 * h, w);
@@ -268,16 +277,10 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_dense_tc_kernel(const __grid_
                     for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * corr);
                     tmem_st16(tmem + lane_base + kColO + 16 * h, w);
                 }
-                tmem_st_wait();
             }
-            if (raise) {
-                l *= corr;
-                m = mx;
-            }
-            __syncwarp();
-            // exponentials into the P columns as bf16 pairs (chunk cc -> columns 16cc ..)
-            const uint32_t taddr = tmem + lane_base + kColP;
-            l += diag ? row_exp<true>(v, r, sl2, m, taddr) : row_exp<false>(v, r, sl2, m, taddr);
+            // P into its columns (chunk cc -> columns 16cc ..)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) tmem_st16(tmem + lane_base + kColP + 16 * cc, pk[cc]);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
