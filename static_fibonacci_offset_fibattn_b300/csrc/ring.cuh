@@ -78,9 +78,14 @@ struct Ring {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(empty(seq));
     }
-    // MMA-warp release: the slot is free once the MMAs issued so far have completed
+    // MMA-warp release: the slot is free once the MMAs issued so far have completed. All but
+    // one of the EMPTY barrier's arrivals are made at once; the last is the commit, which
+    // arrives when those MMAs complete, so the phase cannot complete before they do. (Each
+    // tcgen05.commit costs the issuing thread about as much as an MMA; one per release keeps
+    // them off the MMA warp's path.)
     __device__ __forceinline__ void release_mma(uint32_t seq) const {
-        for (uint32_t i = 0; i < empty_arrivals; ++i) tc::mma_commit(empty(seq));
+        if (empty_arrivals > 1) tc::mbar_arrive_cnt(empty(seq), empty_arrivals - 1);
+        tc::mma_commit(empty(seq));
     }
     // release of a staging slot by one thread, after its bulk store has read the slot
     __device__ __forceinline__ void release_stage(uint32_t seq) const {
