@@ -347,6 +347,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             uint32_t seq = 0, gcount = 0, tcount = 0;
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);
             const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
+            const uint32_t idesc_s2 = idesc_bf16(128, 128, 0, 0);
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x, ++tcount) {
                 int half;
                 const ring::Tile tl = tile_at<kWide>(p, idx, half);
@@ -365,6 +366,18 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                     if constexpr (kRope) mbar_wait(B_R, gcount & 1, aborted, p.err);  // rotated in place
                     tc_fence_after();
                     for (int c = 0; c < nch; ++c) {
+                        if (!kWide && (c & 1) == 0 && c + 1 < nch) {
+                            // two chunks of one slot (128 contiguous key rows): one N = 128 MMA
+                            // per k-step into columns [64c, 64c + 128)
+                            const uint32_t qaddr = rg.addr(qseq);
+                            const uint32_t kaddr = rg.addr(kseq + c / 2);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tmem + 64 * c, sdesc_sw128(qaddr + 32 * kk, 16, 1024),
+                                       sdesc_sw128(kaddr + 32 * kk, 16, 1024), idesc_s2, kk > 0);
+                            ++c;
+                            continue;
+                        }
                         if constexpr (kWide) {
                             // K-dim 128: Q half 0 against the chunk's columns 0-63, then half 1
                             const uint32_t kaddr = rg.addr(kseq + c);
