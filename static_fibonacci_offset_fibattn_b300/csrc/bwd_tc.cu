@@ -126,11 +126,16 @@ namespace dq {
 
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 64, kColP = 128;  // dQ accumulator in columns [0, 64)
+// dQ accumulator in columns [0, 64), S and dP of a 64-key chunk in [64, 128) and [128, 192),
+// the chunk's dS (bf16 pairs, the dQ MMA's A operand) in [192, 224): the row threads free the
+// S and dP columns as soon as they hold them in registers, so that the next chunk's S and dP
+// form while they compute this chunk's dS (head size 64)
+constexpr uint32_t kColS = 64, kColP = 128, kColDS = 192;
 
 // barriers: 0 q+dO, 1-2 band K/V full, 3 S/dP ready, 4 dS written (128), 5 dQ MMA done,
-// 6-7 ring full, 8-9 ring empty (128), 10 band done (every band MMA has completed)
-constexpr int kNumBars = 11;
+// 6-7 ring full, 8-9 ring empty (128), 10 band done (every band MMA has completed),
+// 11 S/dP read out (4 warps)
+constexpr int kNumBars = 12;
 // Shared memory: the Q and dO tiles, two stages of K and V chunks, the two ring slots (a
 // tile, plus in the fractional mode the 8 rows after it). Head size 128 (kWide) doubles the
 // tiles (two 64-column halves each) but keeps one stage of K and V chunks (both halves: 16 KB
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
     const uint32_t B_DQ = bar_at(sbase, kOffBar, 5);
     auto B_FULL = [&](int s) { return bar_at(sbase, kOffBar, 6 + s); };
     auto B_EMPTY = [&](int s) { return bar_at(sbase, kOffBar, 8 + s); };
-    const uint32_t B_BD = bar_at(sbase, kOffBar, 10);
+    const uint32_t B_BD = bar_at(sbase, kOffBar, 10), B_F = bar_at(sbase, kOffBar, 11);
     static_assert(!kWide || (L::kOffRing == L::kOffK && L::kOffV == L::kOffK + kSlot && L::kStage == kSlot),
                   "head size 128: the ring slots are the K and V stages");
 
@@ -204,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
 
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b)
-            mbar_init(bar_at(sbase, kOffBar, b), (b == 4 || b == 8 || b == 9) ? kRows : 1);
+            mbar_init(bar_at(sbase, kOffBar, b), (b == 4 || b == 8 || b == 9) ? kRows : (b == 11 ? 4 : 1));
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -248,14 +253,20 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
             } else {
                 load_chunk(0);
                 if (n_chunks > 1) load_chunk(1);
+                // the later chunks load only once a stage frees: bring them into L2 now
+                for (int c = 2; c < n_chunks; ++c) {
+                    const int32_t y = (c_lo + c) * kChunk;
+                    tma_prefetch_l2_3d(&p.tm_k, 0, y, zk);
+                    tma_prefetch_l2_3d(&p.tm_v, 0, y, zk);
+                }
             }
             mbar_wait(B_QDO, 0, aborted, p.err);
             const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
             const uint32_t idesc_q = idesc_bf16(128, 64, 0, 1);
-            for (int c = 0; c < n_chunks; ++c) {
+            // S = Q K_c^T and dP = dO V_c^T of chunk c
+            auto issue_sdp = [&](int c) {
                 const int s = kWide ? 0 : (c & 1);
                 mbar_wait(B_KV(s), (kWide ? c : c >> 1) & 1, aborted, p.err);
-                if (c > 0) mbar_wait(B_DQ, (c - 1) & 1, aborted, p.err);
                 tc_fence_after();
                 const uint32_t kaddr = sbase + kOffK + s * kStage;
                 const uint32_t vaddr = sbase + kOffV + s * kStage;
@@ -273,12 +284,17 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                            sdesc_sw128(vaddr + (kk >> 2) * kChunkBytes + 32 * (kk & 3), 16, 1024),
                            idesc_s, kk > 0);
                 mma_commit(B_S);
+            };
+            // dQ (own output half) += dS_c K_c_half, once the row threads have written dS_c;
+            // then the chunk's stage takes the chunk after next
+            auto issue_dq = [&](int c) {
+                const int s = kWide ? 0 : (c & 1);
+                const uint32_t kaddr = sbase + kOffK + s * kStage;
                 mbar_wait(B_DS, c & 1, aborted, p.err);
                 tc_fence_after();
-                // dQ (own output half) += dS K_half
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tmem, tmem + kColS + 8 * kk,
+                    mma_ts(tmem, tmem + kColDS + 8 * kk,
                            sdesc_sw128(kaddr + half * kChunkBytes + 2048 * kk, 0, 1024),
                            idesc_q, (c > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(B_DQ);
@@ -287,6 +303,22 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                     mbar_wait(B_DQ, c & 1, aborted, p.err);
                     load_chunk(next);
                 }
+            };
+            if constexpr (kWide) {
+                // one stage: chunk c + 1 loads into it once dQ of chunk c is done
+                for (int c = 0; c < n_chunks; ++c) {
+                    issue_sdp(c);
+                    issue_dq(c);
+                }
+            } else {
+                // S/dP of chunk c as soon as the row threads hold chunk c - 1's, then dQ of c - 1
+                issue_sdp(0);
+                for (int c = 1; c < n_chunks; ++c) {
+                    mbar_wait(B_F, (c - 1) & 1, aborted, p.err);
+                    issue_sdp(c);
+                    issue_dq(c - 1);
+                }
+                issue_dq(n_chunks - 1);
             }
             mma_commit(B_BD);  // the stage memory is free for the ring once every MMA completes
             mbar_wait(B_DQ, (n_chunks - 1) & 1, aborted, p.err);
@@ -372,24 +404,32 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
             p.lse2[wrow] = lse2;
         }
 
-        // ---- band: dS over the window, written back to TMEM as the dQ MMA's A operand
+        // ---- band: dS over the window, into TMEM as the dQ MMA's A operand
         for (int c = 0; c < n_chunks; ++c) {
             const int32_t kb = (c_lo + c) * kChunk;
             const int32_t d0 = i - kb;
             mbar_wait(B_S, c & 1, aborted, p.err);
             tc_fence_after();
             __syncwarp();  // converged for the warp-collective TMEM accesses below
+            uint32_t pk[2][16];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 // does any (row of this warp, key of this 32-column half) pair lie in the window?
                 const int32_t rlo = i0 + warp * 32, klo = kb + 32 * hh;
                 const bool need = (rlo + 31 - klo >= 0) && (rlo - (klo + 31) < W);
-                uint32_t pk[16];
+                uint32_t sv[32], dv[32];
                 if (need) {
-                    uint32_t sv[32], dv[32];
                     tmem_ld32(tmem + lane_base + kColS + 32 * hh, sv);
                     tmem_ld32(tmem + lane_base + kColP + 32 * hh, dv);
                     tmem_ld_wait(sv, dv);
+                }
+                if (hh == 1) {
+                    // both halves are in registers: the S and dP columns are free
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B_F);
+                }
+                if (need) {
                     const int32_t dj = d0 - 32 * hh;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -397,15 +437,22 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                         const bool ok1 = row_ok && (uint32_t)(dj - e - 1) < (uint32_t)W;
                         const float p0 = ok0 ? ex2(__uint_as_float(sv[e]) * sl2 - lse2) : 0.f;
                         const float p1 = ok1 ? ex2(__uint_as_float(sv[e + 1]) * sl2 - lse2) : 0.f;
-                        pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - D),
-                                                 p1 * (__uint_as_float(dv[e + 1]) - D));
+                        pk[hh][e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - D),
+                                                     p1 * (__uint_as_float(dv[e + 1]) - D));
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                    for (int e = 0; e < 16; ++e) pk[hh][e] = 0u;
                 }
-                tmem_st16(tmem + lane_base + kColS + 16 * hh, pk);
             }
+            // dQ of the chunk before has read the dS columns
+            if (c > 0) {
+                mbar_wait(B_DQ, (c - 1) & 1, aborted, p.err);
+                tc_fence_after();
+            }
+            __syncwarp();  // converged for the warp-collective TMEM accesses below
+            tmem_st16(tmem + lane_base + kColDS, pk[0]);
+            tmem_st16(tmem + lane_base + kColDS + 16, pk[1]);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(B_DS);

@@ -94,6 +94,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& a
 // ------------------------------------------------------------------ TMA
 // 3D tiled load, box written to smem with the tensor map's swizzle; completion is
 // signalled as transaction bytes on `bar`.
+// Brings a 3D tile into L2 ahead of a later load of it (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y, int32_t z) {
     asm volatile(
