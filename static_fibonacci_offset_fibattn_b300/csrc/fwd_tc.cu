@@ -348,6 +348,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);
             const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
             const uint32_t idesc_s2 = idesc_bf16(128, 128, 0, 0);
+            const uint32_t idesc_s3 = idesc_bf16(128, 192, 0, 0);
             for (uint32_t idx = blockIdx.x; idx < p.total_tiles; idx += gridDim.x, ++tcount) {
                 int half;
                 const ring::Tile tl = tile_at<kWide>(p, idx, half);
@@ -365,7 +366,17 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                     for (int j = 0; j < nk; ++j) rg.wait_full(kseq + j, aborted, p.err);
                     if constexpr (kRope) mbar_wait(B_R, gcount & 1, aborted, p.err);  // rotated in place
                     tc_fence_after();
-                    for (int c = 0; c < nch; ++c) {
+                    // head size 64, three chunks in two consecutive slots that do not wrap
+                    // around the ring: 192 key rows at one stride, one N = 192 MMA per k-step
+                    const bool one_n192 = !kWide && !kFrac && nch == 3 && rg.slot(kseq) + 1 < kSlots;
+                    if (one_n192) {
+                        const uint32_t qaddr = rg.addr(qseq), kaddr = rg.addr(kseq);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem, sdesc_sw128(qaddr + 32 * kk, 16, 1024),
+                                   sdesc_sw128(kaddr + 32 * kk, 16, 1024), idesc_s3, kk > 0);
+                    }
+                    for (int c = 0; c < (one_n192 ? 0 : nch); ++c) {
                         if (!kWide && (c & 1) == 0 && c + 1 < nch) {
                             // two chunks of one slot (128 contiguous key rows): one N = 128 MMA
                             // per k-step into columns [64c, 64c + 128)
