@@ -696,8 +696,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_fused_kernel(const __grid_con
         }
     }
 
+    // after a timeout in this CTA, its own copies and MMAs in flight land before TMEM is released
     tc_fence_before();
-    __syncthreads();
+    settle_if_aborted(__syncthreads_or(aborted ? 1 : 0));
     if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

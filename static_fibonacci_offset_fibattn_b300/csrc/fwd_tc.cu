@@ -731,8 +731,9 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
         }
     }
 
+    // after a timeout in this CTA, its own copies and MMAs in flight land before TMEM is released
     tc_fence_before();
-    __syncthreads();
+    settle_if_aborted(__syncthreads_or(aborted ? 1 : 0));
     if (warp == 4) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

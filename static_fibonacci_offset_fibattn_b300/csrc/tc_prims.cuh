@@ -91,6 +91,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& a
     }
 }
 
+// After a bounded wait has run out in a CTA, its later waits return at once, so it may reach
+// its teardown with its own bulk copies or MMAs still in flight. Its threads then wait a
+// fixed 100 us at the final barrier, far longer than any of those takes to land, before the
+// CTA releases TMEM and its shared memory: the timeout stays an error status instead of
+// becoming a fault. (`any_aborted` comes from __syncthreads_or over the threads' flags.)
+__device__ __forceinline__ void settle_if_aborted(int any_aborted) {
+    if (!any_aborted) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) __nanosleep(1000);
+}
+
 // ------------------------------------------------------------------ TMA
 // 3D tiled load, box written to smem with the tensor map's swizzle; completion is
 // signalled as transaction bytes on `bar`.
