@@ -39,7 +39,8 @@
 // taken in the same order, so the two backwards agree bit for bit.
 //
 // Every mbarrier wait is bounded (tc::mbar_wait); a wait that runs out latches the device
-// error word, later waits return at once, and the block still releases its TMEM.
+// error word, later waits return at once, and the block still releases its TMEM, after a
+// fixed wait that lets its own copies and MMAs in flight land (tc::settle_if_aborted).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>

@@ -16,8 +16,11 @@
 //   Preamble: D_i from o_i (the first item of the offset ring) and dO_i, written to the
 //   workspace for the second kernel.
 //   Band, per 64-key chunk: S = Q K^T and dP = dO V^T (M=128, N=64) into TMEM; each row
-//   thread forms dS = P (dP - D) in fp32 and writes it back as bf16 over S; then
-//   dQ += dS K (A = dS from TMEM, B = K chunk MN-major) accumulates in TMEM.
+//   thread forms dS = P (dP - D) in fp32 and writes it as bf16 to TMEM columns of its own;
+//   then dQ += dS K (A = dS from TMEM, B = K chunk MN-major) accumulates in TMEM. At head
+//   size 64 the row threads signal once a chunk's S and dP are in their registers, and the
+//   next chunk's S and dP form while they compute dS (chunks past the two K/V stages are
+//   prefetched into L2 at the start).
 //   Offsets (a diagonal per table entry): s = q.k_{i-o}, dp = dO.v_{i-o} by CUDA-core row
 //   dot products, dq += ds k_{i-o} in registers; (P, dS) of each (row, offset) pair is
 //   written to the workspace as a bf16 pair, indexed by the key row i-o; D and lse log2(e)
@@ -50,7 +53,8 @@
 // as row lo + 1, weight w); its shifted Q/dO items carry the 8 rows before their tile.
 //
 // Every mbarrier wait is bounded (tc::mbar_wait); a wait that runs out latches the device
-// error word, later waits return at once, and the CTA still releases its TMEM.
+// error word, later waits return at once, and the CTA still releases its TMEM, after a fixed
+// wait that lets its own copies and MMAs in flight land (tc::settle_if_aborted).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>

@@ -26,7 +26,8 @@
 // Epilogue: O / l staged in the Q buffer (every S MMA that read it has completed), TMA store;
 // lse = (m + log2 l) ln 2.
 // Every mbarrier wait is bounded (tc::mbar_wait); a wait that runs out latches the device
-// error word, later waits return at once, and the CTA still releases its TMEM.
+// error word, later waits return at once, and the CTA still releases its TMEM, after a fixed
+// wait that lets its own copies and MMAs in flight land (tc::settle_if_aborted).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>

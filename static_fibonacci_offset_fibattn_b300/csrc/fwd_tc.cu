@@ -18,7 +18,10 @@
 // V[i0-o ..] (negative rows zero-filled); a staging slot for the output tile. Every item is
 // released without waiting on a later one, so the in-order ring cannot stall.
 // Band: keys [max(0, i0-W+1), i0+127] in 64-key chunks, up to 3 chunks per group:
-//   S = Q K^T (tcgen05, M=128, N=64 per chunk, K=64) -> TMEM columns [0, 192)
+//   S = Q K^T (tcgen05, M=128, K=64) -> TMEM columns [0, 192): one N=192 MMA per k-step when
+//   the three chunks sit in consecutive slots, else N=128 for the two chunks of a slot and
+//   N=64 for a lone one (each tcgen05.mma costs the issuing thread about 100 cycles, and the
+//   tile's S is on the row threads' path)
 //   masked online softmax per row (fp32, log2 domain), P (bf16) written back over S
 //   O_band += P V (tcgen05, A = P from TMEM, B = V MN-major in smem) -> TMEM [192, 256)
 // Offsets: thread r takes row r of each shifted tile: s = q_r . k_{i-o}, then accumulates
@@ -368,6 +371,7 @@ fwd_tc_kernel(const __grid_constant__ FwdArgs<kFrac> p) {
                     tc_fence_after();
                     // head size 64, three chunks in two consecutive slots that do not wrap
                     // around the ring: 192 key rows at one stride, one N = 192 MMA per k-step
+                    // (the fractional mode's 17 KB slots break the stride)
                     const bool one_n192 = !kWide && !kFrac && nch == 3 && rg.slot(kseq) + 1 < kSlots;
                     if (one_n192) {
                         const uint32_t qaddr = rg.addr(qseq), kaddr = rg.addr(kseq);
