@@ -124,3 +124,14 @@ def test_one_pass_backward_bytes_per_token():
     c5 = fi.WORKLOADS["c5"]
     assert {k: v for k, v in c5o.items() if k not in ("desc", "bwd_fused")} == \
         {k: v for k, v in c5.items() if k != "desc"}
+
+
+def test_committed_traffic_covers_the_current_sources():
+    # the bench reports DRAM traffic from profiles/ncu_traffic.txt only for the kernel source
+    # it was captured on (a sha256 prefix); the default run's kernels must have a line for
+    # their current sources, else the roofline records carry traffic null
+    for kernel, workload in [("fwd_tc_bf16", "c4"), ("fwd_tc_bf16", "c5"), ("bwd_dq_tc", "c5"),
+                             ("bwd_dkdv_tc", "c5"), ("bwd_fused_tc", "c5o"), ("bwd_prep", "c5o")]:
+        t = bench.committed_traffic(kernel, workload)
+        assert t is not None, (kernel, workload, "recapture its traffic line on the current source")
+        assert 100.0 < t < 2000.0, (kernel, workload, t)
