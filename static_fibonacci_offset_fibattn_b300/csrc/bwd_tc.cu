@@ -1033,6 +1033,14 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                     const float* L = side_ptr(cseq) + 32 * h;
                     const float* Dd = L + kChunk;
                     const int32_t dist0 = qb - j;
+                    // bit c: query qb + c is this key row's (0 <= qb + c - j < W, qb + c < T)
+                    uint32_t okm = 0u;
+                    if (row_ok) {
+                        const int32_t lo = max(0, -dist0);
+                        const int32_t hi = min(32, min(W - dist0, T - qb));
+                        if (hi > lo)
+                            okm = (hi == 32 ? 0xffffffffu : (1u << hi) - 1u) & ~((1u << lo) - 1u);
+                    }
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const uint32_t col = 32 * h + 16 * half;
@@ -1043,19 +1051,27 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dkdv_tc_kernel(const __grid_c
                             tmem_ld16(tmem + lane_base + kColP + col, dv);
                             tmem_ld_wait(sv, dv);
 #pragma unroll
-                            for (int e = 0; e < 16; e += 2) {
+                            for (int e = 0; e < 16; e += 4) {
                                 const int ee = 16 * half + e;
-                                const bool ok0 = row_ok && (uint32_t)(dist0 + ee) < (uint32_t)W && qb + ee < T;
-                                const bool ok1 = row_ok && (uint32_t)(dist0 + ee + 1) < (uint32_t)W && qb + ee + 1 < T;
-                                const float p0 = ok0 ? ex2(__uint_as_float(sv[e]) * sl2 - L[ee]) : 0.f;
-                                const float p1 = ok1 ? ex2(__uint_as_float(sv[e + 1]) * sl2 - L[ee + 1]) : 0.f;
-                                pp[e >> 1] = pack_bf16x2(p0, p1);
-                                // selects, not products with p = 0: for a query column at or
-                                // past T, Dd holds bytes this call never wrote (pad rows of the
-                                // workspace, or slot memory past the side copy), possibly
-                                // non-finite, and 0 * NaN would reach dK through the MMA
-                                pd[e >> 1] = pack_bf16x2(ok0 ? p0 * (__uint_as_float(dv[e]) - Dd[ee]) : 0.f,
-                                                         ok1 ? p1 * (__uint_as_float(dv[e + 1]) - Dd[ee + 1]) : 0.f);
+                                const float4 l4 = *reinterpret_cast<const float4*>(L + ee);
+                                const float4 d4 = *reinterpret_cast<const float4*>(Dd + ee);
+                                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                                const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+                                float pv[4], ds[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const bool ok = (okm >> (ee + u)) & 1u;
+                                    pv[u] = ok ? ex2(__uint_as_float(sv[e + u]) * sl2 - lv[u]) : 0.f;
+                                    // selects, not products with p = 0: for a query column at or
+                                    // past T, Dd holds bytes this call never wrote (pad rows of
+                                    // the workspace, or slot memory past the side copy), possibly
+                                    // non-finite, and 0 * NaN would reach dK through the MMA
+                                    ds[u] = ok ? pv[u] * (__uint_as_float(dv[e + u]) - dd[u]) : 0.f;
+                                }
+                                pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                                pp[(e >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+                                pd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                                pd[(e >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
                             }
                         } else {
 #pragma unroll
