@@ -435,10 +435,12 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_tc_kernel(const __grid_con
                 }
                 if (need) {
                     const int32_t dj = d0 - 32 * hh;
+                    // bit e: key kb + 32 hh + e is in this query's window
+                    const uint32_t okm = row_ok ? window_bits(dj, W) : 0u;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const bool ok0 = row_ok && (uint32_t)(dj - e) < (uint32_t)W;
-                        const bool ok1 = row_ok && (uint32_t)(dj - e - 1) < (uint32_t)W;
+                        const bool ok0 = (okm >> e) & 1u;
+                        const bool ok1 = (okm >> (e + 1)) & 1u;
                         const float p0 = ok0 ? ex2(__uint_as_float(sv[e]) * sl2 - lse2) : 0.f;
                         const float p1 = ok1 ? ex2(__uint_as_float(sv[e + 1]) * sl2 - lse2) : 0.f;
                         pk[hh][e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - D),

@@ -354,6 +354,15 @@ __device__ __forceinline__ void axpy2_bf16(uint32_t p, uint32_t v, float& c0, fl
         : "r"(p), "r"(v));
 }
 
+// Bit e (0 <= e < 32) set when 0 <= d - e < W: the keys of a 32-column chunk that lie in a
+// query's window of W keys, d being the query's distance to the chunk's first key. Built once
+// per chunk, it replaces a compare per element.
+__device__ __forceinline__ uint32_t window_bits(int32_t d, int32_t W) {
+    const int32_t lo = max(0, d - W + 1), hi = min(32, d + 1);
+    if (hi <= lo) return 0u;
+    return (hi == 32 ? 0xffffffffu : (1u << hi) - 1u) & ~((1u << lo) - 1u);
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
