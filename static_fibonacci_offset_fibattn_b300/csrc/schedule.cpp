@@ -133,10 +133,13 @@ fibattn_status build_frac_table(int32_t base, int64_t base_max, float alpha, int
     };
     if (fib) {
         const int64_t fmax = base_max > 0 ? base_max : 987;
-        for (int64_t f = 1, g = 2; f <= fmax;) {
-            if (a * (double)f > (double)T - 1) break;  // d grows with F: nothing further fits
-            keep(a * (double)f, f);
-            const int64_t h = f + g;
+        // The pair is carried in 128 bits: a tiny alpha keeps alpha * F below T - 1 for every
+        // F up to fmax (at most 2^63 - 1), and the next term must not overflow on the way.
+        for (i128 f = 1, g = 2; f <= (i128)fmax;) {
+            const int64_t f64 = (int64_t)f;  // f <= fmax fits
+            if (a * (double)f64 > (double)T - 1) break;  // d grows with F: nothing further fits
+            keep(a * (double)f64, f64);
+            const i128 h = f + g;
             f = g;
             g = h;
         }

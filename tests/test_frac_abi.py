@@ -35,6 +35,20 @@ def test_frac_tables_match_oracle(base, WT):
 
 
 @pytest.mark.parametrize("base", [S.FIB, S.POW2])
+@pytest.mark.parametrize("WT", [(16, 1 << 30), (1, 100000), (64, 2 ** 31 - 1)])
+def test_frac_table_of_a_tiny_alpha_over_an_uncapped_base(base, WT):
+    # alpha * F stays below T - 1 for every base value up to 2^63 - 1: the builder visits them
+    # all and stops at the cap, without overflowing the next term (it used to loop forever)
+    W, T = WT
+    a, base_max = float(np.float32(1e-12)), 2 ** 63 - 1
+    want = oracle.frac_distances(a, base, W, T, base_max)
+    c, w = fa.frac_offsets(a, W, T, base, base_max)
+    assert len(want) > 10
+    assert c == [math.ceil(d) for d in want]
+    assert w == [float(np.float32(math.ceil(d) - d)) for d in want]
+
+
+@pytest.mark.parametrize("base", [S.FIB, S.POW2])
 def test_integer_alpha_gives_static_table(base):
     for a in (1, 2, 3, 5):
         for W, T in ((16, 256), (64, 1024), (2, 5000)):
