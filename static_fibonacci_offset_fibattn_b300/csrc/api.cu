@@ -573,7 +573,8 @@ fibattn_status fibattn_rope(const void* x, void* y, int64_t slices, int32_t T, i
     if (!x || !y || !table || !aligned16(x) || !aligned16(y) || !aligned16(table))
         return FIBATTN_ERR_INVALID_ARG;
     if (table_rows < T) return FIBATTN_ERR_INVALID_ARG;
-    if (slices < 1 || T < 1 || slices * (int64_t)T > ((int64_t)1 << 40)) return FIBATTN_ERR_INVALID_ARG;
+    // slices * T <= 2^40, tested without forming a product that could overflow
+    if (slices < 1 || T < 1 || slices > (((int64_t)1 << 40) / T)) return FIBATTN_ERR_INVALID_ARG;
     if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
     if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
     const int64_t bytes = slices * (int64_t)T * d * (int64_t)elt_size(dtype);

@@ -253,6 +253,9 @@ def test_rope_entry_points_validate_before_launch():
     assert L.fibattn_rope(ok, ctypes.c_void_p(256 + 128), 1, 8, 64, 1, ok, 8, 0, None) == fa.INVALID_ARG
     assert L.fibattn_rope(ctypes.c_void_p(264), ok, 1, 8, 64, 1, ok, 8, 0, None) == fa.INVALID_ARG
     assert L.fibattn_rope(ok, ok, 1, 8, 64, 3, ok, 8, 0, None) == fa.UNSUPPORTED
+    # more than 2^40 rows, also where slices * T would wrap around in 64 bits
+    assert L.fibattn_rope(ok, ok, (1 << 38) + 1, 4, 64, 1, ok, 8, 0, None) == fa.INVALID_ARG
+    assert L.fibattn_rope(ok, ok, (1 << 62) + 1, 4, 64, 1, ok, 8, 0, None) == fa.INVALID_ARG
     assert L.fibattn_fwd_rope(*([ok] * 7), 1, 4, 2, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 7,
                               None) == fa.INVALID_ARG
     assert L.fibattn_fwd_rope(*([ok] * 7), 1, 4, 3, 8, 64, 1, 4, 0.0, ctypes.byref(sc), 0, 1, ok, 8,
