@@ -28,6 +28,10 @@
  *   - d (head size) is 64, or 128 for the static and grouped-query forward and backward
  *     (the fractional-offset and RoPE calls take 64); dtype FIBATTN_F32 or FIBATTN_BF16, the
  *     same for every q/k/v/o/dO/dq/dk/dv tensor of a call.
+ *   - T (sequence length) is in [1, FIBATTN_T_MAX] for every call that launches work, so
+ *     that tile counts, padded row counts and row coordinates stay in 32 bits; a larger T
+ *     returns FIBATTN_ERR_INVALID_ARG. The host table calls (fibattn_offsets,
+ *     fibattn_frac_offsets) take any T >= 1.
  */
 #ifndef FIBATTN_H
 #define FIBATTN_H
@@ -63,6 +67,7 @@ typedef enum { FIBATTN_F32 = 0, FIBATTN_BF16 = 1 } fibattn_dtype;
 typedef struct { int32_t num, den; } fibattn_ratio;
 #define FIBATTN_RATIO_MAX (1 << 20)
 #define FIBATTN_LAYERS_MAX (1 << 20)
+#define FIBATTN_T_MAX (1 << 30)
 
 /*
  * A per-layer alpha schedule (Metodologia / Variaveis Experimentais):

@@ -18,7 +18,7 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 fibattn_status check_common(int32_t B, int32_t H, int32_t T, int32_t d, int32_t dtype, int32_t W,
                             const fibattn_schedule* sched, int32_t layer0, int32_t n_layers_call) {
     if (!sched) return FIBATTN_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || T < 1 || W < 1 || n_layers_call < 1 || layer0 < 0)
+    if (B < 1 || H < 1 || T < 1 || T > FIBATTN_T_MAX || W < 1 || n_layers_call < 1 || layer0 < 0)
         return FIBATTN_ERR_INVALID_ARG;
     if (sched->n_layers < 1 || (int64_t)layer0 + n_layers_call > sched->n_layers)
         return FIBATTN_ERR_INVALID_ARG;
@@ -100,7 +100,8 @@ fibattn_status check_frac(int32_t B, int32_t H, int32_t T, int32_t d, int32_t dt
                           int32_t base, int64_t base_max, const float* alphas,
                           int32_t n_layers_call, int32_t* n_max) {
     if (!alphas) return FIBATTN_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || T < 1 || W < 1 || n_layers_call < 1 || n_layers_call > FIBATTN_LAYERS_MAX)
+    if (B < 1 || H < 1 || T < 1 || T > FIBATTN_T_MAX || W < 1 || n_layers_call < 1 ||
+        n_layers_call > FIBATTN_LAYERS_MAX)
         return FIBATTN_ERR_INVALID_ARG;
     if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
     if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
@@ -154,7 +155,7 @@ fibattn_status fibattn_offsets_device(const fibattn_schedule* sched, int32_t lay
                                       int32_t* d_tables, int32_t* d_counts, void* cuda_stream) {
     if (!sched || !d_tables || !d_counts || n_layers_call < 1 || layer0 < 0)
         return FIBATTN_ERR_INVALID_ARG;
-    if (W < 1 || T < 1) return FIBATTN_ERR_INVALID_ARG;
+    if (W < 1 || T < 1 || T > FIBATTN_T_MAX) return FIBATTN_ERR_INVALID_ARG;
     if ((int64_t)layer0 + n_layers_call > sched->n_layers) return FIBATTN_ERR_INVALID_ARG;
     for (int32_t c = 0; c < n_layers_call; ++c) {  // same validation and capacity as the host
         Alpha a;
@@ -171,7 +172,7 @@ fibattn_status fibattn_offsets_device(const fibattn_schedule* sched, int32_t lay
 fibattn_status fibattn_keyset_debug(const fibattn_schedule* sched, int32_t layer, int32_t W,
                                     int32_t T, uint32_t* d_mask, void* cuda_stream) {
     if (!sched || !d_mask) return FIBATTN_ERR_INVALID_ARG;
-    if (W < 1 || T < 1) return FIBATTN_ERR_INVALID_ARG;
+    if (W < 1 || T < 1 || T > FIBATTN_T_MAX) return FIBATTN_ERR_INVALID_ARG;
     OffsetTables t;
     fibattn_status st = build_launch_tables(sched, layer, 1, W, T, &t);
     if (st != FIBATTN_OK) return st;
@@ -561,7 +562,8 @@ fibattn_status fibattn_bwd_frac(const void* q, const void* k, const void* v, con
 
 fibattn_status fibattn_rope_table(float* table, int32_t T, int32_t d, double base,
                                   void* cuda_stream) {
-    if (!table || (reinterpret_cast<uintptr_t>(table) & 15u) != 0 || T < 1) return FIBATTN_ERR_INVALID_ARG;
+    if (!table || (reinterpret_cast<uintptr_t>(table) & 15u) != 0 || T < 1 || T > FIBATTN_T_MAX)
+        return FIBATTN_ERR_INVALID_ARG;
     if (!(base > 1.0) || !(base < 1e300)) return FIBATTN_ERR_INVALID_ARG;
     if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
     return launch_rope_table(table, T, base, as_stream(cuda_stream));
@@ -574,7 +576,8 @@ fibattn_status fibattn_rope(const void* x, void* y, int64_t slices, int32_t T, i
         return FIBATTN_ERR_INVALID_ARG;
     if (table_rows < T) return FIBATTN_ERR_INVALID_ARG;
     // slices * T <= 2^40, tested without forming a product that could overflow
-    if (slices < 1 || T < 1 || slices > (((int64_t)1 << 40) / T)) return FIBATTN_ERR_INVALID_ARG;
+    if (slices < 1 || T < 1 || T > FIBATTN_T_MAX || slices > (((int64_t)1 << 40) / T))
+        return FIBATTN_ERR_INVALID_ARG;
     if (dtype != FIBATTN_F32 && dtype != FIBATTN_BF16) return FIBATTN_ERR_UNSUPPORTED;
     if (d != 64) return FIBATTN_ERR_UNSUPPORTED;
     const int64_t bytes = slices * (int64_t)T * d * (int64_t)elt_size(dtype);

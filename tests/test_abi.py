@@ -142,6 +142,36 @@ def test_fwd_validates_before_launch():
                          None) == fa.INVALID_ARG
 
 
+def _header_define(name):
+    text = open(os.path.join(ROOT, "include", "fibattn.h")).read()
+    m = re.search(r"#define\s+" + name + r"\s+\(1 << (\d+)\)", text)
+    return 1 << int(m.group(1))
+
+
+def test_sequence_length_limit():
+    # T above FIBATTN_T_MAX is rejected on the host by every call that launches work (tile
+    # and padded row counts of T + 127 or T + 31 would leave 32 bits); the host table call
+    # still takes any T
+    TM = _header_define("FIBATTN_T_MAX")
+    assert TM == 1 << 30
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    ok = ctypes.c_void_p(256)
+    for T in (TM + 1, 2 ** 31 - 1):
+        assert _fwd_raw(T=T) == fa.INVALID_ARG
+        n = ctypes.c_uint64(0)
+        assert L.fibattn_bwd_workspace_size(1, 1, T, 64, 1, 4, ctypes.byref(sc), 0, 1,
+                                            ctypes.byref(n)) == fa.INVALID_ARG
+        assert L.fibattn_keyset_debug(ctypes.byref(sc), 0, 4, T, ok, None) == fa.INVALID_ARG
+        assert L.fibattn_offsets_device(ctypes.byref(sc), 0, 1, 4, T, ok, ok, None) == fa.INVALID_ARG
+        assert L.fibattn_rope_table(ok, T, 64, ctypes.c_double(1e4), None) == fa.INVALID_ARG
+        assert L.fibattn_rope(ok, ok, 1, T, 64, 1, ok, T, 0, None) == fa.INVALID_ARG
+    buf = (ctypes.c_int32 * 64)()
+    cnt = ctypes.c_int32(0)
+    assert L.fibattn_offsets(ctypes.byref(sc), 0, 4, 2 ** 31 - 1, buf, 64, ctypes.byref(cnt)) == fa.OK
+    assert list(buf[: cnt.value]) == S.offset_table(S.FIB, Fraction(1), 4, 2 ** 31 - 1)
+
+
 def test_bwd_validates_before_launch():
     L = fa.lib()
     sc = fa.Schedule().to_c()

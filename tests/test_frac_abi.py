@@ -84,6 +84,7 @@ def _fwd_frac_raw(q=256, B=1, H=1, T=8, d=64, dtype=1, W=4, base=0, base_max=0, 
 
 def test_fwd_frac_validates_before_launch():
     assert _fwd_frac_raw(q=0) == fa.INVALID_ARG
+    assert _fwd_frac_raw(T=(1 << 30) + 1) == fa.INVALID_ARG  # above FIBATTN_T_MAX
     assert _fwd_frac_raw(q=264) == fa.INVALID_ARG          # misaligned
     assert _fwd_frac_raw(alphas=None, n=1) == fa.INVALID_ARG
     assert _fwd_frac_raw(B=0) == fa.INVALID_ARG
