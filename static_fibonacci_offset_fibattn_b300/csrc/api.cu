@@ -198,7 +198,7 @@ fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv, d};
+        AttnShape sh{(int64_t)B * H, T, W < T ? W : T, scale, n, H / H_kv, d};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t koff = (size_t)c * per_layer_kv * d * es;
         const char* qc = (const char*)q + off;
@@ -253,7 +253,7 @@ fibattn_status fibattn_fwd_frac(const void* q, const void* k, const void* v, voi
         FracTables t;
         fibattn_status st = build_frac_launch_tables(base, base_max, alphas + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        AttnShape sh{(int64_t)B * H, T, W < T ? W : T, scale, n};
         const size_t off = (size_t)c * per_layer * d * es;
         const char* qc = (const char*)q + off;
         const char* kc = (const char*)k + off;
@@ -313,7 +313,7 @@ fibattn_status bwd_common(const void* q, const void* k, const void* v, const voi
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv, d};
+        AttnShape sh{(int64_t)B * H, T, W < T ? W : T, scale, n, H / H_kv, d};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t koff = (size_t)c * per_layer_kv * d * es;
         const size_t loff = (size_t)c * per_layer;
@@ -397,7 +397,7 @@ fibattn_status fibattn_fwd_rope_fused(const void* q, const void* k, const void* 
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n, H / H_kv, d};
+        AttnShape sh{(int64_t)B * H, T, W < T ? W : T, scale, n, H / H_kv, d};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t koff = (size_t)c * per_layer_kv * d * es;
         st = launch_fwd_rope_tc_bf16((const char*)q + off, (const char*)k + koff,
@@ -473,7 +473,7 @@ fibattn_status fibattn_bwd_fused(const void* q, const void* k, const void* v, co
         OffsetTables t;
         st = build_launch_tables(sched, layer0 + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n, 1, d};
+        AttnShape sh{(int64_t)B * H, T, W < T ? W : T, scale, n, 1, d};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t poff = (size_t)c * per_layer_pad;
         st = launch_bwd_fused_tc_bf16((const char*)q + off, (const char*)k + off,
@@ -532,7 +532,7 @@ fibattn_status fibattn_bwd_frac(const void* q, const void* k, const void* v, con
         FracTables t;
         st = build_frac_launch_tables(base, base_max, alphas + c, n, W, T, &t);
         if (st != FIBATTN_OK) return st;
-        AttnShape sh{(int64_t)B * H, T, W, scale, n};
+        AttnShape sh{(int64_t)B * H, T, W < T ? W : T, scale, n};
         const size_t off = (size_t)c * per_layer * d * es;
         const size_t loff = (size_t)c * per_layer;
         if (dtype == FIBATTN_F32) {

@@ -89,7 +89,9 @@ fibattn_status launch_keyset(const OffsetTables& t, int32_t W, int32_t T, uint32
 struct AttnShape {
     int64_t slices_per_layer;  // B * H (query heads)
     int32_t T;
-    int32_t W;
+    int32_t W;                 // the window, clamped to T by every caller: a window of T keys
+                               // already holds every causal key, and W + j or d - W in the
+                               // kernels' 32-bit row arithmetic cannot overflow
     float scale;
     int32_t n_layers;          // layers in this launch
     int32_t group = 1;         // query heads per kv head: K/V (and dK/dV) have

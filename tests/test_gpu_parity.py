@@ -311,6 +311,26 @@ def test_bwd_edge_cases(dtype, case):
             assert_grad(n, f64(got[l, b, h]), want, dtype, (b, h))
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 128)])
+def test_window_at_the_int32_limit_equals_a_window_of_T(dtype, d):
+    # a window of T keys already holds every causal key, so W = 2^31 - 1 must give the same
+    # forward and backward, bit for bit (the window is clamped to T before the kernels' 32-bit
+    # row arithmetic sees it)
+    T = 300
+    inp = to_dev(fi.draw((1, 1, 2, T, d), seed=41, scale=0.5, dtype=dtype,
+                         names=("q", "k", "v", "dO")))
+    sc = lib_schedule(SCHEDS[2])
+    outs = []
+    for W in (T, 2 ** 31 - 1):
+        o, lse = fa.fwd(inp["q"], inp["k"], inp["v"], W, sc, layer0=15)
+        grads = fa.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["dO"], W, sc, layer0=15)
+        outs.append((o, lse) + tuple(grads))
+    torch.cuda.synchronize()
+    fa.poll_device_error()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
 def test_autograd_wrapper_matches_bwd():
     inp = to_dev(fi.draw((1, 2, 1, 300, 64), seed=31, scale=0.25, dtype="bf16",
                          names=("q", "k", "v", "dO")))
