@@ -125,7 +125,7 @@ FIBATTN_API fibattn_status fibattn_offsets_device(const fibattn_schedule* sched,
  *             the pages apply it before the gather).
  *   o       : [Lc][B][H][T][d] device, written, same dtype.
  *   lse     : [Lc][B][H][T] float32 device, written: log sum_j exp(scale * q_i.k_j).
- *   scale   : <= 0 selects 1/sqrt(d).
+ *   scale   : <= 0 or NaN selects 1/sqrt(d); +inf returns FIBATTN_ERR_INVALID_ARG.
  *   W >= 1 (W >= T gives dense causal attention). bf16 runs on the tcgen05 tensor-core
  *   kernel (d = 128: two CTAs per 128-query tile, one per half of the output columns; d = 64
  *   with W >= T: a dense causal kernel over 128 x 128 score blocks); f32 on the SIMT fp32

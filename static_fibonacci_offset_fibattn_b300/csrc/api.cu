@@ -40,6 +40,14 @@ fibattn_status check_common(int32_t B, int32_t H, int32_t T, int32_t d, int32_t 
 
 size_t elt_size(int32_t dtype) { return dtype == FIBATTN_F32 ? 4 : 2; }
 
+// The softmax scale: <= 0 or NaN selects 1/sqrt(d); +inf is refused (every score would be
+// infinite).
+bool resolve_scale(float& scale, int32_t d) {
+    if (scale == INFINITY) return false;
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    return true;
+}
+
 // Layout of the backward workspace. f32 path: D [rows] (rows of T). bf16 path: rows padded to
 // T_pad = T rounded up to 4 (16-byte rows for bulk copies): D [rows_pad], lse*log2(e)
 // [rows_pad], then the (P, dS) pairs [slices][n_max][T_pad]; each array starts 256-aligned.
@@ -189,7 +197,7 @@ fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void
     if (H_kv < 1 || H < 1 || H % H_kv != 0) return FIBATTN_ERR_INVALID_ARG;
     fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (st != FIBATTN_OK) return st;
-    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const int64_t per_layer = (int64_t)B * H * T;
     const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
@@ -246,7 +254,7 @@ fibattn_status fibattn_fwd_frac(const void* q, const void* k, const void* v, voi
     fibattn_status st0 = check_frac(B, H, T, d, dtype, W, base, base_max, alphas, n_layers_call, nullptr);
     if (st0 != FIBATTN_OK) return st0;
     const int64_t per_layer = (int64_t)B * H * T;
-    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const size_t es = elt_size(dtype);
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
@@ -304,7 +312,7 @@ fibattn_status bwd_common(const void* q, const void* k, const void* v, const voi
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2_offset);
     uint32_t* pds = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.pds_offset);
     const int64_t per_layer_pad = (int64_t)B * H * ws.T_pad;
-    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const int64_t per_layer = (int64_t)B * H * T;
     const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
@@ -388,7 +396,7 @@ fibattn_status fibattn_fwd_rope_fused(const void* q, const void* k, const void* 
     fibattn_status st = check_common(B, H, T, d, dtype, W, sched, layer0, n_layers_call);
     if (st != FIBATTN_OK) return st;
     if (dtype != FIBATTN_BF16 || d != 64) return FIBATTN_ERR_UNSUPPORTED;
-    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const int64_t per_layer = (int64_t)B * H * T;
     const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
@@ -465,7 +473,7 @@ fibattn_status fibattn_bwd_fused(const void* q, const void* k, const void* v, co
     float* delta = static_cast<float*>(workspace);
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2_offset);
     const int64_t per_layer_pad = (int64_t)B * H * ws.T_pad;
-    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const int64_t per_layer = (int64_t)B * H * T;
     const size_t es = elt_size(dtype);
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
@@ -520,7 +528,7 @@ fibattn_status fibattn_bwd_frac(const void* q, const void* k, const void* v, con
     float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2_offset);
     uint32_t* pds = reinterpret_cast<uint32_t*>(wsb + ws.pds_offset);
     float* galpha = reinterpret_cast<float*>(wsb + ws.galpha_offset);
-    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const int64_t per_layer = (int64_t)B * H * T;
     const int64_t per_layer_pad = (int64_t)B * H * ws.T_pad;
     // dalpha partials per layer: one per query (f32) or one per 128-query tile (bf16)

@@ -140,6 +140,9 @@ def test_fwd_validates_before_launch():
                          None) == fa.INVALID_ARG
     assert L.fibattn_fwd(ok, ok, ok, ok, ok, 1, 1, 8, 64, 1, 4, 0.0, None, 0, 1,
                          None) == fa.INVALID_ARG
+    # an infinite softmax scale is refused (<= 0 and NaN select 1/sqrt(d))
+    assert L.fibattn_fwd(ok, ok, ok, ok, ok, 1, 1, 8, 64, 1, 4, float("inf"), ctypes.byref(sc),
+                         0, 1, None) == fa.INVALID_ARG
 
 
 def _header_define(name):
