@@ -250,6 +250,13 @@ def _check_tensors(ref: torch.Tensor, *ts):
             raise ValueError("tensors must be contiguous")
 
 
+def _check_lse(lse: torch.Tensor, q: torch.Tensor):
+    # lse is written by the forwards and read by the backwards: one float32 per query row
+    if (lse.dtype != torch.float32 or lse.device != q.device
+            or tuple(lse.shape) != tuple(q.shape[:-1]) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 tensor shaped q.shape[:-1] on q's device")
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, sched: Schedule,
         layer0: int = 0, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
         lse: Optional[torch.Tensor] = None):
@@ -265,6 +272,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, sched: Schedu
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     s = sched.to_c()
+    _check_lse(lse, q)
     st = lib().fibattn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, T, d,
                                _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s), layer0,
                                Lc, _stream(q))
@@ -295,6 +303,7 @@ def fwd_frac(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, W: int, alphas: 
     _check_tensors(q, k, v, o)
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    _check_lse(lse, q)
     st = lib().fibattn_fwd_frac(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, d,
                                 _DTYPES[q.dtype], W, float(scale or 0.0), _BASES[base],
                                 int(base_max), a, Lc, _stream(q))
@@ -341,6 +350,7 @@ def bwd_frac(q, k, v, o, lse, dO, W: int, alphas: Sequence[float], base: str = "
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if workspace.device != q.device or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on q's device")
+    _check_lse(lse, q)
     st = lib().fibattn_bwd_frac(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                                 _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), B, H, T, d,
@@ -383,6 +393,7 @@ def bwd(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
     if workspace.device != q.device or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on q's device")
     s = sched.to_c()
+    _check_lse(lse, q)
     st = lib().fibattn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                                _ptr(dk), _ptr(dv), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), B, H, Hkv, T, d,
@@ -416,6 +427,7 @@ def bwd_fused(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
     if workspace.device != q.device or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on q's device")
     s = sched.to_c()
+    _check_lse(lse, q)
     st = lib().fibattn_bwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), B, H, T, d,
@@ -458,14 +470,13 @@ def fwd_bwd(q, k, v, dO, W: int, sched: Schedule, layer0: int = 0, n_streams: in
     _check_tensors(k, v, dk, dv)
     if k.dtype != q.dtype or k.device != q.device:
         raise ValueError("q/k/v must share device and dtype")
-    if lse.dtype != torch.float32 or lse.device != q.device or tuple(lse.shape) != tuple(q.shape[:-1]):
-        raise ValueError("lse must be float32 [..., T] on q's device")
     need = fwd_bwd_workspace_size(q, W, sched, layer0, n_streams)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if workspace.device != q.device or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on q's device")
     s = sched.to_c()
+    _check_lse(lse, q)
     st = lib().fibattn_fwd_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(o), _ptr(lse), _ptr(dq),
                                _ptr(dk), _ptr(dv), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), B, H, Hkv, T, d,
@@ -489,6 +500,7 @@ def bwd_noalloc(q, k, v, o, lse, dO, W: int, sched: Schedule, layer0: int = 0,
     dv = torch.empty_like(q) if dv is None else dv
     _check_tensors(q, k, v, o, dO, dq, dk, dv)
     s = sched.to_c()
+    _check_lse(lse, q)
     st = lib().fibattn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, T, d, _DTYPES[q.dtype], W,
                                    float(scale or 0.0), ctypes.byref(s), layer0, Lc, _stream(q))
@@ -605,6 +617,7 @@ def fwd_rope(q, k, v, W: int, sched: Schedule, table: torch.Tensor, layer0: int 
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     s = sched.to_c()
+    _check_lse(lse, q)
     st = lib().fibattn_fwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(o), _ptr(lse),
                                 B, H, Hkv, T, d, _DTYPES[q.dtype], W, float(scale or 0.0),
                                 ctypes.byref(s), layer0, Lc, _ptr(table), table.shape[0],
@@ -629,6 +642,7 @@ def fwd_rope_fused(q, k, v, W: int, sched: Schedule, table: torch.Tensor, layer0
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     s = sched.to_c()
+    _check_lse(lse, q)
     st = lib().fibattn_fwd_rope_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, T,
                                       d, _DTYPES[q.dtype], W, float(scale or 0.0), ctypes.byref(s),
                                       layer0, Lc, _ptr(table), table.shape[0], _stream(q))
@@ -653,6 +667,7 @@ def bwd_rope(q_rot, k_rot, v, o, lse, dO, W: int, sched: Schedule, table: torch.
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_rot.device)
     s = sched.to_c()
+    _check_lse(lse, q_rot)
     st = lib().fibattn_bwd_rope(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), B, H, Hkv, T, d,

@@ -274,6 +274,17 @@ def test_binding_checks_kv_head_shapes():
                torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16), 4, fa.Schedule())
 
 
+def test_binding_checks_lse():
+    # a caller-given lse must be float32, shaped q.shape[:-1], contiguous, on q's device:
+    # otherwise the forward would write (or the backward read) past its end
+    q = torch.empty(2, 3, 8, 64)
+    fa._check_lse(torch.empty(2, 3, 8), q)
+    for bad in (torch.empty(2, 3, 8, dtype=torch.bfloat16), torch.empty(2, 3, 7),
+                torch.empty(2, 3, 16)[:, :, ::2], torch.empty(6, 8), torch.empty(2, 3, 8, 1)):
+        with pytest.raises(ValueError):
+            fa._check_lse(bad, q)
+
+
 def test_rope_entry_points_validate_before_launch():
     L = fa.lib()
     sc = fa.Schedule().to_c()
