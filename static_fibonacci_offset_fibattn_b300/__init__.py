@@ -343,8 +343,9 @@ def bwd_frac(q, k, v, o, lse, dO, W: int, alphas: Sequence[float], base: str = "
     _check_tensors(q, k, v, o, dO, dq, dk, dv)
     if dalpha is None:
         dalpha = torch.empty(Lc, dtype=torch.float32, device=q.device)
-    if dalpha.device != q.device or dalpha.dtype != torch.float32 or dalpha.numel() != Lc:
-        raise ValueError("dalpha must be a float32 [Lc] tensor on q's device")
+    if (dalpha.device != q.device or dalpha.dtype != torch.float32 or dalpha.numel() != Lc
+            or not dalpha.is_contiguous()):
+        raise ValueError("dalpha must be a contiguous float32 [Lc] tensor on q's device")
     need = bwd_frac_workspace_size(q, W, alphas, base, base_max)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -666,6 +667,8 @@ def bwd_rope(q_rot, k_rot, v, o, lse, dO, W: int, sched: Schedule, table: torch.
     need = bwd_workspace_size(q_rot, W, sched, layer0)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_rot.device)
+    if workspace.device != q_rot.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on q's device")
     s = sched.to_c()
     _check_lse(lse, q_rot)
     st = lib().fibattn_bwd_rope(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
