@@ -4,6 +4,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <initializer_list>
+
 #include "internal.h"
 
 using namespace fibattn;
@@ -11,6 +13,29 @@ using namespace fibattn;
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A buffer of a call: its first byte and its length in bytes.
+struct Span {
+    const void* p;
+    uint64_t n;
+};
+
+bool spans_overlap(Span a, Span b) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a.p), pb = reinterpret_cast<uintptr_t>(b.p);
+    return a.n > 0 && b.n > 0 && pa < pb + b.n && pb < pa + a.n;
+}
+
+// True when an output overlaps another output or an input. Inputs may share memory (k == v):
+// they are only read.
+bool outputs_overlap(std::initializer_list<Span> outs, std::initializer_list<Span> ins) {
+    for (const Span* a = outs.begin(); a != outs.end(); ++a) {
+        for (const Span* b = a + 1; b != outs.end(); ++b)
+            if (spans_overlap(*a, *b)) return true;
+        for (const Span& b : ins)
+            if (spans_overlap(*a, b)) return true;
+    }
+    return false;
+}
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -201,6 +226,11 @@ fibattn_status fibattn_fwd_gqa(const void* q, const void* k, const void* v, void
     const int64_t per_layer = (int64_t)B * H * T;
     const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
+    const uint64_t qb = (uint64_t)n_layers_call * per_layer * d * es;
+    const uint64_t kb = (uint64_t)n_layers_call * per_layer_kv * d * es;
+    const uint64_t lb = (uint64_t)n_layers_call * per_layer * 4;
+    if (outputs_overlap({{o, qb}, {lse, lb}}, {{q, qb}, {k, kb}, {v, kb}}))
+        return FIBATTN_ERR_INVALID_ARG;
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
         OffsetTables t;
@@ -256,6 +286,10 @@ fibattn_status fibattn_fwd_frac(const void* q, const void* k, const void* v, voi
     const int64_t per_layer = (int64_t)B * H * T;
     if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const size_t es = elt_size(dtype);
+    const uint64_t qb = (uint64_t)n_layers_call * per_layer * d * es;
+    if (outputs_overlap({{o, qb}, {lse, (uint64_t)n_layers_call * per_layer * 4}},
+                        {{q, qb}, {k, qb}, {v, qb}}))
+        return FIBATTN_ERR_INVALID_ARG;
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
         FracTables t;
@@ -316,6 +350,14 @@ fibattn_status bwd_common(const void* q, const void* k, const void* v, const voi
     const int64_t per_layer = (int64_t)B * H * T;
     const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
+    {
+        const uint64_t qb = (uint64_t)n_layers_call * per_layer * d * es;
+        const uint64_t kb = (uint64_t)n_layers_call * per_layer_kv * d * es;
+        const uint64_t lb = (uint64_t)n_layers_call * per_layer * 4;
+        if (outputs_overlap({{dq, qb}, {dk, kb}, {dv, kb}, {workspace, ws.total}},
+                            {{q, qb}, {k, kb}, {v, kb}, {o, qb}, {lse, lb}, {dO, qb}}))
+            return FIBATTN_ERR_INVALID_ARG;
+    }
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
         OffsetTables t;
@@ -400,6 +442,13 @@ fibattn_status fibattn_fwd_rope_fused(const void* q, const void* k, const void* 
     const int64_t per_layer = (int64_t)B * H * T;
     const int64_t per_layer_kv = (int64_t)B * H_kv * T;
     const size_t es = elt_size(dtype);
+    {
+        const uint64_t qb = (uint64_t)n_layers_call * per_layer * d * es;
+        const uint64_t kb = (uint64_t)n_layers_call * per_layer_kv * d * es;
+        if (outputs_overlap({{o, qb}, {lse, (uint64_t)n_layers_call * per_layer * 4}},
+                            {{q, qb}, {k, kb}, {v, kb}, {rope_table, (uint64_t)table_rows * 256}}))
+            return FIBATTN_ERR_INVALID_ARG;
+    }
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
         OffsetTables t;
@@ -476,6 +525,13 @@ fibattn_status fibattn_bwd_fused(const void* q, const void* k, const void* v, co
     if (!resolve_scale(scale, d)) return FIBATTN_ERR_INVALID_ARG;
     const int64_t per_layer = (int64_t)B * H * T;
     const size_t es = elt_size(dtype);
+    {
+        const uint64_t qb = (uint64_t)n_layers_call * per_layer * d * es;
+        const uint64_t lb = (uint64_t)n_layers_call * per_layer * 4;
+        if (outputs_overlap({{dq, qb}, {dk, qb}, {dv, qb}, {workspace, ws.total}},
+                            {{q, qb}, {k, qb}, {v, qb}, {o, qb}, {lse, lb}, {dO, qb}}))
+            return FIBATTN_ERR_INVALID_ARG;
+    }
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;
         OffsetTables t;
@@ -534,6 +590,14 @@ fibattn_status fibattn_bwd_frac(const void* q, const void* k, const void* v, con
     // dalpha partials per layer: one per query (f32) or one per 128-query tile (bf16)
     const int64_t parts = dtype == FIBATTN_F32 ? per_layer : (int64_t)B * H * ((T + 127) / 128);
     const size_t es = elt_size(dtype);
+    {
+        const uint64_t qb = (uint64_t)n_layers_call * per_layer * d * es;
+        const uint64_t lb = (uint64_t)n_layers_call * per_layer * 4;
+        if (outputs_overlap({{dq, qb}, {dk, qb}, {dv, qb}, {dalpha, (uint64_t)n_layers_call * 4},
+                             {workspace, ws.total}},
+                            {{q, qb}, {k, qb}, {v, qb}, {o, qb}, {lse, lb}, {dO, qb}}))
+            return FIBATTN_ERR_INVALID_ARG;
+    }
     cudaStream_t s = as_stream(cuda_stream);
     for (int32_t c = 0; c < n_layers_call; c += kMaxLayersPerLaunch) {
         const int32_t n = n_layers_call - c < kMaxLayersPerLaunch ? n_layers_call - c : kMaxLayersPerLaunch;

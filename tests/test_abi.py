@@ -274,6 +274,33 @@ def test_binding_checks_kv_head_shapes():
                torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16), 4, fa.Schedule())
 
 
+def test_outputs_must_not_overlap_inputs():
+    # every argument is valid except that an output shares bytes with an input or another
+    # output, so the overlap check is what rejects these calls, before any launch
+    L = fa.lib()
+    sc = fa.Schedule().to_c()
+    P = lambda mib, off=0: ctypes.c_void_p((mib << 20) + off)  # 1 MiB apart: disjoint here
+    B, H, T, d, W = 1, 1, 8, 64, 4                              # 1 KB per bf16 tensor
+    fwd = lambda q, k, v, o, lse: L.fibattn_fwd(q, k, v, o, lse, B, H, T, d, 1, W, 0.0,
+                                                 ctypes.byref(sc), 0, 1, None)
+    assert fwd(P(1), P(2), P(3), P(1), P(5)) == fa.INVALID_ARG          # o is q
+    assert fwd(P(1), P(2), P(3), P(4), P(4, 512)) == fa.INVALID_ARG     # lse inside o
+    assert fwd(P(1), P(2), P(3), P(3, 1008), P(5)) == fa.INVALID_ARG    # o's start in v
+    need = ctypes.c_uint64(0)
+    assert L.fibattn_bwd_workspace_size(B, H, T, d, 1, W, ctypes.byref(sc), 0, 1,
+                                        ctypes.byref(need)) == fa.OK
+    ws = ctypes.c_uint64(need.value)
+
+    def bwd(dq, dk, dv, wsp):
+        return L.fibattn_bwd(P(1), P(2), P(3), P(4), P(5), P(6), dq, dk, dv, wsp, ws, B, H, T, d,
+                             1, W, 0.0, ctypes.byref(sc), 0, 1, None)
+
+    assert bwd(P(7), P(2), P(9), P(10)) == fa.INVALID_ARG    # dk is k
+    assert bwd(P(7), P(8), P(8), P(10)) == fa.INVALID_ARG    # dk is dv
+    assert bwd(P(7), P(8), P(9), P(7)) == fa.INVALID_ARG     # the workspace over dq
+    assert bwd(P(6), P(8), P(9), P(10)) == fa.INVALID_ARG    # dq over dO
+
+
 def test_binding_checks_lse():
     # a caller-given lse must be float32, shaped q.shape[:-1], contiguous, on q's device:
     # otherwise the forward would write (or the backward read) past its end
