@@ -20,7 +20,8 @@
  *     fibattn_bwd_noalloc (both static). Device pointers must be 16-byte aligned.
  *   - No output (o, lse, dq, dk, dv, dalpha, the workspace) may share a byte with another
  *     output or an input of the same attention call; inputs may share memory (k == v). The
- *     extents are compared on the host and an overlap returns FIBATTN_ERR_INVALID_ARG.
+ *     extents are compared on the host and an overlap returns FIBATTN_ERR_INVALID_ARG
+ *     (fibattn_fwd_bwd compares them within each layer group's forward and backward).
  *     fibattn_rope alone allows x == y (in place).
  *   - Work is enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default
  *     stream) and returns once launched; results are ready when the stream is.
